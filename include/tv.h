@@ -1,0 +1,224 @@
+/*
+ * tv.h -- C ABI of the GB300 tree verify round.
+ *
+ * One verify round of speculative decoding [Drafters and tree verify, §The
+ * round]: (2) one forward pass scores every node of a draft tree of at most 32
+ * nodes against the KV cache, (3) a walk accepts a root path, (4) the commit
+ * keeps only the accepted path's KV rows.  Every entry point is asynchronous
+ * on the given CUDA stream and runs hand-written sm_103a kernels; there is no
+ * CPU fallback.
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ * - bf16 values are passed as uint16_t bit patterns (tv_bf16).
+ * - "device" pointers point to memory the GPU can read/write (cudaMalloc'd or
+ *   torch CUDA tensors); "host" values are plain C values read during the call.
+ * - The caller owns every buffer.  The library allocates nothing: scratch
+ *   space is the caller's workspace, sized by tv_workspace_size().
+ * - A draft tree is a parent array in parent-before-child order: parent[0] = -1
+ *   (the root, the round's anchor token whose K/V this verify computes) and
+ *   0 <= parent[i] < i, with no two siblings carrying the same token
+ *   [Algorithm and correctness contract, §Target position and batching].
+ *   Depth-first pre-order [Drafters and tree verify, §Tree verify through
+ *   recurrent layers] is one such order; any parent-before-child order works.
+ * - Row i of a tree scores node i's children: it processes node i's token at
+ *   position ctx + depth(i) and attends to the cached context plus the
+ *   root-to-i path, i included.  Siblings therefore share the parent's row
+ *   [Algorithm and correctness contract, §Target position and batching].
+ * - Several requests may share one pass (joint verify [Exactness, §Parallel
+ *   requests]): their rows are concatenated in request order, at most 32 rows
+ *   in all; request r owns rows row_off(r) .. row_off(r) + n_r - 1 of every
+ *   per-row array, where row_off(r) = n_0 + ... + n_{r-1}.  Each request has
+ *   its own cache and sees only its own cache and its own ancestors.
+ *
+ * Errors
+ * ------
+ * Every entry point returns TV_OK (0) or a negative TV_E_* code.  Checks that
+ * need only host values happen before anything is launched; nothing is
+ * launched when one fails.  Checks that need device data (the tree arrays, the
+ * uniforms) run in the kernels, which then write the code into *dev_status.
+ * dev_status is sticky: kernels only ever change it from 0 to a code, and every
+ * kernel of every entry point does nothing while it is non-zero.  So a caller
+ * can chain verify -> accept -> commit with one status word, zeroed once per
+ * round, and read it after the round; a commit never runs on a bad path.
+ * Device waits are bounded: a wait that gives up writes TV_E_TIMEOUT.
+ */
+#ifndef TV_H
+#define TV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* the library is built with hidden visibility; these are its only exports */
+#if defined(__GNUC__)
+#define TV_API __attribute__((visibility("default")))
+#else
+#define TV_API
+#endif
+
+#define TV_OK              0
+#define TV_E_ARG          -1   /* a null pointer, a bad size or a bad dims field        */
+#define TV_E_ORDER        -2   /* parent[0] != -1 or parent[i] not in [0, i)            */
+#define TV_E_DUP_SIBLING  -3   /* two children of one node carry the same token         */
+#define TV_E_TOKEN        -4   /* a token id outside [0, vocab)                         */
+#define TV_E_CAPACITY     -5   /* ctx_len + n > capacity                                */
+#define TV_E_ROWS         -6   /* a tree outside 1..32 nodes, or more than 32 rows total */
+#define TV_E_UNIFORM      -7   /* a uniform that is not finite or not in [0, 1)         */
+#define TV_E_TEMP         -8   /* temperature not finite or <= 0                        */
+#define TV_E_WORKSPACE    -9   /* workspace null or smaller than tv_workspace_size()    */
+#define TV_E_CUDA        -10   /* a CUDA runtime call failed                            */
+#define TV_E_UNSUPPORTED -11   /* a shape these kernels do not handle (see tv_dims)     */
+#define TV_E_TIMEOUT     -12   /* a bounded device wait gave up                         */
+#define TV_E_PATH        -13   /* commit: accept_len or a path entry out of range       */
+
+typedef uint16_t tv_bf16;
+
+/* Shapes of the layer.  Supported: head_dim 64 or 128; hidden and
+ * n_q_heads*head_dim multiples of 64; n_q_heads a multiple of n_kv_heads;
+ * (n_q_heads / n_kv_heads) * (rows of one request) <= 160; vocab >= 2. */
+typedef struct tv_dims {
+  int32_t hidden, n_q_heads, n_kv_heads, head_dim, vocab;
+  float rope_theta;   /* RoPE base (rotate-half pairs (d, d + head_dim/2)) */
+  float rms_eps;      /* RMSNorm epsilon                                    */
+} tv_dims;
+
+/* The layer + head, all device pointers to bf16, row-major, caller-owned:
+ *   embed   [vocab][hidden]            token embedding
+ *   ln1     [hidden]                   RMSNorm gain before the projections
+ *   wqkv    [(Hq + 2 Hkv) D][hidden]   rows: the Q heads, then K heads, then V heads
+ *   wo      [hidden][Hq D]             output projection
+ *   ln_f    [hidden]                   final RMSNorm gain
+ *   lm_head [vocab][hidden]            output head                               */
+typedef struct tv_model {
+  const tv_bf16 *embed, *ln1, *wqkv, *wo, *ln_f, *lm_head;
+  tv_dims dims;
+} tv_model;
+
+/* One request's KV cache, device pointers to bf16, layout [Hkv][capacity][D].
+ * Slots [0, ctx_len) hold the cached context.  ctx_len and capacity are host
+ * values; the caller advances ctx_len after a commit (new_ctx). */
+typedef struct tv_kv {
+  tv_bf16 *k, *v;
+  int32_t ctx_len, capacity;
+} tv_kv;
+
+/* One request's draft tree: device int32 arrays of n entries; n is a host value. */
+typedef struct tv_tree {
+  const int32_t *parent, *token;
+  int32_t n;
+} tv_tree;
+
+/*
+ * Bytes of workspace that tv_verify_tree and tv_accept_residual need for any
+ * round of up to max_rows rows (<= 32) whose requests have ctx_len <= max_ctx.
+ * Host-only; writes *bytes.  Returns TV_E_ARG / TV_E_UNSUPPORTED on bad dims.
+ */
+TV_API int tv_workspace_size(const tv_dims *dims, int max_rows, int max_ctx, size_t *bytes);
+
+/*
+ * The verify pass [Drafters and tree verify, §The round, step 2; §Tree verify
+ * through recurrent layers]: one forward pass over every row of n_req trees.
+ *
+ *   model        host struct of device weight pointers
+ *   kv           host array [n_req]; verify writes row i's K/V into slot
+ *                ctx_len + i of its request's cache ("the cache holds every node
+ *                at its depth-first slot"); slots below ctx_len are only read
+ *   trees        host array [n_req]
+ *   logits       device fp32 [total_rows][vocab] -- the head's fp32 logits
+ *                [Exactness, §The one exception: near ties]
+ *   argmax       device int32 [total_rows] -- per row the index of the largest
+ *                logit, the lowest index among equal maxima
+ *   top2_gap     device fp32 [total_rows] -- largest minus second-largest logit
+ *                (0 when the maximum is attained twice)
+ *   attn_out     device bf16 [total_rows][Hq*D] or NULL -- attention output
+ *   workspace    device, >= tv_workspace_size(dims, total_rows, max ctx_len)
+ *   dev_status   device int32, sticky (see Errors)
+ *   stream       cudaStream_t (NULL = legacy default stream)
+ *
+ * Host checks: TV_E_ARG, TV_E_ROWS, TV_E_CAPACITY, TV_E_WORKSPACE,
+ * TV_E_UNSUPPORTED.  Device checks (-> *dev_status): TV_E_ORDER,
+ * TV_E_DUP_SIBLING, TV_E_TOKEN.  Every row's logits use one reduction order,
+ * fixed by the weight shapes and never by the row count, so a row's results do
+ * not depend on the other rows in the pass [Exactness, §Parallel requests].
+ */
+TV_API int tv_verify_tree(const tv_model *model, const tv_kv *kv, const tv_tree *trees, int n_req,
+                   float *logits, int32_t *argmax, float *top2_gap, tv_bf16 *attn_out,
+                   void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Greedy accept [Drafters and tree verify, §The round, step 3]: walk down from
+ * the root; at each node take the model's token (argmax of its row); move to
+ * the child that carries it; stop where no child does; keep the model's token
+ * at the stopping node too, so a round yields at least one token.
+ *
+ *   trees        host array [n_req]
+ *   argmax       device int32 [total_rows] (from tv_verify_tree)
+ *   path         device int32 [total_rows]: request r's accepted node indices,
+ *                root first, at path[row_off(r) .. row_off(r) + a_r]
+ *   accept_len   device int32 [n_req]: a_r = accepted non-root nodes
+ *   out_tokens   device int32 [total_rows]: the a_r accepted drafts then the
+ *                stopping node's token, a_r + 1 tokens at row_off(r)
+ *   dev_status   device int32, sticky.  Device checks: TV_E_ORDER,
+ *                TV_E_DUP_SIBLING.
+ */
+TV_API int tv_accept_greedy(const tv_tree *trees, int n_req, const int32_t *argmax,
+                     int32_t *path, int32_t *accept_len, int32_t *out_tokens,
+                     int32_t *dev_status, void *stream);
+
+/*
+ * Deterministic-candidate residual sampling [Algorithm and correctness
+ * contract, §Deterministic tree candidates and residual verification]: at the
+ * current node r := p = softmax(logits_row / temperature); its children are
+ * tried in increasing node index: accept candidate x iff u < r(x); on
+ * rejection remove x from r and renormalise; on acceptance follow that child.
+ * If every child fails, draw one token from the residual r, emit it, end.
+ * At a leaf the round ends; if bonus_at_leaf, one draw from p is emitted there
+ * (the target's own token at the stopping point, as the greedy walk keeps it).
+ * A draw y from r is the smallest y with sum_{j<=y} r(j) > u * sum(r).
+ *
+ *   logits       device fp32 [total_rows][vocab] (from tv_verify_tree)
+ *   uniforms     device fp32 [total_rows]: request r consumes
+ *                uniforms[row_off(r) ..] in order, one per candidate test and
+ *                one for the final draw (at most n_r draws)
+ *   path, accept_len  as tv_accept_greedy
+ *   out_tokens   device int32 [total_rows]; out_count device int32 [n_req]
+ *                holds how many tokens request r emitted (a_r or a_r + 1)
+ *   workspace    device, >= tv_workspace_size(dims with this vocab, total_rows, 0)
+ * Host checks: TV_E_TEMP, TV_E_ARG, TV_E_ROWS, TV_E_WORKSPACE.  Device checks:
+ * TV_E_ORDER, TV_E_DUP_SIBLING, TV_E_TOKEN, TV_E_UNIFORM.
+ */
+TV_API int tv_accept_residual(const tv_tree *trees, int n_req, const float *logits, int32_t vocab,
+                       float temperature, const float *uniforms, int bonus_at_leaf,
+                       int32_t *path, int32_t *accept_len, int32_t *out_tokens, int32_t *out_count,
+                       int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * KV commit [Drafters and tree verify, §The round, step 4; §Tree verify through
+ * recurrent layers, last paragraph]: keep the accepted path's KV rows and drop
+ * the rest -- for d = 0..a_r, copy slot ctx_len + path[d] to slot ctx_len + d,
+ * every KV head, K and V.  All source rows are read before any row is written
+ * (a target slot can be an earlier step's source).
+ *
+ *   kv           host array [n_req] (the same caches verify wrote into)
+ *   trees        host array [n_req] (only n is read, for the row offsets)
+ *   path, accept_len  device, from an accept walk
+ *   committed_src device int32 [total_rows]: slot ctx_len + path[d] for
+ *                d = 0..a_r at row_off(r)
+ *   new_ctx      device int32 [n_req]: ctx_len + a_r + 1
+ * Host checks: TV_E_ARG, TV_E_ROWS.  Device checks: TV_E_PATH.
+ */
+TV_API int tv_commit_kv(const tv_kv *kv, const tv_dims *dims, const tv_tree *trees, int n_req,
+                 const int32_t *path, const int32_t *accept_len,
+                 int32_t *committed_src, int32_t *new_ctx, int32_t *dev_status, void *stream);
+
+/* A short English name of a status code (static storage). */
+TV_API const char *tv_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TV_H */

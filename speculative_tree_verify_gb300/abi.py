@@ -1,0 +1,139 @@
+"""Python binding of the C ABI in include/tv.h -- argument marshalling only.
+
+Every function here has the name of its C entry point and does nothing but
+turn Python values (ints, torch tensors, lists of structs) into the C
+arguments and call the CUDA library.  All computation happens in the
+library's kernels.  If the library is missing the import of a function fails
+loudly: there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtv.so")
+
+TV_OK = 0
+STATUS = {
+    0: "TV_OK", -1: "TV_E_ARG", -2: "TV_E_ORDER", -3: "TV_E_DUP_SIBLING", -4: "TV_E_TOKEN",
+    -5: "TV_E_CAPACITY", -6: "TV_E_ROWS", -7: "TV_E_UNIFORM", -8: "TV_E_TEMP", -9: "TV_E_WORKSPACE",
+    -10: "TV_E_CUDA", -11: "TV_E_UNSUPPORTED", -12: "TV_E_TIMEOUT", -13: "TV_E_PATH",
+}
+CODES = {v: k for k, v in STATUS.items()}
+
+# entry points declared in include/tv.h
+SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv",
+           "tv_status_string")
+
+
+class TvDims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_float),
+                ("rms_eps", ctypes.c_float)]
+
+
+class TvModel(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("ln1", ctypes.c_void_p), ("wqkv", ctypes.c_void_p),
+                ("wo", ctypes.c_void_p), ("ln_f", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
+                ("dims", TvDims)]
+
+
+class TvKv(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("ctx_len", ctypes.c_int32),
+                ("capacity", ctypes.c_int32)]
+
+
+class TvTree(ctypes.Structure):
+    _fields_ = [("parent", ctypes.c_void_p), ("token", ctypes.c_void_p), ("n", ctypes.c_int32)]
+
+
+_lib = None
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+def load():
+    """Load libtv.so (built in-tree by speculative_tree_verify_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise LibraryMissing(f"CUDA library not built: {LIB_PATH} is missing "
+                                 "(run speculative_tree_verify_gb300.build.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.tv_workspace_size.argtypes = [ctypes.POINTER(TvDims), I, I, ctypes.POINTER(Z)]
+        lib.tv_verify_tree.argtypes = [ctypes.POINTER(TvModel), ctypes.POINTER(TvKv), ctypes.POINTER(TvTree), I,
+                                       P, P, P, P, P, Z, P, P]
+        lib.tv_accept_greedy.argtypes = [ctypes.POINTER(TvTree), I, P, P, P, P, P, P]
+        lib.tv_accept_residual.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float, P, I,
+                                           P, P, P, P, P, P, Z, P]
+        lib.tv_commit_kv.argtypes = [ctypes.POINTER(TvKv), ctypes.POINTER(TvDims), ctypes.POINTER(TvTree), I,
+                                     P, P, P, P, P, P]
+        lib.tv_status_string.argtypes = [I]
+        lib.tv_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _p(x) -> Optional[int]:
+    """Device/host address of a tensor, an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _arr(ctype, items: Sequence):
+    return (ctype * len(items))(*items)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def tv_status_string(code: int) -> str:
+    return load().tv_status_string(int(code)).decode()
+
+
+def tv_workspace_size(dims: TvDims, max_rows: int, max_ctx: int) -> int:
+    out = ctypes.c_size_t(0)
+    rc = load().tv_workspace_size(ctypes.byref(dims), int(max_rows), int(max_ctx), ctypes.byref(out))
+    if rc != TV_OK:
+        raise ValueError(f"tv_workspace_size: {STATUS.get(rc, rc)}")
+    return int(out.value)
+
+
+def tv_verify_tree(model: TvModel, kvs: Sequence[TvKv], trees: Sequence[TvTree], logits, argmax, top2_gap,
+                   attn_out, workspace, workspace_bytes: int, dev_status, stream=None) -> int:
+    return load().tv_verify_tree(ctypes.byref(model), _arr(TvKv, kvs), _arr(TvTree, trees), len(trees),
+                                 _p(logits), _p(argmax), _p(top2_gap), _p(attn_out), _p(workspace),
+                                 int(workspace_bytes), _p(dev_status), _stream(stream))
+
+
+def tv_accept_greedy(trees: Sequence[TvTree], argmax, path, accept_len, out_tokens, dev_status, stream=None) -> int:
+    return load().tv_accept_greedy(_arr(TvTree, trees), len(trees), _p(argmax), _p(path), _p(accept_len),
+                                   _p(out_tokens), _p(dev_status), _stream(stream))
+
+
+def tv_accept_residual(trees: Sequence[TvTree], logits, vocab: int, temperature: float, uniforms,
+                       bonus_at_leaf: bool, path, accept_len, out_tokens, out_count, dev_status, workspace,
+                       workspace_bytes: int, stream=None) -> int:
+    return load().tv_accept_residual(_arr(TvTree, trees), len(trees), _p(logits), int(vocab), float(temperature),
+                                     _p(uniforms), 1 if bonus_at_leaf else 0, _p(path), _p(accept_len),
+                                     _p(out_tokens), _p(out_count), _p(dev_status), _p(workspace),
+                                     int(workspace_bytes), _stream(stream))
+
+
+def tv_commit_kv(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], path, accept_len, committed_src,
+                 new_ctx, dev_status, stream=None) -> int:
+    return load().tv_commit_kv(_arr(TvKv, kvs), ctypes.byref(dims), _arr(TvTree, trees), len(trees), _p(path),
+                               _p(accept_len), _p(committed_src), _p(new_ctx), _p(dev_status), _stream(stream))

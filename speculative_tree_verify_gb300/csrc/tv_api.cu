@@ -1,0 +1,246 @@
+// The C ABI (include/tv.h): host-side argument checks, the workspace layout and
+// the launch sequence of each entry point.  Everything runs on the caller's
+// stream; nothing here allocates device memory.
+#include <cmath>
+#include <cstring>
+
+#include "tv_common.cuh"
+#include "tv_gemm.cuh"
+#include "tv_kernels.cuh"
+
+namespace tv {
+namespace {
+
+constexpr int kMaxHeadGrid = 1024;   // top-2 partial rows reserved in the workspace
+
+struct WsLayout {
+  size_t rstats, meta, rope, counter, h, q, part_qkv, attn_ml, attn_o, attn, part_o, hf, top2, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The residual walk's statistics come first, so that tv_accept_residual needs
+// only the vocabulary to find them.
+WsLayout ws_layout(const tv_dims& d) {
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t H = d.hidden, QD = (size_t)d.n_q_heads * d.head_dim;
+  const size_t QKV = (size_t)(d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const GemmPlan pq = plan_gemm((int)QKV, (int)H, false);
+  const GemmPlan po = plan_gemm((int)H, (int)QD, false);
+  L.rstats = take((size_t)kMaxRows * n_vchunks(d.vocab) * sizeof(RowStat));
+  L.meta = take(kMaxRows * sizeof(RowMeta));
+  L.rope = take((size_t)kMaxRows * (d.head_dim / 2) * sizeof(float2));
+  L.counter = take(256);
+  L.h = take(kMaxRows * H * 2);
+  L.q = take(kMaxRows * QD * 2);
+  L.part_qkv = take((size_t)pq.splits * kMaxRows * QKV * 4);
+  L.attn_ml = take((size_t)kMaxRows * d.n_q_heads * kChunkSlots * 2 * 4);
+  L.attn_o = take((size_t)kMaxRows * d.n_q_heads * kChunkSlots * d.head_dim * 4);
+  L.attn = take(kMaxRows * QD * 2);
+  L.part_o = take((size_t)po.splits * kMaxRows * H * 4);
+  L.hf = take(kMaxRows * H * 2);
+  L.top2 = take((size_t)kMaxHeadGrid * 32 * sizeof(Top2));
+  L.total = off;
+  return L;
+}
+
+int check_dims(const tv_dims& d) {
+  if (d.hidden <= 0 || d.n_q_heads <= 0 || d.n_kv_heads <= 0 || d.head_dim <= 0 || d.vocab < 2) return TV_E_ARG;
+  if (!(d.rms_eps >= 0.f) || !(d.rope_theta > 0.f) || !std::isfinite(d.rope_theta)) return TV_E_ARG;
+  if (d.head_dim != 64 && d.head_dim != 128) return TV_E_UNSUPPORTED;
+  if (d.hidden % 64 != 0 || (d.n_q_heads * d.head_dim) % 64 != 0) return TV_E_UNSUPPORTED;
+  if (d.n_q_heads % d.n_kv_heads != 0) return TV_E_UNSUPPORTED;
+  return TV_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Fills the request table from host structs.  kv may be null (walks).
+int build_table(ReqTable& t, const tv_tree* trees, const tv_kv* kv, int n_req, bool need_parent) {
+  if (!trees || n_req < 1 || n_req > kMaxReq) return n_req < 1 || n_req > kMaxReq ? TV_E_ROWS : TV_E_ARG;
+  memset(&t, 0, sizeof(t));
+  t.n_req = n_req;
+  int total = 0;
+  for (int r = 0; r < n_req; ++r) {
+    const int n = trees[r].n;
+    if (n < 1 || n > kMaxRows) return TV_E_ROWS;
+    t.row_off[r] = total;
+    t.n[r] = n;
+    total += n;
+    if (total > kMaxRows) return TV_E_ROWS;
+    if (need_parent && (!trees[r].parent || !trees[r].token)) return TV_E_ARG;
+    t.parent[r] = trees[r].parent;
+    t.token[r] = trees[r].token;
+    if (kv) {
+      if (!kv[r].k || !kv[r].v || !aligned16(kv[r].k) || !aligned16(kv[r].v)) return TV_E_ARG;
+      if (kv[r].ctx_len < 0 || kv[r].capacity < 0) return TV_E_ARG;
+      if ((long long)kv[r].ctx_len + n > (long long)kv[r].capacity) return TV_E_CAPACITY;
+      t.ctx[r] = kv[r].ctx_len;
+      t.capacity[r] = kv[r].capacity;
+      t.k[r] = reinterpret_cast<__nv_bfloat16*>(kv[r].k);
+      t.v[r] = reinterpret_cast<__nv_bfloat16*>(kv[r].v);
+    }
+  }
+  t.row_off[n_req] = total;
+  t.total_rows = total;
+  return TV_OK;
+}
+
+}  // namespace
+}  // namespace tv
+
+using namespace tv;
+
+extern "C" {
+
+int tv_workspace_size(const tv_dims* dims, int max_rows, int max_ctx, size_t* bytes) {
+  if (!dims || !bytes || max_rows < 0 || max_ctx < 0) return TV_E_ARG;
+  if (max_rows > kMaxRows) return TV_E_ROWS;
+  const int rc = check_dims(*dims);
+  if (rc) return rc;
+  *bytes = ws_layout(*dims).total;
+  return TV_OK;
+}
+
+int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees, int n_req, float* logits,
+                   int32_t* argmax, float* top2_gap, tv_bf16* attn_out, void* workspace, size_t workspace_bytes,
+                   int32_t* dev_status, void* stream) {
+  if (!model || !kv || !trees || !logits || !argmax || !top2_gap || !dev_status) return TV_E_ARG;
+  const tv_dims& d = model->dims;
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if (!model->embed || !model->ln1 || !model->wqkv || !model->wo || !model->ln_f || !model->lm_head)
+    return TV_E_ARG;
+  if (!aligned16(model->wqkv) || !aligned16(model->wo) || !aligned16(model->lm_head)) return TV_E_ARG;
+  ReqTable t;
+  rc = build_table(t, trees, kv, n_req, true);
+  if (rc) return rc;
+  const int G = d.n_q_heads / d.n_kv_heads;
+  for (int r = 0; r < n_req; ++r)
+    if (G * t.n[r] > kMaxQueriesPerKvHead) return TV_E_UNSUPPORTED;
+  const WsLayout L = ws_layout(d);
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return TV_E_WORKSPACE;
+  if (attn_out && !aligned16(attn_out)) return TV_E_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return TV_E_CUDA;
+  if (sms > kMaxHeadGrid) return TV_E_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  LayerBufs b;
+  b.meta = reinterpret_cast<RowMeta*>(ws + L.meta);
+  b.rope = reinterpret_cast<float2*>(ws + L.rope);
+  b.head_counter = reinterpret_cast<unsigned int*>(ws + L.counter);
+  b.h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
+  b.q = reinterpret_cast<__nv_bfloat16*>(ws + L.q);
+  b.part_qkv = reinterpret_cast<float*>(ws + L.part_qkv);
+  b.attn_ml = reinterpret_cast<float*>(ws + L.attn_ml);
+  b.attn_o = reinterpret_cast<float*>(ws + L.attn_o);
+  b.attn = attn_out ? reinterpret_cast<__nv_bfloat16*>(attn_out) : reinterpret_cast<__nv_bfloat16*>(ws + L.attn);
+  b.part_o = reinterpret_cast<float*>(ws + L.part_o);
+  b.hf = reinterpret_cast<__nv_bfloat16*>(ws + L.hf);
+
+  const int H = d.hidden, QD = d.n_q_heads * d.head_dim;
+  const int QKV = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const GemmPlan pq = plan_gemm(QKV, H, false);
+  const GemmPlan po = plan_gemm(H, QD, false);
+  const GemmPlan ph = plan_gemm(d.vocab, H, true);
+  GemmParams gp;
+  memset(&gp, 0, sizeof(gp));
+  gp.status = dev_status;
+
+  if ((rc = launch_prologue(t, d, b, dev_status, st))) return rc;
+  if ((rc = launch_embed_norm(t, *model, b, dev_status, st))) return rc;
+  gp.out = b.part_qkv;
+  if ((rc = launch_gemm(GEMM_PARTIAL, model->wqkv, QKV, H, b.h, t.total_rows, pq, gp, sms, st))) return rc;
+  if ((rc = launch_qkv_finalize(t, d, b, pq.splits, dev_status, st))) return rc;
+  if ((rc = launch_attention(t, d, b, dev_status, st))) return rc;
+  gp.out = b.part_o;
+  if ((rc = launch_gemm(GEMM_PARTIAL, model->wo, H, QD, b.attn, t.total_rows, po, gp, sms, st))) return rc;
+  if ((rc = launch_o_finalize(t, *model, b, po.splits, dev_status, st))) return rc;
+  gp.out = logits;
+  gp.top2_part = reinterpret_cast<Top2*>(ws + L.top2);
+  gp.done_counter = b.head_counter;
+  gp.argmax = argmax;
+  gp.gap = top2_gap;
+  return launch_gemm(GEMM_HEAD, model->lm_head, d.vocab, H, b.hf, t.total_rows, ph, gp, sms, st);
+}
+
+int tv_accept_greedy(const tv_tree* trees, int n_req, const int32_t* argmax, int32_t* path, int32_t* accept_len,
+                     int32_t* out_tokens, int32_t* dev_status, void* stream) {
+  if (!argmax || !path || !accept_len || !out_tokens || !dev_status) return TV_E_ARG;
+  ReqTable t;
+  const int rc = build_table(t, trees, nullptr, n_req, true);
+  if (rc) return rc;
+  return launch_accept_greedy(t, argmax, path, accept_len, out_tokens, dev_status,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tv_accept_residual(const tv_tree* trees, int n_req, const float* logits, int32_t vocab, float temperature,
+                       const float* uniforms, int bonus_at_leaf, int32_t* path, int32_t* accept_len,
+                       int32_t* out_tokens, int32_t* out_count, int32_t* dev_status, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return TV_E_TEMP;
+  if (!logits || !uniforms || !path || !accept_len || !out_tokens || !out_count || !dev_status || vocab < 2)
+    return TV_E_ARG;
+  ReqTable t;
+  const int rc = build_table(t, trees, nullptr, n_req, true);
+  if (rc) return rc;
+  const size_t need = align256((size_t)kMaxRows * n_vchunks(vocab) * sizeof(RowStat));
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return TV_E_WORKSPACE;
+  return launch_accept_residual(t, logits, vocab, temperature, uniforms, bonus_at_leaf ? 1 : 0,
+                                static_cast<RowStat*>(workspace), path, accept_len, out_tokens, out_count,
+                                dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tv_commit_kv(const tv_kv* kv, const tv_dims* dims, const tv_tree* trees, int n_req, const int32_t* path,
+                 const int32_t* accept_len, int32_t* committed_src, int32_t* new_ctx, int32_t* dev_status,
+                 void* stream) {
+  if (!kv || !dims || !path || !accept_len || !committed_src || !new_ctx || !dev_status) return TV_E_ARG;
+  if (dims->n_kv_heads <= 0 || (dims->head_dim != 64 && dims->head_dim != 128)) return TV_E_UNSUPPORTED;
+  ReqTable t;
+  const int rc = build_table(t, trees, kv, n_req, false);
+  if (rc) return rc;
+  return launch_commit(t, *dims, path, accept_len, committed_src, new_ctx, dev_status,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* tv_status_string(int code) {
+  switch (code) {
+    case TV_OK: return "ok";
+    case TV_E_ARG: return "bad argument";
+    case TV_E_ORDER: return "parent array not in parent-before-child order";
+    case TV_E_DUP_SIBLING: return "duplicate sibling token";
+    case TV_E_TOKEN: return "token id outside the vocabulary";
+    case TV_E_CAPACITY: return "cache capacity below ctx_len + tree rows";
+    case TV_E_ROWS: return "tree size outside 1..32 or more than 32 rows in one pass";
+    case TV_E_UNIFORM: return "uniform not finite or not in [0, 1)";
+    case TV_E_TEMP: return "temperature not finite or not above 0";
+    case TV_E_WORKSPACE: return "workspace missing or too small";
+    case TV_E_CUDA: return "CUDA runtime error";
+    case TV_E_UNSUPPORTED: return "shape not supported by these kernels";
+    case TV_E_TIMEOUT: return "a bounded device wait gave up";
+    case TV_E_PATH: return "accept length or path entry out of range";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

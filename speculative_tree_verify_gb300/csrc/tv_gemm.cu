@@ -1,0 +1,385 @@
+// Skinny GEMM on the 5th-generation tensor cores: out = W * X^T for a weight W
+// [M][K] (bf16, K-major, streamed from HBM once) and at most 32 activation rows
+// X [rows][K] (bf16).  Used for the LM head (fused fp32 logits + per-row
+// argmax / top-2 gap) and for the QKV / O projections (split-K fp32 partials,
+// summed in a fixed order by the finalize kernels).
+//
+// Reduction order.  "Every matrix-product kernel fixes its reduction order by
+// the weight's shape and never by the row count" [Exactness, §The one
+// exception: near ties]: the activation rows always fill a fixed MMA N of 32
+// (missing rows read as zeros from the TMA's out-of-bounds fill), the K loop of
+// every tile runs in increasing k, and the split-K partition is a function of
+// (M, K) alone.  A row's outputs therefore do not depend on how many other rows
+// share the pass [Exactness, §Parallel requests].
+//
+// Design (one CTA per SM, persistent over tiles):
+//   - swap-AB: the weight is the MMA's A operand (M = 128 weight rows per tile
+//     on the TMEM lanes), the activations are B (N = 32 columns), so the weight
+//     stream needs no padding and the tiny operand is the one that is re-read
+//     (from L2).
+//   - warp 0 issues TMA loads of 128x64 weight tiles and 32x64 activation tiles
+//     (128-byte swizzle) into an 8-stage shared-memory ring, weights with an
+//     L2 evict-first hint;
+//   - warp 1 owns the TMEM allocation and issues tcgen05.mma (M128 N32 K16,
+//     bf16 in, fp32 accumulate in TMEM) from one thread; tcgen05.commit frees a
+//     smem stage when its MMAs are done;
+//   - warps 2-5 are the epilogue: each reads its 32 TMEM lanes with
+//     tcgen05.ld while the MMA fills the other of two accumulators.
+//   - LM head: the epilogue writes the fp32 logits and keeps a running per-row
+//     top-2; the last CTA to finish (an atomic counter, no spin) merges the
+//     per-CTA top-2 in CTA order and writes argmax and gap.
+#include <climits>
+
+#include "tv_common.cuh"
+#include "tv_gemm.cuh"
+
+namespace tv {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 32;
+constexpr int BK = 64;
+constexpr int STAGES = 8;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 64;
+constexpr int EPI_STRIDE = 33;
+constexpr size_t SMEM_TILES = (size_t)STAGES * (A_BYTES + B_BYTES);
+constexpr size_t SMEM_BAR = 1024;
+constexpr size_t SMEM_EPI = 4 * 32 * EPI_STRIDE * sizeof(float);
+constexpr size_t SMEM_T2 = 4 * 32 * sizeof(Top2);
+constexpr size_t SMEM_BYTES = 1024 + SMEM_TILES + SMEM_BAR + SMEM_EPI + SMEM_T2;
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                       GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + (size_t)STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SMEM_TILES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_status = reinterpret_cast<int*>(tmem_slot + 1);
+  float* epi = reinterpret_cast<float*>(smem + SMEM_TILES + SMEM_BAR);
+  Top2* t2s = reinterpret_cast<Top2*>(epi + 4 * 32 * EPI_STRIDE);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) *s_status = status_get(p.status);
+  __syncthreads();
+  if (*s_status != 0) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    prefetch_tmap(&mapA);
+    prefetch_tmap(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int KB = p.K / BK;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0;   // bit s: stage s was armed at least once
+      uint32_t last_par = 0;   // bit s: parity of stage s's last armed phase
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const int mt = u / p.splits, sp = u % p.splits;
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(KB, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          tma_load_2d(sA + (size_t)stage * A_BYTES, &mapA, &full[stage], kb * BK, mt * BM, pol_w);
+          tma_load_2d(sB + (size_t)stage * B_BYTES, &mapB, &full[stage], kb * BK, 0, pol_x);
+          armed |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) status_set(p.status, TV_E_TIMEOUT);
+      // every load this thread issued has landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) mbar_wait(&full[s], (last_par >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        const int sp = u % p.splits;
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(KB, kb0 + p.kb_per_split);
+        if (!mbar_wait(&tempty[acc], aphase ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(sA + (size_t)stage * A_BYTES));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(sB + (size_t)stage * B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K inside the swizzled row
+            umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aphase ^= 1u;
+        }
+      }
+      if (!ok) status_set(p.status, TV_E_TIMEOUT);
+      // all MMAs issued by this thread are complete before TMEM is released
+      umma_commit(drain);
+      mbar_wait(drain, 0);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;        // TMEM lane quarter this warp may access
+    const int ew = warp - 2;
+    float* mys = epi + ew * 32 * EPI_STRIDE;
+    Top2 best;
+    best.m1 = -INFINITY;
+    best.i1 = INT_MAX;
+    best.m2 = -INFINITY;
+    best.pad = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+      const int mt = u / p.splits, sp = u % p.splits;
+      if (!mbar_wait(&tfull[acc], aphase)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN), r);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1u;
+      }
+      const int m0 = mt * BM + q * 32;
+      const int m = m0 + lane;
+      if (MODE == GEMM_PARTIAL) {
+        if (m < p.M) {
+          float* dst = p.out + (size_t)sp * kMaxRows * p.M + m;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < p.n_rows) dst[(size_t)j * p.M] = __uint_as_float(r[j]);
+        }
+      } else {
+        if (m < p.M) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < p.n_rows) p.out[(size_t)j * p.M + m] = __uint_as_float(r[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mys[lane * EPI_STRIDE + j] = m < p.M ? __uint_as_float(r[j]) : -INFINITY;
+        __syncwarp();
+        // lane j scans column j (activation row j) over this warp's 32 weight rows
+        for (int l = 0; l < 32; ++l) top2_push(best, mys[l * EPI_STRIDE + lane], m0 + l);
+        __syncwarp();
+      }
+    }
+    if (!ok) status_set(p.status, TV_E_TIMEOUT);
+    if (MODE == GEMM_HEAD) t2s[ew * 32 + lane] = best;
+  }
+
+  __syncthreads();
+
+  if (MODE == GEMM_HEAD && warp == 2) {
+    Top2 b = t2s[lane];
+    for (int e = 1; e < 4; ++e) top2_merge(b, t2s[e * 32 + lane]);
+    p.top2_part[(size_t)blockIdx.x * 32 + lane] = b;
+    __threadfence();
+    unsigned prev = 0;
+    if (lane == 0) prev = atomicAdd(p.done_counter, 1u);
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev == gridDim.x - 1) {
+      __threadfence();
+      Top2 g;
+      g.m1 = -INFINITY;
+      g.i1 = INT_MAX;
+      g.m2 = -INFINITY;
+      g.pad = 0;
+      for (unsigned c = 0; c < gridDim.x; ++c) {
+        const Top2* src = p.top2_part + (size_t)c * 32 + lane;
+        Top2 t;
+        t.m1 = __ldcg(&src->m1);
+        t.i1 = __ldcg(&src->i1);
+        t.m2 = __ldcg(&src->m2);
+        t.pad = 0;
+        top2_merge(g, t);
+      }
+      if (lane < p.n_rows) {
+        p.argmax[lane] = g.i1;
+        p.gap[lane] = g.m1 - g.m2;
+      }
+      if (lane == 0) *p.done_counter = 0u;
+    }
+  }
+
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+GemmPlan plan_gemm(int M, int K, bool head) {
+  GemmPlan pl;
+  const int KB = K / BK;
+  const int tiles = (M + BM - 1) / BM;
+  if (head) {
+    pl.splits = 1;
+    pl.kb_per_split = KB;
+  } else {
+    // about two work units per SM of a 152-SM part; a constant, so the split
+    // (and with it the summation order) depends on the weight shape only
+    const int target_units = 304;
+    int splits = target_units / tiles;
+    if (splits < 1) splits = 1;
+    if (splits > KB) splits = KB;
+    pl.kb_per_split = (KB + splits - 1) / splits;
+    pl.splits = (KB + pl.kb_per_split - 1) / pl.kb_per_split;
+  }
+  pl.n_units = tiles * pl.splits;
+  return pl;
+}
+
+size_t gemm_smem_bytes() { return SMEM_BYTES; }
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+}  // namespace
+
+int make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int box_inner, int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return TV_E_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (inner * 2) % 16 != 0) return TV_E_ARG;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TV_OK : TV_E_CUDA;
+}
+
+int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows, const GemmPlan& pl,
+                const GemmParams& base, int num_sms, cudaStream_t stream) {
+  if (K % BK != 0 || n_rows < 1 || n_rows > kMaxRows) return TV_E_UNSUPPORTED;
+  CUtensorMap mA, mB;
+  int rc = make_tmap_bf16(&mA, W, K, M, BK, BM);
+  if (rc) return rc;
+  rc = make_tmap_bf16(&mB, X, K, n_rows, BK, BN);
+  if (rc) return rc;
+  GemmParams p = base;
+  p.M = M;
+  p.K = K;
+  p.n_rows = n_rows;
+  p.splits = pl.splits;
+  p.kb_per_split = pl.kb_per_split;
+  p.n_units = pl.n_units;
+  const int grid = pl.n_units < num_sms ? pl.n_units : num_sms;
+  if (mode == GEMM_HEAD) {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(gemm_skinny_kernel<GEMM_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SMEM_BYTES) != cudaSuccess)
+        return TV_E_CUDA;
+      attr = true;
+    }
+    gemm_skinny_kernel<GEMM_HEAD><<<grid, THREADS, SMEM_BYTES, stream>>>(mA, mB, p);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(gemm_skinny_kernel<GEMM_PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SMEM_BYTES) != cudaSuccess)
+        return TV_E_CUDA;
+      attr = true;
+    }
+    gemm_skinny_kernel<GEMM_PARTIAL><<<grid, THREADS, SMEM_BYTES, stream>>>(mA, mB, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA;
+}
+
+}  // namespace tv

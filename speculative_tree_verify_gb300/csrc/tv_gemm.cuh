@@ -1,0 +1,41 @@
+// Host interface of the tcgen05 skinny GEMM (tv_gemm.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tv_common.cuh"
+
+namespace tv {
+
+enum GemmMode { GEMM_PARTIAL = 0, GEMM_HEAD = 1 };
+
+struct GemmParams {
+  int M, K;                  // weight [M][K]
+  int n_rows;                // activation rows present (<= 32)
+  int splits;                // split-K count (1 for the head)
+  int kb_per_split;          // 64-wide k-blocks per split
+  int n_units;               // ceil(M / 128) * splits
+  float* out;                // PARTIAL: [splits][32][M] fp32; HEAD: logits [n_rows][M]
+  Top2* top2_part;           // HEAD: [gridDim.x][32]
+  unsigned int* done_counter;// HEAD: zero before the launch, left at zero
+  int32_t* argmax;           // HEAD: [n_rows]
+  float* gap;                // HEAD: [n_rows]
+  int32_t* status;           // sticky status word
+};
+
+struct GemmPlan {
+  int splits, kb_per_split, n_units;
+};
+
+// The split-K partition of a weight [M][K]: a function of (M, K) only.
+GemmPlan plan_gemm(int M, int K, bool head);
+size_t gemm_smem_bytes();
+// 2-D bf16 tensor map over [rows][inner] with a box of box_rows x box_inner
+// and the 128-byte swizzle; rows past `rows` read as zeros.
+int make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int box_inner, int box_rows);
+int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows, const GemmPlan& pl,
+                const GemmParams& base, int num_sms, cudaStream_t stream);
+
+}  // namespace tv

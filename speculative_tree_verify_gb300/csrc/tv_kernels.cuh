@@ -1,0 +1,96 @@
+// Internal interface between the kernel translation units and the C ABI layer.
+// Each .cu file launches its own kernels through the host functions declared
+// here, so the library needs no relocatable device code.
+#pragma once
+
+#include "tv_common.cuh"
+
+namespace tv {
+
+// ---- attention chunking: a function of the context length only ------------
+constexpr int kMaxChunks = 32;               // cache chunks per request
+constexpr int kTreeSlot = kMaxChunks;        // partial slot of the tree keys
+constexpr int kChunkSlots = kMaxChunks + 1;
+
+__host__ __device__ inline int attn_chunk_len(int ctx) {
+  const int per = (ctx + kMaxChunks - 1) / kMaxChunks;
+  const int ch = ((per + 63) / 64) * 64;
+  return ch < 64 ? 64 : ch;
+}
+__host__ __device__ inline int attn_n_chunks(int ctx) {
+  return ctx <= 0 ? 0 : (ctx + attn_chunk_len(ctx) - 1) / attn_chunk_len(ctx);
+}
+
+// ---- residual walk: per-row statistics over vocabulary chunks --------------
+constexpr int kVChunk = 4096;
+struct RowStat {
+  float m;   // max logit of the chunk
+  float s;   // sum over the chunk of exp((logit - m) / T)
+};
+inline int n_vchunks(int vocab) { return (vocab + kVChunk - 1) / kVChunk; }
+
+// ---- block-uniform status check -------------------------------------------
+__device__ __forceinline__ bool block_skip(const int32_t* status) {
+  __shared__ int s_stat;
+  if (threadIdx.x == 0) s_stat = status_get(status);
+  __syncthreads();
+  return s_stat != 0;
+}
+
+// ---- tree validation by one warp (lanes = nodes) ---------------------------
+// Reports the first rule broken, in this order: parent order (parent[0] = -1,
+// 0 <= parent[i] < i), token range (skipped when vocab <= 0), duplicate sibling
+// tokens [Algorithm and correctness contract, §Target position and batching].
+// par/tok receive this lane's parent and token.
+__device__ __forceinline__ int validate_tree_warp(const int32_t* parent, const int32_t* token, int n, int vocab,
+                                                  int& par, int& tok) {
+  const int lane = threadIdx.x & 31;
+  par = lane < n ? parent[lane] : 0;
+  tok = lane < n ? token[lane] : 0;
+  const bool bad_order = lane < n && (lane == 0 ? par != -1 : (par < 0 || par >= lane));
+  const bool bad_token = lane < n && vocab > 0 && (tok < 0 || tok >= vocab);
+  bool dup = false;
+  for (int j = 1; j < 32; ++j) {
+    const int pj = __shfl_sync(0xffffffffu, par, j);
+    const int tj = __shfl_sync(0xffffffffu, tok, j);
+    if (j < lane && lane < n && pj == par && tj == tok) dup = true;
+  }
+  if (__any_sync(0xffffffffu, bad_order)) return TV_E_ORDER;
+  if (__any_sync(0xffffffffu, bad_token)) return TV_E_TOKEN;
+  if (__any_sync(0xffffffffu, dup)) return TV_E_DUP_SIBLING;
+  return TV_OK;
+}
+
+// ---- launchers (host) -------------------------------------------------------
+struct LayerBufs {
+  RowMeta* meta;
+  float2* rope;
+  unsigned int* head_counter;
+  __nv_bfloat16* h;        // [32][H]
+  __nv_bfloat16* q;        // [32][Hq][D]
+  float* part_qkv;
+  float* attn_ml;          // [32][Hq][kChunkSlots][2]
+  float* attn_o;           // [32][Hq][kChunkSlots][D]
+  __nv_bfloat16* attn;     // [rows][Hq D]
+  float* part_o;
+  __nv_bfloat16* hf;       // [32][H]
+};
+
+int launch_prologue(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st);
+int launch_embed_norm(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status, cudaStream_t st);
+int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
+                        cudaStream_t st);
+int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st);
+int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
+                      cudaStream_t st);
+
+int launch_accept_greedy(const ReqTable& t, const int32_t* argmax, int32_t* path, int32_t* accept_len,
+                         int32_t* out_tokens, int32_t* status, cudaStream_t st);
+int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, float temperature,
+                           const float* uniforms, int bonus_at_leaf, RowStat* stats, int32_t* path,
+                           int32_t* accept_len, int32_t* out_tokens, int32_t* out_count, int32_t* status,
+                           cudaStream_t st);
+int launch_commit(const ReqTable& t, const tv_dims& d, const int32_t* path, const int32_t* accept_len,
+                  int32_t* committed_src, int32_t* new_ctx, int32_t* status, cudaStream_t st);
+
+}  // namespace tv

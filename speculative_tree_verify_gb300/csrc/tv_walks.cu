@@ -1,0 +1,348 @@
+// Accept walks and the KV commit.
+//
+//  - greedy walk: one warp per request, lanes = tree nodes [Drafters and tree
+//    verify, §The round, step 3];
+//  - residual walk: a multi-CTA pass of per-chunk softmax statistics over the
+//    logits, then one warp per request walks the tree [Algorithm and
+//    correctness contract, §Deterministic tree candidates and residual
+//    verification];
+//  - commit: gathers the accepted rows down into place [Drafters and tree
+//    verify, §Tree verify through recurrent layers, last paragraph].
+#include <climits>
+
+#include "tv_common.cuh"
+#include "tv_kernels.cuh"
+
+namespace tv {
+
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// greedy: cur = root; repeat { t = argmax[cur]; the child of cur carrying t? }
+// ---------------------------------------------------------------------------
+__global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t* path, int32_t* accept_len,
+                                     int32_t* out_tokens, int32_t* status) {
+  const int r = blockIdx.x, lane = threadIdx.x;
+  if (status_get(status) != 0) return;
+  const int n = t.n[r], row0 = t.row_off[r];
+  int par, tok;
+  const int err = validate_tree_warp(t.parent[r], t.token[r], n, 0, par, tok);
+  if (err != TV_OK) {
+    if (lane == 0) status_set(status, err);
+    return;
+  }
+  int cur = 0, a = 0;
+  if (lane == 0) path[row0] = 0;
+  for (;;) {
+    const int want = argmax[row0 + cur];
+    const unsigned hit = __ballot_sync(FULL, lane > 0 && lane < n && par == cur && tok == want);
+    if (hit == 0u) {
+      if (lane == 0) out_tokens[row0 + a] = want;   // the model's token at the stopping node
+      break;
+    }
+    const int c = __ffs(hit) - 1;
+    const int ctok = __shfl_sync(FULL, tok, c);
+    ++a;
+    if (lane == 0) {
+      path[row0 + a] = c;
+      out_tokens[row0 + a - 1] = ctok;
+    }
+    cur = c;
+  }
+  if (lane == 0) accept_len[r] = a;
+}
+
+// ---------------------------------------------------------------------------
+// residual walk, pass 1: per (row, vocab chunk) the chunk max m and
+// s = sum exp((l - m) / T).  grid (chunks, rows), block 256.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) row_stats_kernel(const float* logits, int V, float inv_t, int nvc,
+                                                        RowStat* stats, const int32_t* status) {
+  __shared__ float red[8];
+  if (block_skip(status)) return;
+  const int c = blockIdx.x, row = blockIdx.y;
+  const float* lr = logits + (size_t)row * V;
+  const int y0 = c * kVChunk;
+  float v[kVChunk / 256];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kVChunk / 256; ++k) {
+    const int y = y0 + k * 256 + threadIdx.x;
+    v[k] = y < V ? lr[y] : -INFINITY;
+    mx = fmaxf(mx, v[k]);
+  }
+  mx = warp_max(mx);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = mx;
+  __syncthreads();
+  mx = red[0];
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < kVChunk / 256; ++k)
+    if (v[k] != -INFINITY) s += expf((v[k] - mx) * inv_t);
+  s = warp_sum(s);
+  if (l == 0) red[w] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int i = 0; i < 8; ++i) tot += red[i];
+    RowStat st;
+    st.m = mx;
+    st.s = tot;
+    stats[(size_t)row * nvc + c] = st;
+  }
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+  return v;
+}
+
+__device__ __forceinline__ double warp_incl_scan_d(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double u = __shfl_up_sync(FULL, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+__device__ __forceinline__ bool is_rejected(int y, const int* rej, int nrej) {
+  for (int k = 0; k < nrej; ++k)
+    if (rej[k] == y) return true;
+  return false;
+}
+
+// One draw y from r = p with the rejected tokens removed: the smallest y with
+// sum_{j<=y} r~(j) > target, r~ the unnormalised residual; if rounding leaves
+// none, the last y with r~(y) > 0.  Chunk masses first, then one chunk in
+// lane-contiguous segments of 128 entries.
+__device__ int residual_draw(const float* lr, int V, float M, float inv_t, const RowStat* st, int nvc,
+                             const int* rej, int nrej, double target) {
+  const int lane = threadIdx.x & 31;
+  double base = 0.0, before = 0.0;
+  int chunk = -1, last_pos = -1;
+  for (int c0 = 0; c0 < nvc; c0 += 32) {
+    const int c = c0 + lane;
+    double w = 0.0;
+    if (c < nvc) {
+      w = (double)st[c].s * (double)expf((st[c].m - M) * inv_t);
+      for (int k = 0; k < nrej; ++k)
+        if (rej[k] / kVChunk == c) w -= (double)expf((lr[rej[k]] - M) * inv_t);
+      if (w < 0.0) w = 0.0;
+    }
+    const int lp = __reduce_max_sync(FULL, (c < nvc && w > 0.0) ? c : -1);
+    if (lp > last_pos) last_pos = lp;
+    const double incl = warp_incl_scan_d(w);
+    const unsigned hm = __ballot_sync(FULL, c < nvc && w > 0.0 && base + incl > target);
+    if (hm != 0u) {
+      const int L = __ffs(hm) - 1;
+      chunk = c0 + L;
+      before = base + __shfl_sync(FULL, incl - w, L);
+      break;
+    }
+    base += __shfl_sync(FULL, incl, 31);
+  }
+  double t2 = target - before;
+  if (chunk < 0) {   // rounding: fall back to the last entry with mass
+    chunk = last_pos < 0 ? 0 : last_pos;
+    t2 = INFINITY;
+  }
+  const int y0 = chunk * kVChunk + lane * (kVChunk / 32);
+  double mine = 0.0;
+  int last_valid = -1;
+  for (int k = 0; k < kVChunk / 32; ++k) {
+    const int y = y0 + k;
+    if (y < V && !is_rejected(y, rej, nrej)) {
+      const float e = expf((lr[y] - M) * inv_t);
+      mine += (double)e;
+      if (e > 0.f) last_valid = y;
+    }
+  }
+  const double incl = warp_incl_scan_d(mine);
+  const unsigned hm = __ballot_sync(FULL, mine > 0.0 && incl > t2);
+  if (hm == 0u) {
+    const int lv = __reduce_max_sync(FULL, last_valid);
+    return lv < 0 ? chunk * kVChunk : lv;
+  }
+  const int L = __ffs(hm) - 1;
+  int y_found = -1;
+  if (lane == L) {
+    double cum = incl - mine;
+    for (int k = 0; k < kVChunk / 32; ++k) {
+      const int y = y0 + k;
+      if (y < V && !is_rejected(y, rej, nrej)) {
+        const float e = expf((lr[y] - M) * inv_t);
+        cum += (double)e;
+        last_valid = e > 0.f ? y : last_valid;
+        if (cum > t2) {
+          y_found = y;
+          break;
+        }
+      }
+    }
+    if (y_found < 0) y_found = last_valid;
+  }
+  return __shfl_sync(FULL, y_found, L);
+}
+
+// residual walk, pass 2: one warp per request
+__global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, float inv_t, const float* uniforms,
+                                       int bonus_at_leaf, const RowStat* stats, int nvc, int32_t* path,
+                                       int32_t* accept_len, int32_t* out_tokens, int32_t* out_count,
+                                       int32_t* status) {
+  __shared__ int s_rej[32];
+  const int r = blockIdx.x, lane = threadIdx.x;
+  if (status_get(status) != 0) return;
+  const int n = t.n[r], row0 = t.row_off[r];
+  int par, tok;
+  const int err = validate_tree_warp(t.parent[r], t.token[r], n, V, par, tok);
+  if (err != TV_OK) {
+    if (lane == 0) status_set(status, err);
+    return;
+  }
+  // every random input of the request must be finite and in [0, 1)
+  // [Algorithm and correctness contract, §Single-path sampling]
+  const float uu = lane < n ? uniforms[row0 + lane] : 0.f;
+  if (__any_sync(FULL, lane < n && !(uu >= 0.f && uu < 1.f))) {
+    if (lane == 0) status_set(status, TV_E_UNIFORM);
+    return;
+  }
+  int cur = 0, a = 0, nout = 0, draw = 0;
+  if (lane == 0) path[row0] = 0;
+  for (;;) {
+    const float* lr = logits + (size_t)(row0 + cur) * V;
+    const RowStat* st = stats + (size_t)(row0 + cur) * nvc;
+    float M = -INFINITY;
+    for (int c = lane; c < nvc; c += 32) M = fmaxf(M, st[c].m);
+    M = warp_max(M);
+    double Z = 0.0;
+    for (int c = lane; c < nvc; c += 32) Z += (double)st[c].s * (double)expf((st[c].m - M) * inv_t);
+    Z = warp_sum_d(Z);
+
+    // candidates: the children of cur, in increasing node index
+    unsigned kids = __ballot_sync(FULL, lane > 0 && lane < n && par == cur);
+    double R = 0.0;   // removed (rejected) mass
+    int nrej = 0, acc = -1;
+    while (kids != 0u) {
+      const int c = __ffs(kids) - 1;
+      kids &= kids - 1u;
+      const int x = __shfl_sync(FULL, tok, c);
+      const float u = __shfl_sync(FULL, uu, draw);
+      ++draw;
+      const double ex = (double)expf((lr[x] - M) * inv_t);
+      if ((double)u < ex / (Z - R)) {   // accept x with probability r(x)
+        acc = c;
+        break;
+      }
+      R += ex;   // remove x and renormalise
+      if (lane == 0) s_rej[nrej] = x;
+      ++nrej;
+      __syncwarp();
+    }
+    if (acc >= 0) {
+      const int ctok = __shfl_sync(FULL, tok, acc);
+      ++a;
+      if (lane == 0) {
+        path[row0 + a] = acc;
+        out_tokens[row0 + nout] = ctok;
+      }
+      ++nout;
+      cur = acc;
+      continue;
+    }
+    if (nrej > 0 || bonus_at_leaf) {
+      const float u = __shfl_sync(FULL, uu, draw);
+      ++draw;
+      const int y = residual_draw(lr, V, M, inv_t, st, nvc, s_rej, nrej, (double)u * (Z - R));
+      if (lane == 0) out_tokens[row0 + nout] = y;
+      ++nout;
+    }
+    break;
+  }
+  if (lane == 0) {
+    accept_len[r] = a;
+    out_count[r] = nout;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// commit: slot ctx + path[d] -> slot ctx + d, d = 0..a; every source row is
+// read into shared memory before any is written.  grid (Hkv, K|V, requests).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) commit_kernel(ReqTable t, int D, const int32_t* path, const int32_t* accept_len,
+                                                     int32_t* committed_src, int32_t* new_ctx, int32_t* status) {
+  __shared__ uint4 rows[kMaxRows * 128 * 2 / 16];
+  __shared__ int s_src[kMaxRows];
+  __shared__ int s_a;
+  if (block_skip(status)) return;
+  const int g = blockIdx.x, which = blockIdx.y, r = blockIdx.z;
+  const int n = t.n[r], row0 = t.row_off[r], ctx = t.ctx[r];
+  if (threadIdx.x == 0) s_a = accept_len[r];
+  __syncthreads();
+  const int a = s_a;
+  bool bad = a < 0 || a >= n;
+  if (!bad && (int)threadIdx.x <= a) {
+    const int p = path[row0 + threadIdx.x];
+    s_src[threadIdx.x] = p;
+    if (p < 0 || p >= n || (threadIdx.x == 0 && p != 0)) bad = true;
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) status_set(status, TV_E_PATH);
+    return;
+  }
+  __nv_bfloat16* base = (which ? t.v[r] : t.k[r]) + (size_t)g * t.capacity[r] * D;
+  const int vec_per_row = D / 8;
+  const int total = (a + 1) * vec_per_row;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int d = i / vec_per_row, c = i - d * vec_per_row;
+    rows[i] = *reinterpret_cast<const uint4*>(base + (size_t)(ctx + s_src[d]) * D + c * 8);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int d = i / vec_per_row, c = i - d * vec_per_row;
+    *reinterpret_cast<uint4*>(base + (size_t)(ctx + d) * D + c * 8) = rows[i];
+  }
+  if (g == 0 && which == 0) {
+    if ((int)threadIdx.x <= a) committed_src[row0 + threadIdx.x] = ctx + s_src[threadIdx.x];
+    if (threadIdx.x == 0) new_ctx[r] = ctx + a + 1;
+  }
+}
+
+inline int last_error() { return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA; }
+
+}  // namespace
+
+int launch_accept_greedy(const ReqTable& t, const int32_t* argmax, int32_t* path, int32_t* accept_len,
+                         int32_t* out_tokens, int32_t* status, cudaStream_t st) {
+  accept_greedy_kernel<<<t.n_req, 32, 0, st>>>(t, argmax, path, accept_len, out_tokens, status);
+  return last_error();
+}
+
+int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, float temperature,
+                           const float* uniforms, int bonus_at_leaf, RowStat* stats, int32_t* path,
+                           int32_t* accept_len, int32_t* out_tokens, int32_t* out_count, int32_t* status,
+                           cudaStream_t st) {
+  const int nvc = n_vchunks(vocab);
+  const float inv_t = (float)(1.0 / (double)temperature);
+  row_stats_kernel<<<dim3(nvc, t.total_rows), 256, 0, st>>>(logits, vocab, inv_t, nvc, stats, status);
+  if (cudaGetLastError() != cudaSuccess) return TV_E_CUDA;
+  accept_residual_kernel<<<t.n_req, 32, 0, st>>>(t, logits, vocab, inv_t, uniforms, bonus_at_leaf, stats, nvc, path,
+                                                 accept_len, out_tokens, out_count, status);
+  return last_error();
+}
+
+int launch_commit(const ReqTable& t, const tv_dims& d, const int32_t* path, const int32_t* accept_len,
+                  int32_t* committed_src, int32_t* new_ctx, int32_t* status, cudaStream_t st) {
+  commit_kernel<<<dim3(d.n_kv_heads, 2, t.n_req), 128, 0, st>>>(t, d.head_dim, path, accept_len, committed_src,
+                                                                new_ctx, status);
+  return last_error();
+}
+
+}  // namespace tv

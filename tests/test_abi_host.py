@@ -1,0 +1,126 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+exactly the entry points include/tv.h declares, and its host-side argument
+checks return the documented codes before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from speculative_tree_verify_gb300 import abi, build
+from speculative_tree_verify_gb300.device import tv_dims
+from speculative_tree_verify_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(re.findall(r"TV_API\s+[\w\s\*]*?\b(tv_\w+)\s*\(", text))
+
+
+def test_header_declares_the_four_round_calls():
+    names = _declared()
+    for n in ("tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv"):
+        assert n in names
+    assert sorted(abi.SYMBOLS) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert exported == _declared()
+    for name in _declared():
+        assert getattr(lib, name) is not None
+
+
+def test_status_codes_match_header():
+    defs = dict((name, int(val)) for name, val in re.findall(r"#define\s+(TV_\w+)\s+(-?\d+)", open(HEADER).read()))
+    assert {v: k for k, v in defs.items()} == abi.STATUS
+    for code, name in abi.STATUS.items():
+        assert abi.tv_status_string(code) not in ("", "unknown status")
+
+
+def test_workspace_size_host_only(lib):
+    ws = abi.tv_workspace_size(tv_dims(synth.FULL), 32, 32768)
+    assert ws > 0 and ws % 256 == 0
+    small = abi.tv_workspace_size(tv_dims(synth.TINY), 8, 64)
+    assert 0 < small < ws
+    bad = tv_dims(synth.Dims(hidden=100, n_q_heads=4, n_kv_heads=2, head_dim=64, vocab=1024))
+    with pytest.raises(ValueError, match="UNSUPPORTED"):
+        abi.tv_workspace_size(bad, 8, 64)
+    with pytest.raises(ValueError, match="ROWS"):
+        abi.tv_workspace_size(tv_dims(synth.TINY), 33, 64)
+
+
+FAKE = 0x10000   # a 16-byte aligned non-null address; never dereferenced on these paths
+
+
+def _model(d=synth.TINY):
+    return abi.TvModel(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, tv_dims(d))
+
+
+def _kv(ctx, cap):
+    return abi.TvKv(FAKE, FAKE, ctx, cap)
+
+
+def _tree(n):
+    return abi.TvTree(FAKE, FAKE, n)
+
+
+def test_verify_host_checks(lib):
+    d = synth.TINY
+    ws = abi.tv_workspace_size(tv_dims(d), 32, 64)
+    args = dict(logits=FAKE, argmax=FAKE, top2_gap=FAKE, attn_out=None, workspace=FAKE, workspace_bytes=ws,
+                dev_status=FAKE)
+
+    def call(model=None, kvs=None, trees=None, **over):
+        a = dict(args)
+        a.update(over)
+        return abi.tv_verify_tree(model or _model(), kvs if kvs is not None else [_kv(64, 96)],
+                                  trees if trees is not None else [_tree(8)], **a)
+
+    assert call(logits=None) == abi.CODES["TV_E_ARG"]
+    assert call(trees=[_tree(0)]) == abi.CODES["TV_E_ROWS"]
+    assert call(trees=[_tree(33)], kvs=[_kv(0, 100)]) == abi.CODES["TV_E_ROWS"]
+    assert call(trees=[_tree(20), _tree(13)], kvs=[_kv(0, 64), _kv(0, 64)]) == abi.CODES["TV_E_ROWS"]
+    assert call(kvs=[_kv(90, 96)]) == abi.CODES["TV_E_CAPACITY"]
+    assert call(workspace_bytes=ws - 1) == abi.CODES["TV_E_WORKSPACE"]
+    assert call(workspace=None) == abi.CODES["TV_E_WORKSPACE"]
+    assert call(kvs=[abi.TvKv(FAKE + 2, FAKE, 64, 96)]) == abi.CODES["TV_E_ARG"]   # misaligned cache
+    bad = synth.Dims(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=96, vocab=1024)
+    assert call(model=_model(bad)) == abi.CODES["TV_E_UNSUPPORTED"]
+    wide = synth.Dims(hidden=512, n_q_heads=16, n_kv_heads=2, head_dim=64, vocab=1024)   # 8 heads per group
+    assert call(model=_model(wide), trees=[_tree(21)], kvs=[_kv(0, 64)],
+                workspace_bytes=abi.tv_workspace_size(tv_dims(wide), 32, 64)) == abi.CODES["TV_E_UNSUPPORTED"]
+
+
+def test_walk_and_commit_host_checks(lib):
+    ws = abi.tv_workspace_size(tv_dims(synth.TINY), 32, 64)
+    trees = [_tree(8)]
+    assert abi.tv_accept_greedy(trees, None, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_accept_greedy([_tree(40)], FAKE, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ROWS"]
+    for t in (0.0, -1.0, float("nan"), float("inf")):
+        assert abi.tv_accept_residual(trees, FAKE, 1024, t, FAKE, True, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                      ws) == abi.CODES["TV_E_TEMP"]
+    assert abi.tv_accept_residual(trees, FAKE, 1024, 1.0, FAKE, True, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  16) == abi.CODES["TV_E_WORKSPACE"]
+    dims = tv_dims(synth.TINY)
+    assert abi.tv_commit_kv([_kv(64, 96)], dims, trees, None, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_commit_kv([_kv(64, 96)], dims, [_tree(33)], FAKE, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ROWS"]
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(abi, "_lib", None)
+    monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(abi.LibraryMissing):
+        abi.load()
