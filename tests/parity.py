@@ -2,7 +2,10 @@
 
 * fp32 logits: max |gpu - oracle| <= 2e-2 x the oracle row's RMS logit (the
   "logit scale");
-* attention outputs and the tree rows' K/V: max abs error <= 1e-2;
+* attention outputs: max abs error <= 1e-2;
+* the tree rows' K/V (bf16 stores of values up to ~6 at hidden 5120): error
+  <= 1e-2 x max(1, |oracle value|), which admits one bf16 step (2^-7 relative)
+  where fp32 and fp64 accumulations round to different sides;
 * greedy choice: the GPU's argmax equals the oracle's, except where the
   oracle's top-2 gap is within one BF16 ulp of its top logit, where the
   second token is accepted too [Exactness, §The one exception: near ties];
@@ -48,11 +51,17 @@ def check_logits(orc: np.ndarray, gpu: np.ndarray, tol: float = LOGIT_TOL) -> fl
     return float(frac.max())
 
 
-def check_close_bf16(orc_bits: np.ndarray, gpu_bits: np.ndarray, tol: float, what: str) -> float:
+def check_close_bf16(orc_bits: np.ndarray, gpu_bits: np.ndarray, tol: float, what: str,
+                     relative: bool = False) -> float:
+    """max |gpu - oracle| <= tol (absolute), or <= tol * max(1, |oracle|) when
+    ``relative``.  Returns the worst error in those units."""
     o = bf16_to_f64(orc_bits)
     g = bf16_to_f64(gpu_bits)
-    err = float(np.abs(g - o).max()) if o.size else 0.0
-    assert err <= tol, f"{what}: max abs error {err:.3e} > {tol}"
+    if not o.size:
+        return 0.0
+    denom = np.maximum(1.0, np.abs(o)) if relative else 1.0
+    err = float((np.abs(g - o) / denom).max())
+    assert err <= tol, f"{what}: max {'relative ' if relative else ''}error {err:.3e} > {tol}"
     return err
 
 
@@ -167,8 +176,8 @@ def check_verify(model, host_reqs, dm=None, reqs_b=None):
     for (c, t), o, r in zip(host_reqs, orc, reqs):
         ctx, n = c.ctx_len, t.n
         k, v = to_np(r.k), to_np(r.v)
-        check_close_bf16(o["k"], k[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree K")
-        check_close_bf16(o["v"], v[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree V")
+        check_close_bf16(o["k"], k[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree K", relative=True)
+        check_close_bf16(o["v"], v[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree V", relative=True)
         np.testing.assert_array_equal(k[:, :ctx], c.k[:, :ctx])           # cached rows are only read
         np.testing.assert_array_equal(v[:, :ctx], c.v[:, :ctx])
         np.testing.assert_array_equal(k[:, ctx + n:], c.k[:, ctx + n:])   # nothing past the tree rows
