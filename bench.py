@@ -1,0 +1,482 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 tree verify round.
+
+One step = one verify round on one GPU at the hidden-5120 shapes (40/8 heads
+of 128, vocab 151936, bf16 weights ~ N(0, 0.02) drawn on the device):
+tv_verify_tree over a 16-row lattice tree (spine of 8 + 8 next-best branches)
+at 1024 tokens of context, tv_accept_greedy, tv_commit_kv.  The drafts along
+the spine are teacher-forced (the GPU's own greedy tokens, planted before
+timing) so the walk and the commit do real work.  Inputs are synthetic.
+
+Printed: one JSON line (rank 0).  value = ms per round from CUDA-graph replay
+(the served configuration keeps verify in graphs); the eager number, the row
+sweep 8/16/24/32, a sampled round (residual walk), per-stage times, the
+roofline of the LM head kernel, end-to-end latency with host buffers, clocks
+and the CPU oracle baseline ride along.
+
+--impl reference times the CPU oracle (the only reference there is) on the
+same workload on the host cores.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU:
+the round has no cross-GPU exchange, so there is no collective on the data
+path ("replicas only"); the barrier and the max-over-ranks timing use a
+process group.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "tree-verify latency (ms) at 8-32 nodes, 1k ctx; achieved HBM GB/s vs peak"
+UNIT = "ms"
+ROWS, CTX, SLOTS = 16, 1024, 7
+WORKLOAD = "tree verify round (verify + greedy accept + commit), hidden 5120 layer + 151936-vocab head, " \
+           "16-row lattice tree (spine 8 + 8 branches), 1024-token context"
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="only the headline number (for profiling runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _code_sha256() -> str:
+    h = hashlib.sha256()
+    for sub in ("include", os.path.join("speculative_tree_verify_gb300", "csrc")):
+        d = os.path.join(ROOT, sub)
+        for f in sorted(os.listdir(d)):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def _file_sha256(path) -> str:
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _ncu_traffic(kernel_sha: str):
+    """DRAM bytes per launch of the LM head kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "lm_head_hidden5120_ncu.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "kernel_source_sha256", "rows")):
+            k, v = line.strip().split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_sha or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"]), int(vals.get("rows", "0") or 0)
+
+
+class Clocks:
+    """nvidia-smi samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.idx = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.f = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "200", "-i", self.idx], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.f:
+            c = [x.strip() for x in line.split(",")]
+            if len(c) < 9:
+                continue
+            try:
+                sm.append(float(c[1]))
+                mx.append(float(c[2]))
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                               c[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def _make_request(dv, synth, D, tree, ctx, seed, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    cap = ctx + 64
+    k = torch.randn(D.n_kv_heads, cap, D.head_dim, generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn(D.n_kv_heads, cap, D.head_dim, generator=g, device=device).to(torch.bfloat16)
+    return dv.DeviceRequest(k, v, ctx, torch.from_numpy(tree.parent.copy()).to(device),
+                            torch.from_numpy(tree.token.copy()).to(device))
+
+
+def _plant(dv, dm, req, b, spine):
+    """Teacher forcing on the GPU: spine node d+1 gets the token the model
+    picks at spine node d (siblings re-drawn on a collision)."""
+    par = req.parent.cpu().numpy()
+    tok = req.token.cpu().numpy()
+    rng = np.random.default_rng(0)
+    for d in range(1, len(spine)):
+        req.token.copy_(torch.from_numpy(tok))
+        dv.check(dv.verify(dm, [req], b), "verify")
+        t = int(b.argmax[spine[d - 1]])
+        tok[spine[d]] = t
+        for c in range(1, len(par)):
+            if c != spine[d] and par[c] == par[spine[d]] and tok[c] == t:
+                tok[c] = (t + 1 + int(rng.integers(0, 1000))) % dm.dims.vocab
+    req.token.copy_(torch.from_numpy(tok))
+
+
+def _spine(parent):
+    path, cur = [0], 0
+    while True:
+        kids = [c for c in range(1, len(parent)) if int(parent[c]) == cur]
+        if not kids:
+            return path
+        cur = kids[0]
+        path.append(cur)
+
+
+def _graph(fn, warm=3):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(warm):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _time_graph(g, steps):
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def verify_bytes(D, n, ctx):
+    """Algorithmic bytes one verify must move: every weight once, the cached
+    K/V once, the fp32 logits once; embeddings and tree K/V rows are < 0.5 MB."""
+    H, V, QD = D.hidden, D.vocab, D.n_q_heads * D.head_dim
+    weights = V * H * 2 + D.qkv_out * H * 2 + H * QD * 2
+    kv = ctx * D.n_kv_heads * D.head_dim * 2 * 2
+    return weights + kv + n * V * 4
+
+
+def head_bytes(D, n):
+    return D.vocab * D.hidden * 2 + n * D.vocab * 4 + n * D.hidden * 2
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def _host_model(dm, synth):
+    def bits(t):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return synth.Model(dm.dims, *(bits(dm.t[k]) for k in ("embed", "ln1", "wqkv", "wo", "ln_f", "lm_head")))
+
+
+def _host_cache(req, synth):
+    def bits(t):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return synth.Cache(bits(req.k), bits(req.v), req.ctx_len, req.capacity)
+
+
+def oracle_full_round(oracle, model, cache, tree):
+    out = oracle.verify_tree(model, cache, tree, want=("logits", "k", "v"))
+    idx, _, _, _ = oracle.argmax_top2(out["logits"])
+    path, _ = oracle.accept_greedy(tree.parent, tree.token, idx)
+    k, v = oracle.apply_tree_kv(cache, out["k"], out["v"])
+    oracle.commit_kv(k, v, cache.ctx_len, path)
+
+
+def oracle_sampled_step(oracle, model, cache, tree, r_rows, vocab_ids):
+    """A bounded sample of one round: the layer over the first r_rows nodes (a
+    valid smaller tree) and the head over a vocabulary slice.  Returns
+    (layer seconds, head seconds)."""
+    sub = type(tree)(tree.parent[:r_rows].copy(), tree.token[:r_rows].copy())
+    t0 = time.perf_counter()
+    out = oracle.verify_tree(model, cache, sub, want=("hf",))
+    t1 = time.perf_counter()
+    oracle.head_rows(model, out["hf"], vocab_ids)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def cpu_baseline(oracle, model, cache, tree, seconds):
+    t0 = time.perf_counter()
+    oracle_full_round(oracle, model, cache, tree)
+    one = time.perf_counter() - t0
+    reps = max(1, min(20, int(seconds / max(one, 1e-3))))
+    ts = [one]
+    for _ in range(reps - 1):
+        t0 = time.perf_counter()
+        oracle_full_round(oracle, model, cache, tree)
+        ts.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.median(ts)
+    return {"value": ms, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(ts)} full rounds (verify of all {tree.n} rows over the full vocabulary, greedy walk, "
+                      f"commit), median"}
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from speculative_tree_verify_gb300 import abi, build, synth
+    from speculative_tree_verify_gb300 import device as dv
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    D = synth.FULL
+    dm = dv.DeviceModel.random(D, 1234 + rank, device=dev)
+    tree = synth.tree_lattice(ROWS, SLOTS, D.vocab, 7)
+    req = _make_request(dv, synth, D, tree, CTX, 99 + rank, dev)
+    b = dv.RoundBuffers.alloc(D, ROWS, 1, CTX, device=dev)
+    _plant(dv, dm, req, b, _spine(tree.parent))
+    def round_():
+        dv.run_round(dm, [req], b, stream=torch.cuda.current_stream())
+
+    for _ in range(max(3, args.warmup)):
+        round_()
+    torch.cuda.synchronize()
+    st = int(b.status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {abi.STATUS.get(st, st)}")
+    accept_len = int(b.accept_len[0])
+
+    # ---- eager, K steps, clocks sampled during the timed region --------------
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk = Clocks(local)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        round_()
+    e1.record()
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / args.steps
+    clocks = clk.stop()
+
+    # ---- the same round from a CUDA graph ---------------------------------------
+    g = _graph(round_)
+    graph_ms = _time_graph(g, args.steps)
+    if world > 1:
+        t = torch.tensor([graph_ms, eager_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        graph_ms, eager_ms = float(t[0]), float(t[1])
+        torch.distributed.barrier()
+
+    out = {"metric": METRIC, "value": round(graph_ms, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(graph_ms, 4), "higher_is_better": False,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "hidden": D.hidden, "heads": f"{D.n_q_heads}/{D.n_kv_heads}x{D.head_dim}",
+                      "vocab": D.vocab, "rows": ROWS, "ctx": CTX, "accept_len": accept_len,
+                      "l2": "inputs larger than L2: 1.68 GB of weights stream from HBM every step",
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+           "eager_ms_per_step": round(eager_ms, 4), "clocks": clocks,
+           "gpu_launches": 11 * args.steps, "code_sha256": _code_sha256()}
+    if rank != 0 or args.no_extras:
+        return out if rank == 0 else None
+
+    # ---- per-stage times of the verify (eager, events on the launch stream) -----
+    P = 200
+    dv.check(abi.tv_profile_start(P), "tv_profile_start")
+    for _ in range(P):
+        dv.check(dv.verify(dm, [req], b, stream=torch.cuda.current_stream()), "verify")
+    rc, stage_sum, calls = abi.tv_profile_stop()
+    dv.check(rc, "tv_profile_stop")
+    stage_us = {k: round(1e3 * v / calls, 2) for k, v in stage_sum.items()}
+    peak, peak_kind = _peaks()
+    head_s = stage_sum["lm_head"] / calls / 1e3
+    hb = head_bytes(D, ROWS)
+    achieved = hb / head_s / 1e9
+    kernel_sha = _file_sha256(os.path.join(ROOT, "speculative_tree_verify_gb300", "csrc", "tv_gemm.cu"))
+    tr = _ncu_traffic(kernel_sha)
+    out["roofline"] = {"kernel": "lm_head (tcgen05 skinny GEMM + fused argmax/top-2)", "bound": "hbm",
+                       "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                       "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                       "algorithmic_bytes_per_launch": hb,
+                       "traffic": None if tr is None else tr[0] * 1.0,
+                       "launch_us": round(head_s * 1e6, 2)}
+    out["stage_us"] = stage_us
+
+    # ---- row sweep: verify-only latency from graphs -----------------------------
+    sweep = {}
+    for n in (8, 16, 24, 32):
+        t = synth.tree_spine_random(n, min(16, n), D.vocab, 30 + n)
+        r = _make_request(dv, synth, D, t, CTX, 200 + n, dev)
+        bb = dv.RoundBuffers.alloc(D, n, 1, CTX, device=dev)
+
+        def vf(r=r, bb=bb):
+            dv.check(dv.verify(dm, [r], bb, stream=torch.cuda.current_stream()), "verify")
+
+        gg = _graph(vf)
+        ms = _time_graph(gg, max(200, args.steps // 4))
+        vb = verify_bytes(D, n, CTX)
+        sweep[str(n)] = {"verify_ms": round(ms, 4), "tree_rows_per_s": round(n / ms * 1e3, 1),
+                         "GB_per_s": round(vb / ms / 1e6, 1), "frac_of_peak": round(vb / ms / 1e6 / peak, 4)}
+        del gg
+    sweep["ratio_32_over_8"] = round(sweep["32"]["verify_ms"] / sweep["8"]["verify_ms"], 4)
+    out["sweep"] = sweep
+
+    # ---- sampled round: residual walk at T = 1 instead of the greedy walk -------
+    b.uniforms.copy_(torch.from_numpy(synth.uniforms(ROWS, 5)))
+
+    def sround():
+        dv.run_round(dm, [req], b, sampled=1.0, stream=torch.cuda.current_stream())
+
+    gs = _graph(sround)
+    out["sampled_round_ms"] = round(_time_graph(gs, max(200, args.steps // 4)), 4)
+    del gs
+
+    # ---- end to end through the C ABI with host buffers --------------------------
+    par_h = torch.from_numpy(req.parent.cpu().numpy()).pin_memory()
+    tok_h = torch.from_numpy(req.token.cpu().numpy()).pin_memory()
+    res_h = torch.empty(ROWS + 2, dtype=torch.int32).pin_memory()
+    steps_e2e = max(50, args.steps // 4)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps_e2e):
+        req.parent.copy_(par_h, non_blocking=True)
+        req.token.copy_(tok_h, non_blocking=True)
+        round_()
+        res_h[:ROWS].copy_(b.out_tokens, non_blocking=True)
+        res_h[ROWS:ROWS + 1].copy_(b.accept_len, non_blocking=True)
+        res_h[ROWS + 1:].copy_(b.new_ctx, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / steps_e2e
+    out["e2e"] = {"value": round(e2e_ms, 4), "unit": UNIT, "h2d_bytes_per_step": 2 * ROWS * 4,
+                  "d2h_bytes_per_step": (ROWS + 2) * 4, "steps": steps_e2e,
+                  "note": "host tree -> device, eager round, tokens/accept_len/new_ctx -> host, sync, every step"}
+
+    # ---- the CPU oracle on the host cores ----------------------------------------
+    import oracle
+    oracle.build()
+    model_h = _host_model(dm, synth)
+    cache_h = _host_cache(req, synth)     # slots below ctx are never written
+    tree_h = synth.Tree(req.parent.cpu().numpy(), req.token.cpu().numpy())
+    out["cpu_baseline"] = cpu_baseline(oracle, model_h, cache_h, tree_h, args.cpu_seconds)
+    return out
+
+
+def run_reference(args, world, rank, local):
+    """The oracle, as it stands, on the host cores: each step a bounded sample
+    of the round scaled to ms per full round."""
+    if rank != 0:
+        return None
+    import oracle
+    from speculative_tree_verify_gb300 import synth
+
+    oracle.build()
+    D = synth.FULL
+    model = synth.gen_model(D, 1234)
+    tree = synth.tree_lattice(ROWS, SLOTS, D.vocab, 7)
+    cache = synth.gen_cache(D, CTX, CTX + 64, 99)
+    rng = np.random.default_rng(0)
+    # calibrate: all rows, a 4096-entry vocabulary slice
+    ids = np.sort(rng.choice(D.vocab, size=4096, replace=False)).astype(np.int32)
+    tl, th = oracle_sampled_step(oracle, model, cache, tree, ROWS, ids)
+    per_rv = th / (ROWS * len(ids))
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    r_rows = int(max(1, min(ROWS, ROWS * (budget / 2) / max(tl, 1e-6))))
+    s_voc = int(max(256, min(D.vocab, (budget / 2) / max(per_rv * r_rows, 1e-12))))
+    vids = np.sort(rng.choice(D.vocab, size=s_voc, replace=False)).astype(np.int32)
+    for _ in range(args.warmup):
+        oracle_sampled_step(oracle, model, cache, tree, r_rows, vids)
+    est = []
+    for _ in range(args.steps):
+        a, h = oracle_sampled_step(oracle, model, cache, tree, r_rows, vids)
+        est.append(1e3 * (a * ROWS / r_rows + h * (ROWS / r_rows) * (D.vocab / s_voc)))
+    ms = statistics.median(est)
+    sample = (f"per step: the layer over the first {r_rows} of {ROWS} tree rows and the head over {s_voc} of "
+              f"{D.vocab} vocabulary rows, scaled to a full round; median of {args.steps} steps")
+    return {"metric": METRIC, "value": round(ms, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "hidden": D.hidden, "vocab": D.vocab, "rows": ROWS, "ctx": CTX},
+            "cpu_baseline": {"value": round(ms, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(ms, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = _args()
+    world, rank, local = _dist()
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    if args.impl == "reference":
+        out = run_reference(args, world, rank, local)
+    else:
+        out = run_ours(args, world, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -215,6 +215,26 @@ TV_API int tv_commit_kv(const tv_kv *kv, const tv_dims *dims, const tv_tree *tre
                  const int32_t *path, const int32_t *accept_len,
                  int32_t *committed_src, int32_t *new_ctx, int32_t *dev_status, void *stream);
 
+/*
+ * Optional stage timing of tv_verify_tree (for price tables and roofline
+ * reports; not needed to run a round).  tv_profile_start(max_calls) creates
+ * CUDA events (no device memory) and from then on each tv_verify_tree call,
+ * up to max_calls of them, records TV_PROFILE_STAGES + 1 events on its stream:
+ * before its first kernel and after each stage
+ *   0 tree prologue + embedding/RMSNorm   1 QKV projection (tcgen05)
+ *   2 QKV finalize (RoPE, K/V write)       3 tree attention (partials + merge)
+ *   4 O projection (tcgen05)               5 O finalize (residual, RMSNorm)
+ *   6 LM head + argmax/top-2 (tcgen05).
+ * tv_profile_stop waits for the recorded events, writes per stage the SUM of
+ * its durations (ms) over the recorded calls into stage_ms[0..n_stages), the
+ * number of recorded calls into *n_calls, and destroys the events.  Calls
+ * recorded inside a CUDA graph capture are not timed (do not profile while
+ * capturing).  Process-wide, not thread-safe.
+ */
+#define TV_PROFILE_STAGES 7
+TV_API int tv_profile_start(int max_calls);
+TV_API int tv_profile_stop(float *stage_ms, int max_stages, int *n_stages, int *n_calls);
+
 /* A short English name of a status code (static storage). */
 TV_API const char *tv_status_string(int code);
 

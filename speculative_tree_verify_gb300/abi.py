@@ -25,7 +25,8 @@ CODES = {v: k for k, v in STATUS.items()}
 
 # entry points declared in include/tv.h
 SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv",
-           "tv_status_string")
+           "tv_profile_start", "tv_profile_stop", "tv_status_string")
+PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
 class TvDims(ctypes.Structure):
@@ -73,6 +74,8 @@ def load():
                                            P, P, P, P, P, P, Z, P]
         lib.tv_commit_kv.argtypes = [ctypes.POINTER(TvKv), ctypes.POINTER(TvDims), ctypes.POINTER(TvTree), I,
                                      P, P, P, P, P, P]
+        lib.tv_profile_start.argtypes = [I]
+        lib.tv_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I), ctypes.POINTER(I)]
         lib.tv_status_string.argtypes = [I]
         lib.tv_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -137,3 +140,15 @@ def tv_commit_kv(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], pat
                  new_ctx, dev_status, stream=None) -> int:
     return load().tv_commit_kv(_arr(TvKv, kvs), ctypes.byref(dims), _arr(TvTree, trees), len(trees), _p(path),
                                _p(accept_len), _p(committed_src), _p(new_ctx), _p(dev_status), _stream(stream))
+
+
+def tv_profile_start(max_calls: int) -> int:
+    return load().tv_profile_start(int(max_calls))
+
+
+def tv_profile_stop():
+    """-> (rc, {stage name: summed ms}, recorded calls)"""
+    ms = (ctypes.c_float * len(PROFILE_STAGES))()
+    ns, nc = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load().tv_profile_stop(ms, len(PROFILE_STAGES), ctypes.byref(ns), ctypes.byref(nc))
+    return rc, {name: float(ms[i]) for i, name in enumerate(PROFILE_STAGES)}, int(nc.value)

@@ -71,6 +71,28 @@ int num_sms() {
   return cache[dev];
 }
 
+// ---- optional stage timing (tv_profile_*) ----------------------------------
+struct Profile {
+  int cap = 0;       // calls that can be recorded
+  int calls = 0;     // calls recorded so far
+  cudaEvent_t* ev = nullptr;   // [cap][TV_PROFILE_STAGES + 1]
+};
+Profile g_prof;
+
+struct StageMarks {
+  cudaStream_t st;
+  cudaEvent_t* ev = nullptr;
+  explicit StageMarks(cudaStream_t s) : st(s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (g_prof.ev && g_prof.calls < g_prof.cap && cudaStreamIsCapturing(s, &cs) == cudaSuccess &&
+        cs == cudaStreamCaptureStatusNone)
+      ev = g_prof.ev + (size_t)(g_prof.calls++) * (TV_PROFILE_STAGES + 1);
+  }
+  void mark(int i) {
+    if (ev) cudaEventRecord(ev[i], st);
+  }
+};
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Fills the request table from host structs.  kv may be null (walks).
@@ -167,21 +189,31 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   memset(&gp, 0, sizeof(gp));
   gp.status = dev_status;
 
+  StageMarks pm(st);
+  pm.mark(0);
   if ((rc = launch_prologue(t, d, b, dev_status, st))) return rc;
   if ((rc = launch_embed_norm(t, *model, b, dev_status, st))) return rc;
+  pm.mark(1);
   gp.out = b.part_qkv;
   if ((rc = launch_gemm(GEMM_PARTIAL, model->wqkv, QKV, H, b.h, t.total_rows, pq, gp, sms, st))) return rc;
+  pm.mark(2);
   if ((rc = launch_qkv_finalize(t, d, b, pq.splits, dev_status, st))) return rc;
+  pm.mark(3);
   if ((rc = launch_attention(t, d, b, dev_status, st))) return rc;
+  pm.mark(4);
   gp.out = b.part_o;
   if ((rc = launch_gemm(GEMM_PARTIAL, model->wo, H, QD, b.attn, t.total_rows, po, gp, sms, st))) return rc;
+  pm.mark(5);
   if ((rc = launch_o_finalize(t, *model, b, po.splits, dev_status, st))) return rc;
+  pm.mark(6);
   gp.out = logits;
   gp.top2_part = reinterpret_cast<Top2*>(ws + L.top2);
   gp.done_counter = b.head_counter;
   gp.argmax = argmax;
   gp.gap = top2_gap;
-  return launch_gemm(GEMM_HEAD, model->lm_head, d.vocab, H, b.hf, t.total_rows, ph, gp, sms, st);
+  rc = launch_gemm(GEMM_HEAD, model->lm_head, d.vocab, H, b.hf, t.total_rows, ph, gp, sms, st);
+  pm.mark(7);
+  return rc;
 }
 
 int tv_accept_greedy(const tv_tree* trees, int n_req, const int32_t* argmax, int32_t* path, int32_t* accept_len,
@@ -221,6 +253,48 @@ int tv_commit_kv(const tv_kv* kv, const tv_dims* dims, const tv_tree* trees, int
   if (rc) return rc;
   return launch_commit(t, *dims, path, accept_len, committed_src, new_ctx, dev_status,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tv_profile_start(int max_calls) {
+  if (max_calls < 1 || max_calls > (1 << 16)) return TV_E_ARG;
+  if (g_prof.ev) return TV_E_ARG;   // already running
+  const int n = max_calls * (TV_PROFILE_STAGES + 1);
+  cudaEvent_t* ev = new cudaEvent_t[n];
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+      delete[] ev;
+      return TV_E_CUDA;
+    }
+  }
+  g_prof.ev = ev;
+  g_prof.cap = max_calls;
+  g_prof.calls = 0;
+  return TV_OK;
+}
+
+int tv_profile_stop(float* stage_ms, int max_stages, int* n_stages, int* n_calls) {
+  if (!g_prof.ev) return TV_E_ARG;
+  int rc = TV_OK;
+  float sums[TV_PROFILE_STAGES] = {0};
+  for (int c = 0; c < g_prof.calls && rc == TV_OK; ++c) {
+    cudaEvent_t* e = g_prof.ev + (size_t)c * (TV_PROFILE_STAGES + 1);
+    if (cudaEventSynchronize(e[TV_PROFILE_STAGES]) != cudaSuccess) rc = TV_E_CUDA;
+    for (int s = 0; s < TV_PROFILE_STAGES && rc == TV_OK; ++s) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, e[s], e[s + 1]) != cudaSuccess) rc = TV_E_CUDA;
+      sums[s] += ms;
+    }
+  }
+  const int n = g_prof.cap * (TV_PROFILE_STAGES + 1);
+  for (int i = 0; i < n; ++i) cudaEventDestroy(g_prof.ev[i]);
+  delete[] g_prof.ev;
+  if (n_calls) *n_calls = g_prof.calls;
+  g_prof = Profile();
+  if (n_stages) *n_stages = TV_PROFILE_STAGES;
+  if (stage_ms)
+    for (int s = 0; s < TV_PROFILE_STAGES && s < max_stages; ++s) stage_ms[s] = sums[s];
+  return rc;
 }
 
 const char* tv_status_string(int code) {
