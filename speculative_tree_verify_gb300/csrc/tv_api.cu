@@ -14,7 +14,7 @@ namespace {
 constexpr int kMaxHeadGrid = 1024;   // top-2 partial rows reserved in the workspace
 
 struct WsLayout {
-  size_t rstats, meta, rope, counter, h, q, part_qkv, attn_ml, attn_o, attn, part_o, hf, top2, total;
+  size_t rstats, meta, counter, h, q, part_qkv, attn_ml, attn_o, attn, part_o, hf, top2, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -35,7 +35,6 @@ WsLayout ws_layout(const tv_dims& d) {
   const GemmPlan po = plan_gemm((int)H, (int)QD, false);
   L.rstats = take((size_t)kMaxRows * n_vchunks(d.vocab) * sizeof(RowStat));
   L.meta = take(kMaxRows * sizeof(RowMeta));
-  L.rope = take((size_t)kMaxRows * (d.head_dim / 2) * sizeof(float2));
   L.counter = take(256);
   L.h = take(kMaxRows * H * 2);
   L.q = take(kMaxRows * QD * 2);
@@ -169,7 +168,6 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   LayerBufs b;
   b.meta = reinterpret_cast<RowMeta*>(ws + L.meta);
-  b.rope = reinterpret_cast<float2*>(ws + L.rope);
   b.head_counter = reinterpret_cast<unsigned int*>(ws + L.counter);
   b.h = reinterpret_cast<__nv_bfloat16*>(ws + L.h);
   b.q = reinterpret_cast<__nv_bfloat16*>(ws + L.q);

@@ -25,7 +25,9 @@ namespace tv {
 
 namespace {
 
-constexpr int kQPW = 20;   // query vectors per warp (8 warps -> 160 per KV head)
+constexpr int kQPW = 5;                  // query vectors per warp
+constexpr int kQPB = 8 * kQPW;           // query vectors per CTA (8 warps)
+constexpr int kQSplits = (kMaxQueriesPerKvHead + kQPB - 1) / kQPB;   // CTAs per (request, KV head, chunk)
 
 template <int D>
 struct AttnSmem {
@@ -35,7 +37,7 @@ struct AttnSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     attn_partial_kernel(ReqTable t, const RowMeta* meta, const __nv_bfloat16* q, int Hq, int Hkv, float scale,
                         float* part_ml, float* part_o, const int32_t* status) {
   constexpr int DP = AttnSmem<D>::DP;
@@ -49,7 +51,8 @@ __global__ void __launch_bounds__(256, 1)
   __shared__ uint32_t s_anc[32];
 
   if (block_skip(status)) return;
-  const int slot = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+  const int slot = blockIdx.x, g = blockIdx.y, r = blockIdx.z / kQSplits;
+  const int q0 = (blockIdx.z % kQSplits) * kQPB;   // this CTA's first query vector
   const int ctx = t.ctx[r], n = t.n[r], row0 = t.row_off[r];
   const bool tree = slot == kTreeSlot;
   if (!tree && slot >= attn_n_chunks(ctx)) return;
@@ -64,19 +67,20 @@ __global__ void __launch_bounds__(256, 1)
   }
   const int G = Hq / Hkv;
   const int nq = n * G;
+  if (q0 >= nq) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int nqw = 0;   // valid query vectors of this warp: qi = warp + 8 a
+  int nqw = 0;   // valid query vectors of this warp: qi = q0 + warp + 8 a
   for (int a = 0; a < kQPW; ++a)
-    if (warp + 8 * a < nq) nqw = a + 1;
+    if (q0 + warp + 8 * a < nq) nqw = a + 1;
 
   for (int idx = threadIdx.x; idx < NQ * D; idx += 256) {
-    const int qi = idx / D, d = idx - (idx / D) * D;
+    const int qi = q0 + idx / D, d = idx - (idx / D) * D;
     float v = 0.f;
     if (qi < nq) {
       const int local = qi / G, hq = g * G + qi % G;
       v = bf2f(q[((size_t)(row0 + local) * Hq + hq) * D + d]);
     }
-    Qs[qi * DP + d] = v;
+    Qs[(qi - q0) * DP + d] = v;
   }
   if (threadIdx.x < 32) s_anc[threadIdx.x] = (int)threadIdx.x < n ? meta[row0 + threadIdx.x].anc : 0u;
 
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
     for (int a = 0; a < kQPW; ++a) {
       if (a < nqw) {
-        const int local = (warp + 8 * a) / G;
+        const int local = (q0 + warp + 8 * a) / G;
         const bool vis = kvalid && (!tree || ((s_anc[local] >> j) & 1u));
         const float sc = vis ? s[a] * scale : -INFINITY;
         const float mnew = fmaxf(m[a], warp_max(sc));
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
   for (int a = 0; a < kQPW; ++a) {
     if (a < nqw) {
-      const int qi = warp + 8 * a;
+      const int qi = q0 + warp + 8 * a;
       const float lt = warp_sum(l[a]);
       const int local = qi / G, hq = g * G + qi % G;
       const size_t base = ((size_t)(row0 + local) * Hq + hq) * kChunkSlots + slot;
@@ -221,7 +225,7 @@ int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b,
       return TV_E_CUDA;
     attr = true;
   }
-  dim3 grid(kChunkSlots, dm.n_kv_heads, t.n_req);
+  dim3 grid(kChunkSlots, dm.n_kv_heads, t.n_req * kQSplits);
   attn_partial_kernel<D><<<grid, 256, smem, st>>>(t, b.meta, b.q, dm.n_q_heads, dm.n_kv_heads,
                                                   1.0f / sqrtf((float)D), b.attn_ml, b.attn_o, status);
   if (cudaGetLastError() != cudaSuccess) return TV_E_CUDA;

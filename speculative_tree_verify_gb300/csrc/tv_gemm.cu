@@ -32,6 +32,7 @@
 
 #include "tv_common.cuh"
 #include "tv_gemm.cuh"
+#include "tv_kernels.cuh"
 
 namespace tv {
 
@@ -301,6 +302,7 @@ GemmPlan plan_gemm(int M, int K, bool head) {
     int splits = target_units / tiles;
     if (splits < 1) splits = 1;
     if (splits > KB) splits = KB;
+    if (splits > kMaxSplits) splits = kMaxSplits;
     pl.kb_per_split = (KB + splits - 1) / splits;
     pl.splits = (KB + pl.kb_per_split - 1) / pl.kb_per_split;
   }

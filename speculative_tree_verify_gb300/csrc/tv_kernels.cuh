@@ -62,9 +62,18 @@ __device__ __forceinline__ int validate_tree_warp(const int32_t* parent, const i
 }
 
 // ---- launchers (host) -------------------------------------------------------
+// RoPE frequencies theta^(-2d/D), computed in double on the host and split
+// into hi + lo floats, and 2*pi split into two floats for the reduction.
+struct RopeParams {
+  float f_hi[64];
+  float f_lo[64];
+  float two_pi_hi, two_pi_lo, inv_two_pi;
+};
+
+constexpr int kMaxSplits = 16;   // split-K partials summed by the finalize kernels
+
 struct LayerBufs {
   RowMeta* meta;
-  float2* rope;
   unsigned int* head_counter;
   __nv_bfloat16* h;        // [32][H]
   __nv_bfloat16* q;        // [32][Hq][D]

@@ -1,6 +1,8 @@
 // Per-row kernels of the verify pass: the tree prologue, embedding + RMSNorm,
 // and the two finalizers that sum the projections' split-K partials in a fixed
 // order (QKV + RoPE + tree K/V write; O + residual + final RMSNorm).
+#include <cmath>
+
 #include "tv_common.cuh"
 #include "tv_kernels.cuh"
 
@@ -8,15 +10,16 @@ namespace tv {
 
 namespace {
 
+constexpr int kRowThreads = 512;   // one block per row for the row-wise kernels
+constexpr int kRowVecs = 4;        // uint4 (8 bf16) vectors per thread: hidden <= 16384
+
 // ---------------------------------------------------------------------------
-// prologue: one warp per request.  Validates the tree, computes per row the
+// prologue: one warp per request.  Validates the tree and computes per row the
 // depth, position ctx + depth and ancestor set (node i sees its ancestors and
 // itself: "an attention mask of its ancestors and a position equal to its
-// depth" [Drafters and tree verify, §Tree verify through recurrent layers]),
-// and the RoPE rotation of each row's position (angles in fp64).
+// depth" [Drafters and tree verify, §Tree verify through recurrent layers]).
 // ---------------------------------------------------------------------------
-__global__ void prologue_kernel(ReqTable t, int vocab, int head_dim, float rope_theta, RowMeta* meta,
-                                float2* rope_cs, unsigned int* head_counter, int32_t* status) {
+__global__ void prologue_kernel(ReqTable t, int vocab, RowMeta* meta, unsigned int* head_counter, int32_t* status) {
   __shared__ int s_depth[32];
   __shared__ uint32_t s_anc[32];
   const int r = blockIdx.x;
@@ -42,63 +45,104 @@ __global__ void prologue_kernel(ReqTable t, int vocab, int head_dim, float rope_
     }
     __syncwarp();
   }
-  const int row0 = t.row_off[r];
-  const int ctx = t.ctx[r];
   if (lane < n) {
     RowMeta m;
     m.req = r;
     m.local = lane;
     m.token = tok;
     m.depth = s_depth[lane];
-    m.pos = ctx + s_depth[lane];
+    m.pos = t.ctx[r] + s_depth[lane];
     m.anc = s_anc[lane];
-    meta[row0 + lane] = m;
-  }
-  const int half = head_dim / 2;
-  for (int i = 0; i < n; ++i) {
-    const double pos = (double)(ctx + s_depth[i]);
-    for (int d = lane; d < half; d += 32) {
-      const double inv_freq = pow((double)rope_theta, -2.0 * (double)d / (double)head_dim);
-      double sn, cs;
-      sincos(pos * inv_freq, &sn, &cs);
-      rope_cs[(size_t)(row0 + i) * half + d] = make_float2((float)cs, (float)sn);
-    }
+    meta[t.row_off[r] + lane] = m;
   }
 }
 
-template <int NT>
 __device__ __forceinline__ float block_sum(float v, float* red) {
   v = warp_sum(v);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (l == 0) red[w] = v;
   __syncthreads();
   if (w == 0) {
-    float s = l < NT / 32 ? red[l] : 0.f;
+    float s = l < (int)(blockDim.x >> 5) ? red[l] : 0.f;
     s = warp_sum(s);
-    if (l == 0) red[NT / 32] = s;
+    if (l == 0) red[32] = s;
   }
   __syncthreads();
-  const float s = red[NT / 32];
+  const float s = red[32];
   __syncthreads();
   return s;
 }
 
-// h = bf16( x / sqrt(mean(x^2) + eps) * g ), x = E[token]; one block per row
-__global__ void __launch_bounds__(256) embed_norm_kernel(const RowMeta* meta, const __nv_bfloat16* embed,
-                                                         const __nv_bfloat16* g, int H, float eps,
-                                                         __nv_bfloat16* h, const int32_t* status) {
-  __shared__ float red[16];
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(p[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+// h = bf16( x / sqrt(mean(x^2) + eps) * g ), x = E[token]; one block per row,
+// each thread holds up to kRowVecs 8-element vectors of the row.
+__global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const RowMeta* meta, const __nv_bfloat16* embed,
+                                                                 const __nv_bfloat16* g, int H, float eps,
+                                                                 __nv_bfloat16* h, const int32_t* status) {
+  __shared__ float red[33];
   if (block_skip(status)) return;
   const int row = blockIdx.x;
-  const __nv_bfloat16* x = embed + (size_t)meta[row].token * H;
+  const int nvec = H / 8;
+  const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)meta[row].token * H);
+  float xf[kRowVecs][8];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += 256) {
-    const float v = bf2f(x[c]);
-    ss += v * v;
+#pragma unroll
+  for (int k = 0; k < kRowVecs; ++k) {
+    const int vi = threadIdx.x + k * kRowThreads;
+    if (vi < nvec) {
+      unpack8(x[vi], xf[k]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += xf[k][e] * xf[k][e];
+    }
   }
-  ss = block_sum<256>(ss, red);
+  ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-  for (int c = threadIdx.x; c < H; c += 256) h[(size_t)row * H + c] = f2bf(bf2f(x[c]) * inv * bf2f(g[c]));
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+  uint4* hv = reinterpret_cast<uint4*>(h + (size_t)row * H);
+#pragma unroll
+  for (int k = 0; k < kRowVecs; ++k) {
+    const int vi = threadIdx.x + k * kRowThreads;
+    if (vi < nvec) {
+      float gf[8], y[8];
+      unpack8(gv[vi], gf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = xf[k][e] * inv * gf[e];
+      hv[vi] = pack8(y);
+    }
+  }
+}
+
+// RoPE angle pos * f reduced to about [-pi, pi] in fp32 without fp64: f is
+// carried as f_hi + f_lo; the product pos * f_hi is split into its rounded
+// value and its exact rounding error (one fma); the multiple of 2 pi is taken
+// off with a two-constant Cody-Waite reduction (2 pi = hi + lo), each step an
+// fma with one rounding.  Error about 3e-7 rad for positions below 2^24.
+__device__ __forceinline__ float rope_angle(int pos, float f_hi, float f_lo, const RopeParams& rp) {
+  const float p = (float)pos;
+  const float a = p * f_hi;
+  const float a_err = fmaf(p, f_hi, -a);
+  const float corr = fmaf(p, f_lo, a_err);
+  const float k = rintf(a * rp.inv_two_pi);
+  float r = fmaf(-k, rp.two_pi_hi, a);
+  r = fmaf(-k, rp.two_pi_lo, r);
+  return r + corr;
 }
 
 // qkv: sum the split-K partials in split order, rotate q and k by RoPE
@@ -107,25 +151,37 @@ __global__ void __launch_bounds__(256) embed_norm_kernel(const RowMeta* meta, co
 // its depth-first slot" [Drafters and tree verify, §Tree verify through
 // recurrent layers]).  grid (rows, Hq + 2 Hkv), block D/2.
 __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float* part, int splits, int Hq, int Hkv,
-                                    int D, const float2* rope_cs, __nv_bfloat16* q_out, const int32_t* status) {
+                                    int D, RopeParams rp, __nv_bfloat16* q_out, const int32_t* status) {
   if (block_skip(status)) return;
   const int row = blockIdx.x, head = blockIdx.y, d = threadIdx.x;
   const int half = D / 2;
   const int M = (Hq + 2 * Hkv) * D;
   const int f1 = head * D + d, f2 = f1 + half;
-  float x1 = 0.f, x2 = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float* ps = part + ((size_t)s * kMaxRows + row) * M;
-    x1 += ps[f1];
-    x2 += ps[f2];
+  float p1[kMaxSplits], p2[kMaxSplits];
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    if (s < splits) {
+      const float* ps = part + ((size_t)s * kMaxRows + row) * M;
+      p1[s] = ps[f1];
+      p2[s] = ps[f2];
+    }
   }
-  float y1 = x1, y2 = x2;
-  if (head < Hq + Hkv) {
-    const float2 cs = rope_cs[(size_t)row * half + d];
-    y1 = x1 * cs.x - x2 * cs.y;
-    y2 = x2 * cs.x + x1 * cs.y;
+  float x1 = 0.f, x2 = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxSplits; ++s) {
+    if (s < splits) {
+      x1 += p1[s];
+      x2 += p2[s];
+    }
   }
   const RowMeta m = meta[row];
+  float y1 = x1, y2 = x2;
+  if (head < Hq + Hkv) {
+    float sn, cs;
+    sincosf(rope_angle(m.pos, rp.f_hi[d], rp.f_lo[d], rp), &sn, &cs);
+    y1 = x1 * cs - x2 * sn;
+    y2 = x2 * cs + x1 * sn;
+  }
   __nv_bfloat16* dst;
   if (head < Hq) {
     dst = q_out + ((size_t)row * Hq + head) * D;
@@ -139,70 +195,125 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
   dst[d + half] = f2bf(y2);
 }
 
-// O projection finalize: r = bf16(x + sum_s partial_s), hf = bf16(RMSNorm(r) g_f);
-// one block per row
-__global__ void __launch_bounds__(256) o_finalize_kernel(const RowMeta* meta, const float* part, int splits, int H,
-                                                         const __nv_bfloat16* embed, const __nv_bfloat16* g,
-                                                         float eps, __nv_bfloat16* hf, const int32_t* status) {
-  extern __shared__ float rbuf[];   // [H]
-  __shared__ float red[16];
+// O projection finalize: r = bf16(x + sum_s partial_s) with the splits summed in
+// order, hf = bf16(RMSNorm(r) g_f); one block per row.
+__global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(const RowMeta* meta, const float* part, int splits,
+                                                                 int H, const __nv_bfloat16* embed,
+                                                                 const __nv_bfloat16* g, float eps,
+                                                                 __nv_bfloat16* hf, const int32_t* status) {
+  __shared__ float red[33];
   if (block_skip(status)) return;
   const int row = blockIdx.x;
-  const __nv_bfloat16* x = embed + (size_t)meta[row].token * H;
+  const int nvec = H / 8;
+  const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)meta[row].token * H);
+  float r[kRowVecs][8];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += 256) {
-    float o = 0.f;
-    for (int s = 0; s < splits; ++s) o += part[((size_t)s * kMaxRows + row) * H + c];
-    const float r = bf2f(f2bf(bf2f(x[c]) + o));
-    rbuf[c] = r;
-    ss += r * r;
+#pragma unroll
+  for (int k = 0; k < kRowVecs; ++k) {
+    const int vi = threadIdx.x + k * kRowThreads;
+    if (vi < nvec) {
+      // partials summed in split order; loads issued four splits at a time
+      float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int s0 = 0; s0 < splits; s0 += 4) {
+        float4 pv[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (s0 + j < splits) {
+            const float4* ps =
+                reinterpret_cast<const float4*>(part + ((size_t)(s0 + j) * kMaxRows + row) * H) + 2 * vi;
+            pv[j][0] = ps[0];
+            pv[j][1] = ps[1];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (s0 + j < splits) {
+            o[0] += pv[j][0].x; o[1] += pv[j][0].y; o[2] += pv[j][0].z; o[3] += pv[j][0].w;
+            o[4] += pv[j][1].x; o[5] += pv[j][1].y; o[6] += pv[j][1].z; o[7] += pv[j][1].w;
+          }
+        }
+      }
+      float xf[8];
+      unpack8(x[vi], xf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        r[k][e] = bf2f(f2bf(xf[e] + o[e]));
+        ss += r[k][e] * r[k][e];
+      }
+    }
   }
-  ss = block_sum<256>(ss, red);
+  ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-  for (int c = threadIdx.x; c < H; c += 256) hf[(size_t)row * H + c] = f2bf(rbuf[c] * inv * bf2f(g[c]));
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+  uint4* hv = reinterpret_cast<uint4*>(hf + (size_t)row * H);
+#pragma unroll
+  for (int k = 0; k < kRowVecs; ++k) {
+    const int vi = threadIdx.x + k * kRowThreads;
+    if (vi < nvec) {
+      float gf[8], y[8];
+      unpack8(gv[vi], gf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = r[k][e] * inv * gf[e];
+      hv[vi] = pack8(y);
+    }
+  }
 }
 
 inline int last_error() { return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA; }
 
+RopeParams rope_params(int head_dim, float theta) {
+  RopeParams rp;
+  const double two_pi = 8.0 * std::atan(1.0);
+  for (int d = 0; d < 64; ++d) {
+    const double f = d < head_dim / 2 ? std::pow((double)theta, -2.0 * d / (double)head_dim) : 0.0;
+    rp.f_hi[d] = (float)f;
+    rp.f_lo[d] = (float)(f - (double)rp.f_hi[d]);
+  }
+  rp.two_pi_hi = (float)two_pi;
+  rp.two_pi_lo = (float)(two_pi - (double)rp.two_pi_hi);
+  rp.inv_two_pi = (float)(1.0 / two_pi);
+  return rp;
+}
+
 }  // namespace
 
 int launch_prologue(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st) {
-  prologue_kernel<<<t.n_req, 32, 0, st>>>(t, d.vocab, d.head_dim, d.rope_theta, b.meta, b.rope, b.head_counter,
-                                           status);
+  prologue_kernel<<<t.n_req, 32, 0, st>>>(t, d.vocab, b.meta, b.head_counter, status);
   return last_error();
 }
 
 int launch_embed_norm(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status, cudaStream_t st) {
-  embed_norm_kernel<<<t.total_rows, 256, 0, st>>>(b.meta, reinterpret_cast<const __nv_bfloat16*>(m.embed),
-                                                   reinterpret_cast<const __nv_bfloat16*>(m.ln1), m.dims.hidden,
-                                                   m.dims.rms_eps, b.h, status);
+  if (m.dims.hidden > kRowVecs * kRowThreads * 8) return TV_E_UNSUPPORTED;
+  embed_norm_kernel<<<t.total_rows, kRowThreads, 0, st>>>(b.meta, reinterpret_cast<const __nv_bfloat16*>(m.embed),
+                                                          reinterpret_cast<const __nv_bfloat16*>(m.ln1),
+                                                          m.dims.hidden, m.dims.rms_eps, b.h, status);
   return last_error();
 }
 
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
                         cudaStream_t st) {
+  static RopeParams cached;
+  static int cached_dim = -1;
+  static float cached_theta = 0.f;
+  if (cached_dim != d.head_dim || cached_theta != d.rope_theta) {
+    cached = rope_params(d.head_dim, d.rope_theta);
+    cached_dim = d.head_dim;
+    cached_theta = d.rope_theta;
+  }
+  if (splits > kMaxSplits) return TV_E_UNSUPPORTED;
   dim3 grid(t.total_rows, d.n_q_heads + 2 * d.n_kv_heads);
   qkv_finalize_kernel<<<grid, d.head_dim / 2, 0, st>>>(t, b.meta, b.part_qkv, splits, d.n_q_heads, d.n_kv_heads,
-                                                       d.head_dim, b.rope, b.q, status);
+                                                       d.head_dim, cached, b.q, status);
   return last_error();
 }
 
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st) {
-  const size_t smem = (size_t)m.dims.hidden * sizeof(float);
-  if (smem > 48 * 1024) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(o_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
-        return TV_E_CUDA;
-      attr = true;
-    }
-  }
-  o_finalize_kernel<<<t.total_rows, 256, smem, st>>>(b.meta, b.part_o, splits, m.dims.hidden,
-                                                     reinterpret_cast<const __nv_bfloat16*>(m.embed),
-                                                     reinterpret_cast<const __nv_bfloat16*>(m.ln_f),
-                                                     m.dims.rms_eps, b.hf, status);
+  if (m.dims.hidden > kRowVecs * kRowThreads * 8 || splits > kMaxSplits) return TV_E_UNSUPPORTED;
+  o_finalize_kernel<<<t.total_rows, kRowThreads, 0, st>>>(b.meta, b.part_o, splits, m.dims.hidden,
+                                                          reinterpret_cast<const __nv_bfloat16*>(m.embed),
+                                                          reinterpret_cast<const __nv_bfloat16*>(m.ln_f),
+                                                          m.dims.rms_eps, b.hf, status);
   return last_error();
 }
 
