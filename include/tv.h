@@ -197,6 +197,26 @@ TV_API int tv_accept_residual(const tv_tree *trees, int n_req, const float *logi
                        int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * tv_accept_residual without a workspace.  The pages have no counterpart: this
+ * is for callers that cannot provide device memory -- a plugin step inside
+ * another framework's executor that may not call cudaMalloc, a real-time loop
+ * with a no-allocation rule, a caller holding only a stream and the round's
+ * buffers.  Same walk, same kernels and same results as tv_accept_residual; the
+ * per-row softmax statistics live instead in a 16 KB array inside the
+ * library's device image (one per GPU, held until the process exits), so:
+ *   - vocab may be at most 262144 (TV_E_UNSUPPORTED above that);
+ *   - the first call on a device looks up that array's address
+ *     (cudaGetSymbolAddress) -- make it before any stream capture;
+ *   - all calls on a device share the array: calls whose kernels overlap on the
+ *     GPU race; order them on one stream.
+ * Nothing is allocated.  Arguments and errors as tv_accept_residual.
+ */
+TV_API int tv_accept_residual_noalloc(const tv_tree *trees, int n_req, const float *logits, int32_t vocab,
+                                      float temperature, const float *uniforms, int bonus_at_leaf,
+                                      int32_t *path, int32_t *accept_len, int32_t *out_tokens,
+                                      int32_t *out_count, int32_t *dev_status, void *stream);
+
+/*
  * KV commit [Drafters and tree verify, §The round, step 4; §Tree verify through
  * recurrent layers, last paragraph]: keep the accepted path's KV rows and drop
  * the rest -- for d = 0..a_r, copy slot ctx_len + path[d] to slot ctx_len + d,

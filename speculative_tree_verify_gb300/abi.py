@@ -25,7 +25,7 @@ CODES = {v: k for k, v in STATUS.items()}
 
 # entry points declared in include/tv.h
 SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv",
-           "tv_profile_start", "tv_profile_stop", "tv_status_string")
+           "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -72,6 +72,8 @@ def load():
         lib.tv_accept_greedy.argtypes = [ctypes.POINTER(TvTree), I, P, P, P, P, P, P]
         lib.tv_accept_residual.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float, P, I,
                                            P, P, P, P, P, P, Z, P]
+        lib.tv_accept_residual_noalloc.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float, P,
+                                                   I, P, P, P, P, P, P]
         lib.tv_commit_kv.argtypes = [ctypes.POINTER(TvKv), ctypes.POINTER(TvDims), ctypes.POINTER(TvTree), I,
                                      P, P, P, P, P, P]
         lib.tv_profile_start.argtypes = [I]
@@ -134,6 +136,17 @@ def tv_accept_residual(trees: Sequence[TvTree], logits, vocab: int, temperature:
                                      _p(uniforms), 1 if bonus_at_leaf else 0, _p(path), _p(accept_len),
                                      _p(out_tokens), _p(out_count), _p(dev_status), _p(workspace),
                                      int(workspace_bytes), _stream(stream))
+
+
+def tv_accept_residual_noalloc(trees: Sequence[TvTree], logits, vocab: int, temperature: float, uniforms,
+                               bonus_at_leaf: bool, path, accept_len, out_tokens, out_count, dev_status,
+                               stream=None) -> int:
+    """tv_accept_residual for callers that cannot provide a workspace (the
+    statistics live in a fixed 16 KB array inside the library; vocab <= 262144)."""
+    return load().tv_accept_residual_noalloc(_arr(TvTree, trees), len(trees), _p(logits), int(vocab),
+                                             float(temperature), _p(uniforms), 1 if bonus_at_leaf else 0,
+                                             _p(path), _p(accept_len), _p(out_tokens), _p(out_count),
+                                             _p(dev_status), _stream(stream))
 
 
 def tv_commit_kv(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], path, accept_len, committed_src,
