@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(256, 2)
   float* Ps = Vs + 32 * D;                       // [8][kQPW][32]
   __shared__ uint32_t s_anc[32];
 
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int slot = blockIdx.x, g = blockIdx.y, r = blockIdx.z / kQSplits;
   const int q0 = (blockIdx.z % kQSplits) * kQPB;   // this CTA's first query vector
@@ -198,6 +200,8 @@ __global__ void __launch_bounds__(256, 2)
 // chunks in order 0..nch-1, then the tree slot.  grid (rows, Hq), block D.
 __global__ void attn_merge_kernel(ReqTable t, const RowMeta* meta, int Hq, int D, const float* part_ml,
                                   const float* part_o, __nv_bfloat16* out, const int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x, hq = blockIdx.y, d = threadIdx.x;
   const int nch = attn_n_chunks(t.ctx[meta[row].req]);
@@ -218,20 +222,15 @@ template <int D>
 int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b, int32_t* status,
                        cudaStream_t st) {
   const size_t smem = AttnSmem<D>::bytes;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_partial_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return TV_E_CUDA;
-    attr = true;
-  }
+  static bool attr[64] = {false};
+  if (ensure_smem_limit(attn_partial_kernel<D>, smem, attr)) return TV_E_CUDA;
   dim3 grid(kChunkSlots, dm.n_kv_heads, t.n_req * kQSplits);
-  attn_partial_kernel<D><<<grid, 256, smem, st>>>(t, b.meta, b.q, dm.n_q_heads, dm.n_kv_heads,
-                                                  1.0f / sqrtf((float)D), b.attn_ml, b.attn_o, status);
-  if (cudaGetLastError() != cudaSuccess) return TV_E_CUDA;
-  attn_merge_kernel<<<dim3(t.total_rows, dm.n_q_heads), D, 0, st>>>(t, b.meta, dm.n_q_heads, D, b.attn_ml,
-                                                                    b.attn_o, b.attn, status);
-  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA;
+  int rc = launch_pdl(attn_partial_kernel<D>, grid, dim3(256), smem, st, t, (const RowMeta*)b.meta,
+                      (const __nv_bfloat16*)b.q, dm.n_q_heads, dm.n_kv_heads, 1.0f / sqrtf((float)D), b.attn_ml,
+                      b.attn_o, (const int32_t*)status);
+  if (rc) return rc;
+  return launch_pdl(attn_merge_kernel, dim3(t.total_rows, dm.n_q_heads), dim3(D), 0, st, t, (const RowMeta*)b.meta,
+                    dm.n_q_heads, D, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn, (const int32_t*)status);
 }
 
 }  // namespace

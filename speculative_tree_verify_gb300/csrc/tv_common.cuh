@@ -13,6 +13,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/tv.h"
 
 namespace tv {
@@ -104,6 +106,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Raise the transaction count of the current phase without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -247,6 +254,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation: it may start while the previous kernel in
+// the stream finishes.  Before pdl_wait() a kernel only does set-up that
+// touches no global memory written by earlier kernels, and writes no global
+// memory at all (weights, which no kernel writes, may be read).  pdl_wait()
+// returns once the previous grid has completed and its writes are visible;
+// since every kernel waits before it completes, that covers all earlier grids.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // misc
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -262,6 +281,36 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Host: raise a kernel's dynamic shared memory limit once per device.
+template <typename... Exp>
+inline int ensure_smem_limit(void (*kernel)(Exp...), size_t bytes, bool (&done)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TV_E_CUDA;
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+      return TV_E_CUDA;
+    done[dev] = true;
+  }
+  return TV_OK;
+}
+
+// Host: launch with programmatic stream serialisation allowed.
+template <typename... Exp, typename... Act>
+inline int launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...) == cudaSuccess ? TV_OK : TV_E_CUDA;
 }
 
 }  // namespace tv

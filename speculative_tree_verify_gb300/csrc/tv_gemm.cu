@@ -74,10 +74,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (threadIdx.x == 0) *s_status = status_get(p.status);
-  __syncthreads();
-  if (*s_status != 0) return;
-
+  // ---- set-up: nothing here reads data written by an earlier kernel ----------
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
@@ -100,37 +97,90 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
 
   const int KB = p.K / BK;
+  // this CTA's work items in order: units blockIdx.x + i * gridDim.x, their k-blocks
+  auto unit_kb = [&](int u, int& kb0, int& kb1) {
+    kb0 = (u % p.splits) * p.kb_per_split;
+    kb1 = min(KB, kb0 + p.kb_per_split);
+  };
+
+  // The producer starts streaming weights (never written by any kernel) into
+  // the first stages before the previous kernel has finished.
+  int pre = 0;
+  int pre_u = blockIdx.x, pre_kb = 0, pre_kb1 = 0;
+  uint64_t pol_w = 0, pol_x = 0;
+  if (warp == 0 && lane == 0) {
+    pol_w = policy_evict_first();
+    pol_x = policy_evict_last();
+    if (pre_u < p.n_units) unit_kb(pre_u, pre_kb, pre_kb1);
+    int u = pre_u, kb = pre_kb, kb1 = pre_kb1;
+    while (pre < STAGES && u < p.n_units) {
+      mbar_expect_tx(&full[pre], A_BYTES);
+      tma_load_2d(sA + (size_t)pre * A_BYTES, &mapA, &full[pre], kb * BK, (u / p.splits) * BM, pol_w);
+      ++pre;
+      if (++kb >= kb1) {
+        u += gridDim.x;
+        if (u < p.n_units) unit_kb(u, kb, kb1);
+      }
+    }
+  }
+
+  pdl_wait();
+  if (threadIdx.x == 0) *s_status = status_get(p.status);
+  __syncthreads();
+  if (*s_status != 0) {
+    if (warp == 0 && lane == 0) {   // let the weight loads already in flight land
+      for (int s = 0; s < pre; ++s) {
+        mbar_arrive(&full[s]);
+        mbar_wait(&full[s], 0);
+      }
+    }
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    return;
+  }
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_x = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t armed = 0;   // bit s: stage s was armed at least once
+      uint32_t armed = 0;      // bit s: stage s was armed at least once
       uint32_t last_par = 0;   // bit s: parity of stage s's last armed phase
+      // activations of the pre-issued stages
+      int u = pre_u, kb = pre_kb, kb1 = pre_kb1;
+      for (int s = 0; s < pre; ++s) {
+        mbar_arrive_expect_tx(&full[s], B_BYTES);
+        tma_load_2d(sB + (size_t)s * B_BYTES, &mapB, &full[s], kb * BK, 0, pol_x);
+        armed |= 1u << s;
+        if (++kb >= kb1) {
+          u += gridDim.x;
+          if (u < p.n_units) unit_kb(u, kb, kb1);
+        }
+      }
+      int stage = pre % STAGES;
+      uint32_t phase = pre == STAGES ? 1u : 0u;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        const int mt = u / p.splits, sp = u % p.splits;
-        const int kb0 = sp * p.kb_per_split;
-        const int kb1 = min(KB, kb0 + p.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
-          tma_load_2d(sA + (size_t)stage * A_BYTES, &mapA, &full[stage], kb * BK, mt * BM, pol_w);
-          tma_load_2d(sB + (size_t)stage * B_BYTES, &mapB, &full[stage], kb * BK, 0, pol_x);
-          armed |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+      while (u < p.n_units && ok) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+        tma_load_2d(sA + (size_t)stage * A_BYTES, &mapA, &full[stage], kb * BK, (u / p.splits) * BM, pol_w);
+        tma_load_2d(sB + (size_t)stage * B_BYTES, &mapB, &full[stage], kb * BK, 0, pol_x);
+        armed |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++kb >= kb1) {
+          u += gridDim.x;
+          if (u < p.n_units) unit_kb(u, kb, kb1);
         }
       }
       if (!ok) status_set(p.status, TV_E_TIMEOUT);
@@ -363,25 +413,14 @@ int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows
   p.n_units = pl.n_units;
   const int grid = pl.n_units < num_sms ? pl.n_units : num_sms;
   if (mode == GEMM_HEAD) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(gemm_skinny_kernel<GEMM_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)SMEM_BYTES) != cudaSuccess)
-        return TV_E_CUDA;
-      attr = true;
-    }
-    gemm_skinny_kernel<GEMM_HEAD><<<grid, THREADS, SMEM_BYTES, stream>>>(mA, mB, p);
+    static bool attr[64] = {false};
+    if (ensure_smem_limit(gemm_skinny_kernel<GEMM_HEAD>, SMEM_BYTES, attr)) return TV_E_CUDA;
+    return launch_pdl(gemm_skinny_kernel<GEMM_HEAD>, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, mA, mB, p);
   } else {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(gemm_skinny_kernel<GEMM_PARTIAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)SMEM_BYTES) != cudaSuccess)
-        return TV_E_CUDA;
-      attr = true;
-    }
-    gemm_skinny_kernel<GEMM_PARTIAL><<<grid, THREADS, SMEM_BYTES, stream>>>(mA, mB, p);
+    static bool attr[64] = {false};
+    if (ensure_smem_limit(gemm_skinny_kernel<GEMM_PARTIAL>, SMEM_BYTES, attr)) return TV_E_CUDA;
+    return launch_pdl(gemm_skinny_kernel<GEMM_PARTIAL>, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, mA, mB, p);
   }
-  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA;
 }
 
 }  // namespace tv

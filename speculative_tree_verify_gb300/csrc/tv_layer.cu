@@ -24,6 +24,8 @@ __global__ void prologue_kernel(ReqTable t, int vocab, RowMeta* meta, unsigned i
   __shared__ uint32_t s_anc[32];
   const int r = blockIdx.x;
   const int lane = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (status_get(status) != 0) return;
   if (r == 0 && lane == 0) *head_counter = 0u;
   const int n = t.n[r];
@@ -97,6 +99,8 @@ __global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const RowMeta* 
                                                                  const __nv_bfloat16* g, int H, float eps,
                                                                  __nv_bfloat16* h, const int32_t* status) {
   __shared__ float red[33];
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x;
   const int nvec = H / 8;
@@ -152,6 +156,8 @@ __device__ __forceinline__ float rope_angle(int pos, float f_hi, float f_lo, con
 // recurrent layers]).  grid (rows, Hq + 2 Hkv), block D/2.
 __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float* part, int splits, int Hq, int Hkv,
                                     int D, RopeParams rp, __nv_bfloat16* q_out, const int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x, head = blockIdx.y, d = threadIdx.x;
   const int half = D / 2;
@@ -202,6 +208,8 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(const RowMeta* 
                                                                  const __nv_bfloat16* g, float eps,
                                                                  __nv_bfloat16* hf, const int32_t* status) {
   __shared__ float red[33];
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x;
   const int nvec = H / 8;
@@ -259,8 +267,6 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(const RowMeta* 
   }
 }
 
-inline int last_error() { return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA; }
-
 RopeParams rope_params(int head_dim, float theta) {
   RopeParams rp;
   const double two_pi = 8.0 * std::atan(1.0);
@@ -278,16 +284,14 @@ RopeParams rope_params(int head_dim, float theta) {
 }  // namespace
 
 int launch_prologue(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st) {
-  prologue_kernel<<<t.n_req, 32, 0, st>>>(t, d.vocab, b.meta, b.head_counter, status);
-  return last_error();
+  return launch_pdl(prologue_kernel, dim3(t.n_req), dim3(32), 0, st, t, d.vocab, b.meta, b.head_counter, status);
 }
 
 int launch_embed_norm(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status, cudaStream_t st) {
   if (m.dims.hidden > kRowVecs * kRowThreads * 8) return TV_E_UNSUPPORTED;
-  embed_norm_kernel<<<t.total_rows, kRowThreads, 0, st>>>(b.meta, reinterpret_cast<const __nv_bfloat16*>(m.embed),
-                                                          reinterpret_cast<const __nv_bfloat16*>(m.ln1),
-                                                          m.dims.hidden, m.dims.rms_eps, b.h, status);
-  return last_error();
+  return launch_pdl(embed_norm_kernel, dim3(t.total_rows), dim3(kRowThreads), 0, st, (const RowMeta*)b.meta,
+                    reinterpret_cast<const __nv_bfloat16*>(m.embed), reinterpret_cast<const __nv_bfloat16*>(m.ln1),
+                    m.dims.hidden, m.dims.rms_eps, b.h, (const int32_t*)status);
 }
 
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
@@ -302,19 +306,17 @@ int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b,
   }
   if (splits > kMaxSplits) return TV_E_UNSUPPORTED;
   dim3 grid(t.total_rows, d.n_q_heads + 2 * d.n_kv_heads);
-  qkv_finalize_kernel<<<grid, d.head_dim / 2, 0, st>>>(t, b.meta, b.part_qkv, splits, d.n_q_heads, d.n_kv_heads,
-                                                       d.head_dim, cached, b.q, status);
-  return last_error();
+  return launch_pdl(qkv_finalize_kernel, grid, dim3(d.head_dim / 2), 0, st, t, (const RowMeta*)b.meta,
+                    (const float*)b.part_qkv, splits, d.n_q_heads, d.n_kv_heads, d.head_dim, cached, b.q,
+                    (const int32_t*)status);
 }
 
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st) {
   if (m.dims.hidden > kRowVecs * kRowThreads * 8 || splits > kMaxSplits) return TV_E_UNSUPPORTED;
-  o_finalize_kernel<<<t.total_rows, kRowThreads, 0, st>>>(b.meta, b.part_o, splits, m.dims.hidden,
-                                                          reinterpret_cast<const __nv_bfloat16*>(m.embed),
-                                                          reinterpret_cast<const __nv_bfloat16*>(m.ln_f),
-                                                          m.dims.rms_eps, b.hf, status);
-  return last_error();
+  return launch_pdl(o_finalize_kernel, dim3(t.total_rows), dim3(kRowThreads), 0, st, (const RowMeta*)b.meta,
+                    (const float*)b.part_o, splits, m.dims.hidden, reinterpret_cast<const __nv_bfloat16*>(m.embed),
+                    reinterpret_cast<const __nv_bfloat16*>(m.ln_f), m.dims.rms_eps, b.hf, (const int32_t*)status);
 }
 
 }  // namespace tv

@@ -25,6 +25,8 @@ constexpr unsigned FULL = 0xffffffffu;
 __global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t* path, int32_t* accept_len,
                                      int32_t* out_tokens, int32_t* status) {
   const int r = blockIdx.x, lane = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (status_get(status) != 0) return;
   const int n = t.n[r], row0 = t.row_off[r];
   int par, tok;
@@ -61,6 +63,8 @@ __global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t*
 __global__ void __launch_bounds__(256) row_stats_kernel(const float* logits, int V, float inv_t, int nvc,
                                                         RowStat* stats, const int32_t* status) {
   __shared__ float red[8];
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int c = blockIdx.x, row = blockIdx.y;
   const float* lr = logits + (size_t)row * V;
@@ -199,6 +203,8 @@ __global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, f
                                        int32_t* status) {
   __shared__ int s_rej[32];
   const int r = blockIdx.x, lane = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (status_get(status) != 0) return;
   const int n = t.n[r], row0 = t.row_off[r];
   int par, tok;
@@ -281,6 +287,8 @@ __global__ void __launch_bounds__(128) commit_kernel(ReqTable t, int D, const in
   __shared__ uint4 rows[kMaxRows * 128 * 2 / 16];
   __shared__ int s_src[kMaxRows];
   __shared__ int s_a;
+  pdl_wait();
+  pdl_trigger();
   if (block_skip(status)) return;
   const int g = blockIdx.x, which = blockIdx.y, r = blockIdx.z;
   const int n = t.n[r], row0 = t.row_off[r], ctx = t.ctx[r];
@@ -315,14 +323,12 @@ __global__ void __launch_bounds__(128) commit_kernel(ReqTable t, int D, const in
   }
 }
 
-inline int last_error() { return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA; }
-
 }  // namespace
 
 int launch_accept_greedy(const ReqTable& t, const int32_t* argmax, int32_t* path, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* status, cudaStream_t st) {
-  accept_greedy_kernel<<<t.n_req, 32, 0, st>>>(t, argmax, path, accept_len, out_tokens, status);
-  return last_error();
+  return launch_pdl(accept_greedy_kernel, dim3(t.n_req), dim3(32), 0, st, t, argmax, path, accept_len, out_tokens,
+                    status);
 }
 
 int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, float temperature,
@@ -331,18 +337,17 @@ int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, fl
                            cudaStream_t st) {
   const int nvc = n_vchunks(vocab);
   const float inv_t = (float)(1.0 / (double)temperature);
-  row_stats_kernel<<<dim3(nvc, t.total_rows), 256, 0, st>>>(logits, vocab, inv_t, nvc, stats, status);
-  if (cudaGetLastError() != cudaSuccess) return TV_E_CUDA;
-  accept_residual_kernel<<<t.n_req, 32, 0, st>>>(t, logits, vocab, inv_t, uniforms, bonus_at_leaf, stats, nvc, path,
-                                                 accept_len, out_tokens, out_count, status);
-  return last_error();
+  const int rc = launch_pdl(row_stats_kernel, dim3(nvc, t.total_rows), dim3(256), 0, st, logits, vocab, inv_t, nvc,
+                            stats, (const int32_t*)status);
+  if (rc) return rc;
+  return launch_pdl(accept_residual_kernel, dim3(t.n_req), dim3(32), 0, st, t, logits, vocab, inv_t, uniforms,
+                    bonus_at_leaf, (const RowStat*)stats, nvc, path, accept_len, out_tokens, out_count, status);
 }
 
 int launch_commit(const ReqTable& t, const tv_dims& d, const int32_t* path, const int32_t* accept_len,
                   int32_t* committed_src, int32_t* new_ctx, int32_t* status, cudaStream_t st) {
-  commit_kernel<<<dim3(d.n_kv_heads, 2, t.n_req), 128, 0, st>>>(t, d.head_dim, path, accept_len, committed_src,
-                                                                new_ctx, status);
-  return last_error();
+  return launch_pdl(commit_kernel, dim3(d.n_kv_heads, 2, t.n_req), dim3(128), 0, st, t, d.head_dim, path, accept_len,
+                    committed_src, new_ctx, status);
 }
 
 }  // namespace tv
