@@ -12,10 +12,11 @@ constexpr int kMaxChunks = 32;               // cache chunks per request
 constexpr int kTreeSlot = kMaxChunks;        // partial slot of the tree keys
 constexpr int kChunkSlots = kMaxChunks + 1;
 
+// keys per chunk: a multiple of the attention kernel's 128-key tile
 __host__ __device__ inline int attn_chunk_len(int ctx) {
   const int per = (ctx + kMaxChunks - 1) / kMaxChunks;
-  const int ch = ((per + 63) / 64) * 64;
-  return ch < 64 ? 64 : ch;
+  const int ch = ((per + 127) / 128) * 128;
+  return ch < 128 ? 128 : ch;
 }
 __host__ __device__ inline int attn_n_chunks(int ctx) {
   return ctx <= 0 ? 0 : (ctx + attn_chunk_len(ctx) - 1) / attn_chunk_len(ctx);
