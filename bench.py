@@ -379,6 +379,36 @@ def run_ours(args, world, rank, local):
     sweep["ratio_32_over_8"] = round(sweep["32"]["verify_ms"] / sweep["8"]["verify_ms"], 4)
     out["sweep"] = sweep
 
+    # ---- long context: 32768 cached tokens, 32-row lattice tree ------------------
+    #      (attention graded here: its 134 MB of K/V stream from HBM; at 1k
+    #      context the 4 MB of K/V are L2-sized)
+    lc_ctx, lc_rows = 32768, 32
+    lt = synth.tree_lattice(lc_rows, 15, D.vocab, 41)
+    lr = _make_request(dv, synth, D, lt, lc_ctx, 300, dev)
+    lb = dv.RoundBuffers.alloc(D, lc_rows, 1, lc_ctx, device=dev)
+
+    def lvf():
+        dv.check(dv.verify(dm, [lr], lb, stream=torch.cuda.current_stream()), "verify")
+
+    gl = _graph(lvf)
+    lc_ms = _time_graph(gl, max(100, args.steps // 10))
+    del gl
+    dv.check(abi.tv_profile_start(P), "tv_profile_start")
+    for _ in range(P):
+        lvf()
+    rc, lsum, lcalls = abi.tv_profile_stop()
+    dv.check(rc, "tv_profile_stop")
+    kv_bytes = lc_ctx * D.n_kv_heads * D.head_dim * 2 * 2
+    att_s = lsum["attention"] / lcalls / 1e3
+    out["long_context"] = {
+        "ctx": lc_ctx, "rows": lc_rows, "verify_ms": round(lc_ms, 4),
+        "verify_GB_per_s": round(verify_bytes(D, lc_rows, lc_ctx) / lc_ms / 1e6, 1),
+        "attention_us": round(att_s * 1e6, 2), "attention_kv_bytes": kv_bytes,
+        "attention_GB_per_s": round(kv_bytes / att_s / 1e9, 1),
+        "attention_frac_of_peak": round(kv_bytes / att_s / 1e9 / peak, 4),
+        "stage_us": {k: round(1e3 * v / lcalls, 2) for k, v in lsum.items()}}
+    del lr, lb
+
     # ---- sampled round: residual walk at T = 1 instead of the greedy walk -------
     b.uniforms.copy_(torch.from_numpy(synth.uniforms(ROWS, 5)))
 
