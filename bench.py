@@ -55,6 +55,8 @@ def _args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="only the headline number (for profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rows", type=int, default=ROWS, help="tree rows of the timed round (profiling runs)")
+    ap.add_argument("--ctx", type=int, default=CTX, help="cached context of the timed round (profiling runs)")
     return ap.parse_args()
 
 
@@ -288,9 +290,10 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     D = synth.FULL
     dm = dv.DeviceModel.random(D, 1234 + rank, device=dev)
-    tree = synth.tree_lattice(ROWS, SLOTS, D.vocab, 7)
-    req = _make_request(dv, synth, D, tree, CTX, 99 + rank, dev)
-    b = dv.RoundBuffers.alloc(D, ROWS, 1, CTX, device=dev)
+    rows, ctx = args.rows, args.ctx
+    tree = synth.tree_lattice(rows, SLOTS if rows <= 16 else 15, D.vocab, 7)
+    req = _make_request(dv, synth, D, tree, ctx, 99 + rank, dev)
+    b = dv.RoundBuffers.alloc(D, rows, 1, ctx, device=dev)
     _plant(dv, dm, req, b, _spine(tree.parent))
     def round_():
         dv.run_round(dm, [req], b, stream=torch.cuda.current_stream())
@@ -329,8 +332,10 @@ def run_ours(args, world, rank, local):
     out = {"metric": METRIC, "value": round(graph_ms, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(graph_ms, 4), "higher_is_better": False,
            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-           "config": {"workload": WORKLOAD, "hidden": D.hidden, "heads": f"{D.n_q_heads}/{D.n_kv_heads}x{D.head_dim}",
-                      "vocab": D.vocab, "rows": ROWS, "ctx": CTX, "accept_len": accept_len,
+           "config": {"workload": WORKLOAD if (rows, ctx) == (ROWS, CTX) else
+                      WORKLOAD.replace("16-row", f"{rows}-row").replace("1024-token", f"{ctx}-token"),
+                      "hidden": D.hidden, "heads": f"{D.n_q_heads}/{D.n_kv_heads}x{D.head_dim}",
+                      "vocab": D.vocab, "rows": rows, "ctx": ctx, "accept_len": accept_len,
                       "l2": "inputs larger than L2: 1.68 GB of weights stream from HBM every step",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "eager_ms_per_step": round(eager_ms, 4), "clocks": clocks,
@@ -348,7 +353,7 @@ def run_ours(args, world, rank, local):
     stage_us = {k: round(1e3 * v / calls, 2) for k, v in stage_sum.items()}
     peak, peak_kind = _peaks()
     head_s = stage_sum["lm_head"] / calls / 1e3
-    hb = head_bytes(D, ROWS)
+    hb = head_bytes(D, rows)
     achieved = hb / head_s / 1e9
     kernel_sha = _file_sha256(os.path.join(ROOT, "speculative_tree_verify_gb300", "csrc", "tv_gemm.cu"))
     tr = _ncu_traffic(kernel_sha)
@@ -410,7 +415,7 @@ def run_ours(args, world, rank, local):
     del lr, lb
 
     # ---- sampled round: residual walk at T = 1 instead of the greedy walk -------
-    b.uniforms.copy_(torch.from_numpy(synth.uniforms(ROWS, 5)))
+    b.uniforms.copy_(torch.from_numpy(synth.uniforms(rows, 5)))
 
     def sround():
         dv.run_round(dm, [req], b, sampled=1.0, stream=torch.cuda.current_stream())
@@ -422,7 +427,7 @@ def run_ours(args, world, rank, local):
     # ---- end to end through the C ABI with host buffers --------------------------
     par_h = torch.from_numpy(req.parent.cpu().numpy()).pin_memory()
     tok_h = torch.from_numpy(req.token.cpu().numpy()).pin_memory()
-    res_h = torch.empty(ROWS + 2, dtype=torch.int32).pin_memory()
+    res_h = torch.empty(rows + 2, dtype=torch.int32).pin_memory()
     steps_e2e = max(50, args.steps // 4)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -430,13 +435,13 @@ def run_ours(args, world, rank, local):
         req.parent.copy_(par_h, non_blocking=True)
         req.token.copy_(tok_h, non_blocking=True)
         round_()
-        res_h[:ROWS].copy_(b.out_tokens, non_blocking=True)
-        res_h[ROWS:ROWS + 1].copy_(b.accept_len, non_blocking=True)
-        res_h[ROWS + 1:].copy_(b.new_ctx, non_blocking=True)
+        res_h[:rows].copy_(b.out_tokens, non_blocking=True)
+        res_h[rows:rows + 1].copy_(b.accept_len, non_blocking=True)
+        res_h[rows + 1:].copy_(b.new_ctx, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / steps_e2e
-    out["e2e"] = {"value": round(e2e_ms, 4), "unit": UNIT, "h2d_bytes_per_step": 2 * ROWS * 4,
-                  "d2h_bytes_per_step": (ROWS + 2) * 4, "steps": steps_e2e,
+    out["e2e"] = {"value": round(e2e_ms, 4), "unit": UNIT, "h2d_bytes_per_step": 2 * rows * 4,
+                  "d2h_bytes_per_step": (rows + 2) * 4, "steps": steps_e2e,
                   "note": "host tree -> device, eager round, tokens/accept_len/new_ctx -> host, sync, every step"}
 
     # ---- the CPU oracle on the host cores ----------------------------------------

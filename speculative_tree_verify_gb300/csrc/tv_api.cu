@@ -183,7 +183,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   const GemmPlan pq = plan_gemm(QKV, H, false);
   const GemmPlan po = plan_gemm(H, QD, false);
   const GemmPlan ph = plan_gemm(d.vocab, H, true);
-  GemmParams gp;   // (zeroed below: no prefetch unless set)
+  GemmParams gp;
   memset(&gp, 0, sizeof(gp));
   gp.status = dev_status;
 
@@ -193,23 +193,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   if ((rc = launch_embed_norm(t, *model, b, dev_status, st))) return rc;
   pm.mark(1);
   gp.out = b.part_qkv;
-  // While the QKV finalize, the attention and the O finalize run (latency-bound,
-  // HBM mostly idle), stream the O weights and the first quarter of every head
-  // CTA's first tile into L2.  Each byte still comes from HBM once; the later
-  // kernels read these lines with evict-first.
-  {
-    const int head_grid = ph.n_units < sms ? ph.n_units : sms;
-    gp.pf_ptr[0] = reinterpret_cast<const uint8_t*>(model->wo);
-    gp.pf_rows[0] = H;
-    gp.pf_row_bytes[0] = QD * 2;
-    gp.pf_stride[0] = (long long)QD * 2;
-    gp.pf_ptr[1] = reinterpret_cast<const uint8_t*>(model->lm_head);
-    gp.pf_rows[1] = head_grid * 128 < d.vocab ? head_grid * 128 : d.vocab;
-    gp.pf_row_bytes[1] = ((H / 64) / 4) * 128;
-    gp.pf_stride[1] = (long long)H * 2;
-  }
   if ((rc = launch_gemm(GEMM_PARTIAL, model->wqkv, QKV, H, b.h, t.total_rows, pq, gp, sms, st))) return rc;
-  memset(gp.pf_ptr, 0, sizeof(gp.pf_ptr));
   pm.mark(2);
   if ((rc = launch_qkv_finalize(t, d, b, pq.splits, dev_status, st))) return rc;
   pm.mark(3);

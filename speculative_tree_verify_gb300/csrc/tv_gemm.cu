@@ -184,22 +184,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       if (!ok) status_set(p.status, TV_E_TIMEOUT);
-      // L2 prefetch for a later kernel: this CTA's share of each region's rows
-      for (int j = 0; j < 2 && ok; ++j) {
-        if (!p.pf_ptr[j] || p.pf_rows[j] <= 0) continue;
-        const int per = (p.pf_rows[j] + (int)gridDim.x - 1) / (int)gridDim.x;
-        const int r0 = (int)blockIdx.x * per, r1 = min(p.pf_rows[j], r0 + per);
-        if (p.pf_stride[j] == (long long)p.pf_row_bytes[j]) {   // contiguous rows: one range
-          const uint8_t* a = p.pf_ptr[j] + (size_t)r0 * p.pf_stride[j];
-          const uint8_t* e = p.pf_ptr[j] + (size_t)r1 * p.pf_stride[j];
-          for (; a < e; a += 65536) {
-            const long long left = (long long)(e - a);
-            prefetch_l2_bulk(a, (uint32_t)(left < 65536 ? left : 65536));
-          }
-        } else {
-          for (int rr = r0; rr < r1; ++rr) prefetch_l2_bulk(p.pf_ptr[j] + (size_t)rr * p.pf_stride[j], p.pf_row_bytes[j]);
-        }
-      }
       // every load this thread issued has landed before the CTA may exit
       for (int s = 0; s < STAGES; ++s)
         if (armed & (1u << s)) mbar_wait(&full[s], (last_par >> s) & 1u);

@@ -23,13 +23,6 @@ struct GemmParams {
   int32_t* argmax;           // HEAD: [n_rows]
   float* gap;                // HEAD: [n_rows]
   int32_t* status;           // sticky status word
-  // Optional L2 prefetch of weights a later kernel reads, issued once this
-  // kernel's own loads are out: region j is pf_rows[j] rows of pf_row_bytes[j]
-  // bytes, pf_stride[j] bytes apart, split evenly over the CTAs.
-  const uint8_t* pf_ptr[2];
-  int pf_rows[2];
-  int pf_row_bytes[2];
-  long long pf_stride[2];
 };
 
 struct GemmPlan {
