@@ -78,9 +78,14 @@ def _code_sha256() -> str:
     return h.hexdigest()
 
 
-def _file_sha256(path) -> str:
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()
+def _head_kernel_sha256() -> str:
+    """sha256 over the sources the LM-head kernel is compiled from, in this
+    order: tv_common.cuh, tv_gemm.cuh, tv_gemm.cu."""
+    h = hashlib.sha256()
+    for f in ("tv_common.cuh", "tv_gemm.cuh", "tv_gemm.cu"):
+        with open(os.path.join(ROOT, "speculative_tree_verify_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def _peaks():
@@ -355,8 +360,7 @@ def run_ours(args, world, rank, local):
     head_s = stage_sum["lm_head"] / calls / 1e3
     hb = head_bytes(D, rows)
     achieved = hb / head_s / 1e9
-    kernel_sha = _file_sha256(os.path.join(ROOT, "speculative_tree_verify_gb300", "csrc", "tv_gemm.cu"))
-    tr = _ncu_traffic(kernel_sha)
+    tr = _ncu_traffic(_head_kernel_sha256())
     out["roofline"] = {"kernel": "lm_head (tcgen05 skinny GEMM + fused argmax/top-2)", "bound": "hbm",
                        "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                        "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
