@@ -197,7 +197,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   pm.mark(2);
   if ((rc = launch_qkv_finalize(t, d, b, pq.splits, dev_status, st))) return rc;
   pm.mark(3);
-  if ((rc = launch_attention(t, d, b, dev_status, st))) return rc;
+  if ((rc = launch_attention(t, d, b, sms, dev_status, st))) return rc;
   pm.mark(4);
   gp.out = b.part_o;
   if ((rc = launch_gemm(GEMM_PARTIAL, model->wo, H, QD, b.attn, t.total_rows, po, gp, sms, st))) return rc;

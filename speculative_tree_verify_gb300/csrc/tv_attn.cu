@@ -2,34 +2,45 @@
 // 5th-generation tensor cores.
 //
 // Row i, query head h attends to the cached slots [0, ctx) and to the tree
-// slots ctx + a for every a in anc(i) (its ancestors and itself): "give each
-// node an attention mask of its ancestors and a position equal to its depth"
+// slots ctx + a for every a in anc(i) (its ancestors and itself): each node is
+// masked to its ancestors and placed at a position equal to its depth
 // [Drafters and tree verify, §Tree verify through recurrent layers].  The
 // positions were applied by RoPE before the keys were written.
 //
-// Split-context (flash-decoding) layout: one CTA per (request, KV head, query
-// tile, context chunk) plus one per (request, KV head, query tile) for the
-// tree keys.  A query tile is 128 query vectors = the request's rows x the GQA
-// heads of one KV head, so every K/V byte is read once per query tile.  The
-// chunk length is a function of ctx only (a multiple of 128 keys, at most 32
-// chunks), and the merge kernel combines the partials (max, sum, unnormalised
-// output) in chunk order, then the tree slot: a row's result is the same
-// whatever the other rows are.
+// Split-context (flash-decoding) layout: one CTA per (request, KV head, context
+// chunk).  It holds every query vector of its KV head at once: the request's
+// rows x the GQA heads of the KV head, at most 160, so each K/V byte is read
+// once.  The chunks are whole 128-key tiles, their count aimed at SMs / KV
+// heads (one wave for one request); the tree tile has a chunk of its own in
+// short contexts and otherwise goes first in the last chunk.
+// The merge kernel combines the chunks' partials (offset, sum, unnormalised
+// output) in chunk order, so a row's result does not depend on the other rows.
 //
-// Per CTA, for each 128-key tile of its chunk:
-//   S = Q K^T      tcgen05.mma M128 (queries) N128 (keys) K16, fp32 in TMEM;
-//                  Q staged once into 128B-swizzled smem, K by TMA (K-major)
-//   softmax        16 warps: four per TMEM lane quarter, each thread one query
-//                  row x 32 keys; scores scaled by log2(e)/sqrt(D), masked
-//                  (keys past the chunk; ancestors for the tree tile), row max
-//                  exchanged in smem, online max / sum in fp32, P = 2^(x - m)
-//                  (SFU ex2) rounded to bf16 into swizzled smem, O in TMEM rescaled when
-//                  the max grows; quarters without a valid query row skip
-//   O += P V       tcgen05.mma M128 N=D K16, V straight from its TMA layout as
-//                  an MN-major operand
-// K and V tiles each have a two-stage TMA ring, refilled two tiles ahead.
+// Transposed products: the keys of a tile sit on the 128 TMEM lanes and the
+// query vectors are the MMA's N dimension, so a KV head's queries need no
+// padding to 128.  Per 128-key tile t:
+//   S^T = K_t Q^T      tcgen05.mma M128 (keys) N (queries) K16, fp32 in TMEM;
+//                      K by TMA (K-major A), Q staged once (K-major B)
+//   softmax            16 warps: four per TMEM lane quarter, each thread one key
+//                      x a quarter of the query columns.  Each query column
+//                      has an offset m (log2 units) that moves only when a
+//                      score passes m + 8: the warps of a column slice find
+//                      out with one barrier reduction, and only then compute
+//                      the tile's column maxima.  P = 2^(s log2(e)/sqrt(D) - m)
+//                      (SFU ex2), masked, rounded to bf16, parked in TMEM
+//                      until the previous O^T MMA has read P^T, then stored
+//                      into swizzled smem
+//   O^T += V_t^T P^T   tcgen05.mma M128 (dimensions) N (queries) K16, V straight
+//                      from its TMA layout and P^T as MN-major operands
+// O, the column sums and the offsets all carry the same offset, which cancels
+// in O / sum, so the lazy offset is exact.
+// A 17th warp issues the TMA loads (two K and two V stages) and the MMAs from
+// an event loop.  S^T is double-buffered in TMEM so that S^T of tile t+1
+// overlaps the softmax of t, and O^T of tile t overlaps the next tile's
+// softmax up to its P^T store.
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 
 #include "tv_common.cuh"
 #include "tv_gemm.cuh"
@@ -39,14 +50,18 @@ namespace tv {
 
 namespace {
 
-constexpr int kSlices = 4;                          // softmax warps per TMEM lane quarter
-constexpr int kKeysPer = 128 / kSlices;             // keys of a 128-key tile per softmax thread
-constexpr int kAtSoftWarps = 4 * kSlices;           // 16
-constexpr int kAtSoftThreads = kAtSoftWarps * 32;   // 512
-constexpr int kAtThreads = kAtSoftThreads + 32;     // + one warp: TMEM owner, TMA and MMA issue
-constexpr int kAtTmemCols = 512;  // S double buffer: columns [0, 128) and [128, 256); O: [256, 256 + D)
-constexpr int kAtom = 128 * 128;  // bytes of one 128-row x 128-byte swizzled slab
-constexpr float kRescaleLog2 = 8.f;   // O and l are rescaled only when the row max grows by more than 2^8
+constexpr int kSlices = 4;                         // softmax warps per TMEM lane quarter = query-column slices
+constexpr int kAtSoftWarps = 4 * kSlices;          // 16
+constexpr int kAtSoftThreads = kAtSoftWarps * 32;  // 512
+constexpr int kWarpIssue = kAtSoftWarps;           // TMEM owner, TMA and MMA issue
+constexpr int kAtThreads = kAtSoftThreads + 32;
+constexpr int kNqMax = kMaxQueriesPerKvHead;       // query columns of one KV head
+constexpr int kCps = kNqMax / 8 / kSlices;         // 8-column chunks per slice
+constexpr int kColS0 = 0, kColS1 = kNqMax, kColO = 2 * kNqMax;   // TMEM columns: S^T double buffer, O^T
+constexpr int kAtTmemCols = 512;
+constexpr int kAtom = 128 * 128;                   // bytes of one 128-row x 128-byte swizzled slab
+constexpr float kRescaleLog2 = 8.f;                // an offset moves when a score passes it by 2^8
+static_assert(kNqMax % (8 * kSlices) == 0 && 3 * kNqMax <= kAtTmemCols && kCps == 5, "query columns must fit TMEM");
 
 struct AttnMaps {
   CUtensorMap k[kMaxReq];   // per request: [Hkv * capacity][D] bf16, box 64 x 128, 128B swizzle
@@ -55,15 +70,17 @@ struct AttnMaps {
 
 template <int D>
 struct AtSmem {
-  static constexpr int SLABS = D / 64;               // 64-element slabs along D
-  static constexpr int Q_BYTES = SLABS * kAtom;      // 128 queries x D
-  static constexpr int KV_BYTES = SLABS * kAtom;     // 128 keys x D
-  static constexpr int P_BYTES = 2 * kAtom;          // 128 queries x 128 keys
+  static constexpr int QSLAB = kNqMax * 128;       // one 64-dimension slab of the queries
+  static constexpr int Q_BYTES = (D / 64) * QSLAB;
+  static constexpr int KV_BYTES = 2 * kAtom;       // 128 keys x 128 dimensions (D = 64: the V upper slab stays 0)
+  static constexpr int P_BYTES = 3 * kAtom;        // P^T: 128 keys x 3 slabs of 64 query columns
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;     // K stage s at OFF_KV + s KV_BYTES, V stage s at OFF_KV + (2 + s) KV_BYTES
-  static constexpr int OFF_P = OFF_KV + 4 * KV_BYTES;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;    // K stage s at OFF_K + s KV_BYTES
+  static constexpr int OFF_V = OFF_K + 2 * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + 2 * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
+  static_assert(OFF_K % 1024 == 0, "swizzled slabs start on 1024-byte boundaries");
 };
 
 // 128B-swizzle smem descriptor with explicit leading / stride byte offsets.
@@ -77,7 +94,7 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// byte offset of 16-byte chunk c of row r inside a 128-row x 128-byte slab
+// byte offset of 16-byte chunk c of row r inside a slab of 128-byte rows
 // stored with the 128-byte swizzle (chunk index XOR row mod 8)
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -91,137 +108,145 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// the four warps of one TMEM lane quarter (named barriers 1..4)
-__device__ __forceinline__ void quarter_barrier(int qd) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + qd), "n"(kSlices * 32) : "memory");
+// the four warps of one query-column slice (named barriers 1..4)
+__device__ __forceinline__ void slice_sync(int cs) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + cs), "n"(4 * 32) : "memory");
 }
-__device__ __forceinline__ void soft_barrier() { asm volatile("bar.sync 5, %0;" ::"n"(kAtSoftThreads) : "memory"); }
+// true on every thread of the slice if v is true on any of them
+__device__ __forceinline__ bool slice_any(bool v, int cs) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(1 + cs), "n"(4 * 32)
+      : "memory");
+  return out != 0;
+}
+
+// maximum over the warp's 32 lanes, on every lane (PTX redux.sync.max.f32;
+// NaN inputs are ignored)
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 5, %0;" ::"n"(kAtSoftThreads) : "memory"); }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Columns [OFF, OFF + 32) (or + 16) of a register array from / to 32 (16)
-// consecutive TMEM columns of this thread's lane.  Constant indices keep the
-// arrays in registers.
-template <int OFF, int N>
-__device__ __forceinline__ void ld32_at(uint32_t taddr, uint32_t (&r)[N]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-               : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]), "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]), "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15]), "=r"(r[OFF + 16]), "=r"(r[OFF + 17]), "=r"(r[OFF + 18]), "=r"(r[OFF + 19]), "=r"(r[OFF + 20]), "=r"(r[OFF + 21]), "=r"(r[OFF + 22]), "=r"(r[OFF + 23]), "=r"(r[OFF + 24]), "=r"(r[OFF + 25]), "=r"(r[OFF + 26]), "=r"(r[OFF + 27]), "=r"(r[OFF + 28]), "=r"(r[OFF + 29]), "=r"(r[OFF + 30]), "=r"(r[OFF + 31])
+// 8 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
 }
-template <int OFF, int N>
-__device__ __forceinline__ void ld16_at(uint32_t taddr, uint32_t (&r)[N]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-               : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]), "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]), "=r"(r[OFF + 10]), "=r"(r[OFF + 11]), "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]), "=r"(r[OFF + 15])
+__device__ __forceinline__ void ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
 }
-template <int OFF, int N>
-__device__ __forceinline__ void st32_at(uint32_t taddr, const uint32_t (&r)[N]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr), "r"(r[OFF + 0]), "r"(r[OFF + 1]), "r"(r[OFF + 2]), "r"(r[OFF + 3]), "r"(r[OFF + 4]), "r"(r[OFF + 5]), "r"(r[OFF + 6]), "r"(r[OFF + 7]), "r"(r[OFF + 8]), "r"(r[OFF + 9]), "r"(r[OFF + 10]), "r"(r[OFF + 11]), "r"(r[OFF + 12]), "r"(r[OFF + 13]), "r"(r[OFF + 14]), "r"(r[OFF + 15]), "r"(r[OFF + 16]), "r"(r[OFF + 17]), "r"(r[OFF + 18]), "r"(r[OFF + 19]), "r"(r[OFF + 20]), "r"(r[OFF + 21]), "r"(r[OFF + 22]), "r"(r[OFF + 23]), "r"(r[OFF + 24]), "r"(r[OFF + 25]), "r"(r[OFF + 26]), "r"(r[OFF + 27]), "r"(r[OFF + 28]), "r"(r[OFF + 29]), "r"(r[OFF + 30]), "r"(r[OFF + 31])
+__device__ __forceinline__ void st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
                : "memory");
 }
-template <int OFF, int N>
-__device__ __forceinline__ void st16_at(uint32_t taddr, const uint32_t (&r)[N]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr), "r"(r[OFF + 0]), "r"(r[OFF + 1]), "r"(r[OFF + 2]), "r"(r[OFF + 3]), "r"(r[OFF + 4]), "r"(r[OFF + 5]), "r"(r[OFF + 6]), "r"(r[OFF + 7]), "r"(r[OFF + 8]), "r"(r[OFF + 9]), "r"(r[OFF + 10]), "r"(r[OFF + 11]), "r"(r[OFF + 12]), "r"(r[OFF + 13]), "r"(r[OFF + 14]), "r"(r[OFF + 15])
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
 
-// NC consecutive 32-bit TMEM columns of this thread's lane (NC = 16, 32 or 64)
-template <int NC>
-__device__ __forceinline__ void cols_ld(uint32_t taddr, uint32_t (&r)[NC]) {
-  if constexpr (NC == 16) {
-    ld16_at<0>(taddr, r);
-  } else {
-    ld32_at<0>(taddr, r);
-    if constexpr (NC == 64) ld32_at<32>(taddr + 32, r);
-  }
-}
-template <int NC>
-__device__ __forceinline__ void cols_st(uint32_t taddr, const uint32_t (&r)[NC]) {
-  if constexpr (NC == 16) {
-    st16_at<0>(taddr, r);
-  } else {
-    st32_at<0>(taddr, r);
-    if constexpr (NC == 64) st32_at<32>(taddr + 32, r);
-  }
-}
-
-// grid (query tiles, chunks + 1, requests x KV heads); the query tiles of one
-// chunk are neighbours in launch order, so their K/V tiles meet in L2.
+// grid (chunks, KV heads, requests); 16 softmax warps and one issue warp.
 //
-// Pipeline over the chunk's 128-key tiles t (issuer = one thread of warp 16):
-//   S[t % 2] = Q K_t^T            as soon as K_t has landed and S[t % 2] is free
-//   softmax(t) by warps 0-15      P_t built in registers; stored to smem P once
-//                                 O += P_{t-1} V_{t-1} is done; O rescaled if needed
-//   O += P_t V_t                  after softmax(t); frees K/V stage t % 2
-// so S(t+1) overlaps softmax(t), and the TMA of tile t+2 overlaps both.
+// Tiles of a chunk: (last chunk) the tree tile, then its cached-key tiles.
+// The issue warp's lane 0 runs an event loop: an MMA or TMA instruction holds
+// its thread for about as long as the unit takes to accept it, so one thread
+// serves every ready event in priority order instead of waiting on one:
+//   O^T += V_t^T P_t^T   once P^T(t) is stored and V_t has landed
+//   S^T(t) = K_t Q^T     once K_t has landed and S^T[t % 2] was read (tile t-2)
+//   TMA K_t              once S^T(t-2) is done (its K stage is free)
+//   TMA V_t              once O^T(t-2) is done (its V stage is free)
+// Softmax warps, per tile t: pass 1 (offset check), O^T rescale if an offset
+// moved, pass 2 (P^T), each reading this thread's 40 scores from TMEM.
 template <int D>
 __global__ void __launch_bounds__(kAtThreads, 1)
     attn_tc_kernel(const __grid_constant__ AttnMaps maps, ReqTable t, const RowMeta* meta, const __nv_bfloat16* q,
-                   int Hq, int Hkv, float scale_log2, float* part_ml, float* part_o, int32_t* status) {
+                   int Hq, int Hkv, int chunk_target, float scale_log2, float* part_ml, float* part_o,
+                   int32_t* status) {
   using L = AtSmem<D>;
-  constexpr int OC = D / kSlices;   // O columns per softmax thread
-  static_assert(OC % 16 == 0 && kKeysPer % 32 == 0, "TMEM accesses come in 16- and 32-column pieces");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* k_full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);    // [2] K tile landed
-  uint64_t* k_free = k_full + 2;                                          // [2] S MMA of the K stage done
-  uint64_t* v_full = k_free + 2;                                          // [2] V tile landed
-  uint64_t* v_free = v_full + 2;                                          // [2] O MMA of the V stage done
-  uint64_t* s_full = v_free + 2;                                          // [2] S MMA done
-  uint64_t* p_full = s_full + 2;                                          // [2] softmax done (16 warps)
-  uint64_t* o_ready = p_full + 2;                                         // O MMA of a tile done
-  uint64_t* q_full = o_ready + 1;                                         // queries staged (16 warps)
-  uint64_t* drain = q_full + 1;                                           // every MMA of the CTA done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* v_full = k_full + 2;                                          // [2] V tile landed
+  uint64_t* v_free = v_full + 2;                                          // [2] O^T MMA of the V stage done
+  uint64_t* s_full = v_free + 2;                                          // [2] S^T MMA done
+  uint64_t* s_free = s_full + 2;                                          // [2] S^T buffer read (16 warps)
+  uint64_t* p_full = s_free + 2;                                          // P^T stored (16 warps)
+  uint64_t* o_done = p_full + 1;                                          // O^T MMA of a tile done
+  uint64_t* q_full = o_done + 1;                                          // queries staged (16 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   int* s_stat = reinterpret_cast<int*>(tmem_slot + 1);
   __shared__ uint32_t s_anc[32];
-  __shared__ float s_red[2][kSlices][128];   // partial row maxima, double-buffered by tile parity
-  __shared__ float s_l[kSlices][128];        // partial row sums
+  __shared__ int s_qrow[kNqMax];                     // query column c: its row of q and of the partials, (row0 + c / G) Hq + g G + c % G
+  __shared__ uint32_t s_canc[kNqMax];                // query column c: the ancestor set of its tree row c / G
+  __shared__ float s_red[4][kNqMax];                 // per lane quarter: column maxima; column sums
+  // column offsets, double-buffered: a move writes the other buffer, so the
+  // old offsets stay readable until every thread of the slice has used them
+  __shared__ __align__(16) float s_m[2][kNqMax];     // offset m (log2 units), -inf before any visible key
+  __shared__ __align__(16) float s_negm[2][kNqMax];  // -m
+  __shared__ __align__(16) float s_alpha[kNqMax];    // 2^(m_old - m_new) of the last move
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, slot_x = blockIdx.y, g = blockIdx.z % Hkv, r = blockIdx.z / Hkv;
+  const int chunk = blockIdx.x, g = blockIdx.y, r = blockIdx.z;
+  const bool issuer = warp == kWarpIssue && lane == 0;
 
-  // ---- structural early exits (kernel parameters only) ------------------------
+  // ---- structural early exit (kernel parameters only) -------------------------
   const int ctx = t.ctx[r], n = t.n[r], row0 = t.row_off[r], cap = t.capacity[r];
-  const int nch = attn_n_chunks(ctx);
-  const bool tree = slot_x == (int)gridDim.y - 1;
-  const int G = Hq / Hkv;
-  const int nq = n * G, q0 = qt * 128;
-  if ((!tree && slot_x >= nch) || q0 >= nq) {
+  const AttnPlan plan = attn_plan(ctx, chunk_target);
+  if (chunk >= plan.n_chunks) {
     pdl_wait();
     pdl_trigger();
     return;
   }
-  const int slot = tree ? kTreeSlot : slot_x;
-  int key0, nkeys;
-  if (tree) {
-    key0 = ctx;
-    nkeys = n;
-  } else {
-    const int ch = attn_chunk_len(ctx);
-    key0 = slot * ch;
-    nkeys = min(ch, ctx - key0);
-  }
-  const int T = (nkeys + 127) / 128;
+  const int G = Hq / Hkv, nq = n * G;
+  const int NQ = (nq + 15) & ~15;                    // MMA N: a multiple of 16
+  const bool last = chunk == plan.n_chunks - 1;
+  const int key0 = chunk * plan.tiles_per_chunk * 128;
+  const int ncache = plan.tree_own && last ? 0 : max(0, min(ctx - key0, plan.tiles_per_chunk * 128));
+  const int Tc = (ncache + 127) / 128;
+  const bool has_tree = last;
+  const int T = Tc + (has_tree ? 1 : 0);
+  // tile j: the tree tile first (last chunk), then the cached-key tiles.  The
+  // tree keys usually carry a tree row's largest scores; taking them first
+  // gives those keys the exact offset (P = 1 rounds exactly to bf16)
+  const int tc0 = has_tree ? 1 : 0;
+  auto is_tree = [&](int j) { return has_tree && j == 0; };
+  auto tile_row = [&](int j) { return g * cap + (is_tree(j) ? ctx : key0 + (j - tc0) * 128); };   // first K/V row
+  auto tile_keys = [&](int j) { return is_tree(j) ? n : min(128, ncache - (j - tc0) * 128); };     // valid keys
+  // whole tile of cached keys below ctx: readable before the wait
+  auto pre_ok = [&](int j) { return !is_tree(j) && key0 + (j - tc0 + 1) * 128 <= ctx; };
 
   // ---- set-up --------------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&k_full[b], 1);
-      mbar_init(&k_free[b], 1);
       mbar_init(&v_full[b], 1);
       mbar_init(&v_free[b], 1);
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], kAtSoftWarps);
+      mbar_init(&s_free[b], kAtSoftWarps);
     }
-    mbar_init(o_ready, 1);
+    mbar_init(p_full, kAtSoftWarps);
+    mbar_init(o_done, 1);
     mbar_init(q_full, kAtSoftWarps);
-    mbar_init(drain, 1);
     fence_mbar_init();
     prefetch_tmap(&maps.k[r]);
     prefetch_tmap(&maps.v[r]);
   }
-  if (warp == kAtSoftWarps) {
+  if (warp == kWarpIssue) {
     tmem_alloc(tmem_slot, kAtTmemCols);
     tmem_relinquish();
   }
@@ -229,276 +254,437 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 256;
+
+  // ---- TMA issue ------------------------------------------------------------------
+  int kiss = 0, viss = 0;   // K / V tiles issued (in tile order)
+  uint32_t pre = 0;         // bit j: K_j and V_j issued before the wait
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](bool is_v, int j) {
+    const int st = j & 1;
+    uint8_t* dst = smem + (is_v ? L::OFF_V : L::OFF_K) + st * L::KV_BYTES;
+    uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
+    mbar_arrive_expect_tx(bar, (D / 64) * kAtom);
+#pragma unroll
+    for (int a = 0; a < D / 64; ++a)
+      tma_load_2d(dst + a * kAtom, is_v ? &maps.v[r] : &maps.k[r], bar, a * 64, tile_row(j), pol);
+  };
+  if (issuer) {
+    // Cached keys below ctx are final before this grid starts: it starts once
+    // the previous kernel has passed its own wait, and every kernel waits for
+    // its predecessor before it completes, so every earlier writer of the
+    // cache is done.  The tree slots (written by the previous kernel) and the
+    // queries are read after the wait.
+    for (int j = 0; j < 2 && j < T; ++j)
+      if (pre_ok(j)) {
+        issue(false, j);
+        issue(true, j);
+        pre |= 1u << j;
+      }
+  }
 
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) *s_stat = status_get(status);
   if (threadIdx.x < 32) s_anc[threadIdx.x] = (int)threadIdx.x < n ? meta[row0 + threadIdx.x].anc : 0u;
   __syncthreads();
+  const bool run = *s_stat == 0;
 
-  if (*s_stat == 0) {
-    uint8_t* sQ = smem + L::OFF_Q;
-    if (warp == kAtSoftWarps) {
-      // ---------------- issuer: TMA loads and MMAs (one thread) ----------------
-      if (lane == 0) {
-        const uint64_t pol = policy_evict_first();
-        int k_iss[2] = {0, 0}, k_use[2] = {0, 0}, v_iss[2] = {0, 0}, v_use[2] = {0, 0};
-        const int y0 = g * cap + key0;
-        auto issue = [&](bool is_v, int tile) {   // one 128-key tile of K or V into its ring
-          const int st = tile & 1;
-          uint8_t* dst = smem + L::OFF_KV + ((is_v ? 2 : 0) + st) * L::KV_BYTES;
-          uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
-          mbar_arrive_expect_tx(bar, L::KV_BYTES);
-#pragma unroll
-          for (int a = 0; a < L::SLABS; ++a)
-            tma_load_2d(dst + a * kAtom, is_v ? &maps.v[r] : &maps.k[r], bar, a * 64, y0 + tile * 128, pol);
-          if (is_v) ++v_iss[st]; else ++k_iss[st];
-        };
-        const uint32_t qaddr = smem_u32(sQ);
-        const uint32_t idesc_s = idesc_bf16_f32(128, 128);
-        const uint32_t idesc_o = idesc_bf16_f32(128, D) | (1u << 16);   // B (V) is MN-major
-        auto mma_s = [&](int tile) -> bool {   // S[tile % 2] = Q K_tile^T
-          const int st = tile & 1;
-          if (!mbar_wait(&k_full[st], (uint32_t)(tile >> 1) & 1u)) return false;
-          ++k_use[st];
+  if (warp == kWarpIssue) {
+    // ---------------- event-loop issuer (one thread) ----------------
+    if (issuer && run) {
+      const uint32_t qaddr = smem_u32(smem + L::OFF_Q);
+      const uint32_t paddr = smem_u32(smem + L::OFF_P);
+      const uint32_t idesc_s = idesc_bf16_f32(128, NQ);
+      const uint32_t idesc_o = idesc_bf16_f32(128, NQ) | (1u << 15) | (1u << 16);   // A = V^T, B = P^T: MN-major
+      for (int j = 0; j < 2 && j < T; ++j)
+        if (!((pre >> j) & 1u)) {
+          issue(false, j);
+          issue(true, j);
+        }
+      kiss = viss = T < 2 ? T : 2;
+      int ns = 0, no = 0;   // S^T / O^T MMAs issued
+      bool qready = false, ok = true;
+      unsigned long long t_last = globaltimer();
+      uint32_t polls = 0;
+      while (no < T) {
+        bool progress = false;
+        if (!qready) qready = mbar_test(q_full, 0);
+        // O^T += V^T P^T of tile no
+        if (qready && no < ns && mbar_test(p_full, (uint32_t)no & 1u) &&
+            mbar_test(&v_full[no & 1], (uint32_t)(no >> 1) & 1u)) {
           tc_fence_after();
-          const uint32_t kaddr = smem_u32(smem + L::OFF_KV + st * L::KV_BYTES);
-          const uint32_t tS = tmem + (uint32_t)(st * 128);
+          const uint32_t vaddr = smem_u32(smem + L::OFF_V + (no & 1) * L::KV_BYTES);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)   // 16 keys per step
+            umma_bf16(tmem + kColO, sdesc_sw128(vaddr + k * 2048, kAtom, 1024),
+                      sdesc_sw128(paddr + k * 2048, kAtom, 1024), idesc_o, (no > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&v_free[no & 1]);
+          umma_commit(o_done);
+          ++no;
+          progress = true;
+        }
+        // S^T of tile ns, after O^T of tile ns-2: that MMA is on the softmax's
+        // critical path, S^T(ns) is not needed before the softmax of tile ns
+        if (qready && ns < T && ns - 2 < no && (ns < 2 || mbar_test(&s_free[ns & 1], (uint32_t)((ns - 2) >> 1) & 1u)) &&
+            mbar_test(&k_full[ns & 1], (uint32_t)(ns >> 1) & 1u)) {
+          tc_fence_after();
+          const uint32_t kaddr = smem_u32(smem + L::OFF_K + (ns & 1) * L::KV_BYTES);
+          const uint32_t dS = tmem + (uint32_t)((ns & 1) ? kColS1 : kColS0);
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (uint32_t)((k >> 2) * kAtom + (k & 3) * 32);
-            umma_bf16(tS, sdesc_sw128(qaddr + off, 16, 1024), sdesc_sw128(kaddr + off, 16, 1024), idesc_s,
-                      k > 0 ? 1u : 0u);
+            const uint32_t ka = kaddr + (uint32_t)((k >> 2) * kAtom + (k & 3) * 32);
+            const uint32_t qa = qaddr + (uint32_t)((k >> 2) * L::QSLAB + (k & 3) * 32);
+            umma_bf16(dS, sdesc_sw128(ka, 16, 1024), sdesc_sw128(qa, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
           }
-          umma_commit(&s_full[st]);
-          umma_commit(&k_free[st]);
-          return true;
-        };
-        auto mma_o = [&](int tile) -> bool {   // O += P_tile V_tile
-          const int st = tile & 1;
-          if (!mbar_wait(&v_full[st], (uint32_t)(tile >> 1) & 1u)) return false;
-          ++v_use[st];
-          tc_fence_after();
-          const uint32_t vaddr = smem_u32(smem + L::OFF_KV + (2 + st) * L::KV_BYTES);
-          const uint32_t paddr = smem_u32(smem + L::OFF_P);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {   // 16 keys per step
-            const uint32_t aoff = (uint32_t)((k >> 2) * kAtom + (k & 3) * 32);
-            umma_bf16(tO, sdesc_sw128(paddr + aoff, 16, 1024), sdesc_sw128(vaddr + k * 2048, kAtom, 1024),
-                      idesc_o, (tile > 0 || k > 0) ? 1u : 0u);
-          }
-          umma_commit(&v_free[st]);
-          umma_commit(o_ready);
-          return true;
-        };
-        // K tiles run two ahead of their S MMA (a K stage frees as soon as its
-        // S MMA is done), V tiles two ahead of their O MMA
-        issue(false, 0);
-        issue(true, 0);
-        if (T > 1) {
-          issue(false, 1);
-          issue(true, 1);
+          umma_commit(&s_full[ns & 1]);
+          ++ns;
+          progress = true;
         }
-        bool ok = mbar_wait(q_full, 0) && mma_s(0);
-        if (ok && T > 2) {
-          ok = mbar_wait(&k_free[0], 0);
-          if (ok) issue(false, 2);
+        // K of tile kiss: its stage held tile kiss-2, whose S^T is done (S^T
+        // of tile kiss cannot have run yet, so the parity names tile kiss-2)
+        if (kiss < T && kiss - 2 < ns && mbar_test(&s_full[kiss & 1], (uint32_t)((kiss - 2) >> 1) & 1u)) {
+          issue(false, kiss);
+          ++kiss;
+          progress = true;
         }
-        for (int tl = 0; tl < T && ok; ++tl) {
-          if (tl + 1 < T) {   // S of the next tile, into the buffer softmax(tl - 1) released
-            if (tl >= 1) ok = mbar_wait(&p_full[(tl + 1) & 1], (uint32_t)((tl - 1) >> 1) & 1u);
-            if (ok) ok = mma_s(tl + 1);
-            if (ok && tl + 3 < T) {
-              ok = mbar_wait(&k_free[(tl + 1) & 1], (uint32_t)((tl + 1) >> 1) & 1u);
-              if (ok) issue(false, tl + 3);
-            }
-            if (!ok) break;
-          }
-          ok = mbar_wait(&p_full[tl & 1], (uint32_t)(tl >> 1) & 1u);
-          if (ok) {
-            tc_fence_after();
-            ok = mma_o(tl);
-          }
-          if (ok && tl + 2 < T) {   // V stage tl % 2 is free once this O MMA is done
-            ok = mbar_wait(&v_free[tl & 1], (uint32_t)(tl >> 1) & 1u);
-            if (ok) issue(true, tl + 2);
+        // V of tile viss: its stage held tile viss-2, whose O^T is done (O^T
+        // of tile viss cannot have run yet, so the parity names tile viss-2)
+        if (viss < T && viss - 2 < no && mbar_test(&v_free[viss & 1], (uint32_t)((viss - 2) >> 1) & 1u)) {
+          issue(true, viss);
+          ++viss;
+          progress = true;
+        }
+        if (progress) {
+          t_last = globaltimer();
+          polls = 0;
+        } else {
+          __nanosleep(20);
+          if ((++polls & 255u) == 0 && globaltimer() - t_last > kWaitLimitNs) {
+            ok = false;
+            break;
           }
         }
-        if (!ok) status_set(status, TV_E_TIMEOUT);
-        // loads still in flight land before the CTA leaves
-        for (int st = 0; st < 2; ++st) {
-          if (k_iss[st] > k_use[st]) mbar_wait(&k_full[st], (uint32_t)(k_iss[st] - 1) & 1u);
-          if (v_iss[st] > v_use[st]) mbar_wait(&v_full[st], (uint32_t)(v_iss[st] - 1) & 1u);
-        }
-        umma_commit(drain);   // TMEM is released only after every MMA issued here is complete
-        mbar_wait(drain, 0);
       }
-    } else {
-      // ---------------- softmax / epilogue ----------------
-      // warp (quarter qd, slice cs): query rows 32 qd .. 32 qd + 31 of the tile
-      // (its TMEM lanes), keys kKeysPer cs .. of every 128-key tile, and O
-      // columns OC cs .. OC cs + OC - 1
-      const int qd = warp & 3, cs = warp >> 2;
-      const int i = qd * 32 + lane;
-      const int qi = q0 + i;
-      const bool valid_q = qi < nq;
-      const bool active = q0 + qd * 32 < nq;   // warp-uniform: any valid row in this quarter
-      const int local = valid_q ? qi / G : 0;
-      const uint32_t anc = s_anc[local];
-      for (int idx = threadIdx.x; idx < 128 * (D / 8); idx += kAtSoftThreads) {
-        const int row = idx / (D / 8), c = idx % (D / 8);
-        const int qr = q0 + row;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (qr < nq)
-          v = reinterpret_cast<const uint4*>(q + ((size_t)(row0 + qr / G) * Hq + (size_t)(g * G + qr % G)) * D)[c];
-        *reinterpret_cast<uint4*>(sQ + (c >> 3) * kAtom + swz(row, c & 7)) = v;
+      if (!ok) status_set(status, TV_E_TIMEOUT);
+      // loads still in flight land before the CTA leaves (every load issued is
+      // waited for by an MMA, except after a timeout)
+      for (int j = (ns > 0 ? ns : 0); j < kiss; ++j) mbar_wait(&k_full[j & 1], (uint32_t)(j >> 1) & 1u);
+      for (int j = no; j < viss; ++j) mbar_wait(&v_full[j & 1], (uint32_t)(j >> 1) & 1u);
+      // and every MMA issued is done before TMEM is released
+      if (no > 0) mbar_wait(o_done, (uint32_t)(no - 1) & 1u);
+      if (ns > 0) mbar_wait(&s_full[(ns - 1) & 1], (uint32_t)((ns - 1) >> 1) & 1u);
+    } else if (issuer) {
+      for (int j = 0; j < 2 && j < T; ++j)   // loads issued before the wait land before the CTA leaves
+        if ((pre >> j) & 1u) {
+          mbar_wait(&k_full[j & 1], 0);
+          mbar_wait(&v_full[j & 1], 0);
+        }
+    }
+  } else if (run) {
+    // ---------------- softmax / epilogue (warps 0-15) ----------------
+    // warp (quarter qd, slice cs): TMEM lanes 32 qd .. 32 qd + 31, i.e. key kl
+    // of each tile in S^T and dimension kl in O^T, and the 8-column query
+    // chunks cs, cs + 4, cs + 8, ...
+    const int qd = warp & 3, cs = warp >> 2;
+    const int kl = qd * 32 + lane;
+    const uint32_t lb = (uint32_t)(qd * 32) << 16;
+    const int nu = ((NQ >> 3) - cs + kSlices - 1) / kSlices;   // chunks of this slice
+    uint8_t* sQ = smem + L::OFF_Q;
+    // query column c = local row c / G, head g G + c % G; zero past nq
+    if (threadIdx.x < kNqMax) {
+      const int c = threadIdx.x;
+      s_qrow[c] = c < nq ? (row0 + c / G) * Hq + g * G + c % G : -1;
+      s_canc[c] = c < nq ? s_anc[c / G] : 0u;
+    }
+    soft_sync();
+    for (int idx = threadIdx.x; idx < NQ * (D / 8); idx += kAtSoftThreads) {
+      const int c = idx / (D / 8), e = idx % (D / 8);
+      const int qr = s_qrow[c];
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (qr >= 0) v = reinterpret_cast<const uint4*>(q + (size_t)qr * D)[e];
+      *reinterpret_cast<uint4*>(sQ + (e >> 3) * L::QSLAB + swz(c, e & 7)) = v;
+    }
+    if constexpr (D == 64) {   // O^T is M = 128: dimensions 64..127 read a zero slab
+      for (int idx = threadIdx.x; idx < 2 * kAtom / 16; idx += kAtSoftThreads) {
+        const int st = idx / (kAtom / 16), e = idx % (kAtom / 16);
+        reinterpret_cast<uint4*>(smem + L::OFF_V + st * L::KV_BYTES + kAtom)[e] = make_uint4(0u, 0u, 0u, 0u);
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
+    }
+    for (int c = threadIdx.x; c < kNqMax; c += kAtSoftThreads) {
+      s_m[0][c] = -INFINITY;
+      s_negm[0][c] = INFINITY;
+      s_alpha[c] = 1.f;
+    }
+    fence_async_smem();
+    soft_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_full);
 
-      const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-      float m_use = -INFINITY, l_run = 0.f;   // m_use: the offset P and O are currently scaled by
-      bool ok = true;
-      for (int tl = 0; tl < T; ++tl) {
-        const int b = tl & 1;
-        if (ok) ok = mbar_wait(&s_full[b], (uint32_t)(tl >> 1) & 1u);
-        tc_fence_after();
-        const int kvalid = min(128, nkeys - tl * 128);
-        const bool full = kvalid == 128 && !tree;
-        const uint32_t s_addr = tmem + (uint32_t)(b * 128) + lane_base + cs * kKeysPer;
-        float mx = -INFINITY;   // raw (unscaled) scores; the scale is positive
-        if (active && ok) {   // pass 1: masked row maximum over this thread's keys, 32 at a time
-#pragma unroll
-          for (int h = 0; h < kKeysPer / 32; ++h) {
-            uint32_t s[32];
-            cols_ld<32>(s_addr + h * 32, s);
-            tmem_ld_wait();
-            if (full) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(s[j]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int key = cs * kKeysPer + h * 32 + j;
-                if (key < kvalid && (!tree || ((anc >> key) & 1u))) mx = fmaxf(mx, __uint_as_float(s[j]));
-              }
-            }
-          }
+    // tree tile: bit 8u + j = key kl is an ancestor-or-self of column (cs + 4u) 8 + j's row
+    uint64_t vis = 0;
+    if (has_tree) {
+      for (int u = 0; u < nu; ++u)
+        for (int j = 0; j < 8; ++j) {
+          const int c = (cs + kSlices * u) * 8 + j;
+          if (kl < n && ((s_canc[c] >> kl) & 1u)) vis |= 1ull << (8 * u + j);
         }
-        s_red[b][cs][i] = mx;
-        // keys past the chunk: zero their V rows so that 0 * V stays 0 whatever
-        // those slots hold (all softmax threads share the rows)
-        if (kvalid < 128) {
-          if (ok) ok = mbar_wait(&v_full[b], (uint32_t)(tl >> 1) & 1u);   // the V tile has landed
-          uint8_t* vd = smem + L::OFF_KV + (2 + b) * L::KV_BYTES;
-          const int nz = (128 - kvalid) * L::SLABS * 8;
-          for (int idx = threadIdx.x; idx < nz; idx += kAtSoftThreads) {
-            const int row = kvalid + idx / (L::SLABS * 8), rem = idx % (L::SLABS * 8);
-            *reinterpret_cast<uint4*>(vd + (rem >> 3) * kAtom + row * 128 + (rem & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        quarter_barrier(qd);
-        float m_tile = s_red[b][0][i];
+    }
+
+    float l[kCps][8];   // this key's share of each column sum, at the column's current offset
 #pragma unroll
-        for (int c = 1; c < kSlices; ++c) m_tile = fmaxf(m_tile, s_red[b][c][i]);
-        m_tile *= scale_log2;   // to log2 units
-        // new offset only when the max outgrows the current one by 2^8 (exact:
-        // O and l carry the same offset, which cancels in O / l)
-        const bool grow = m_tile > m_use + kRescaleLog2;
-        const float m_new = grow ? m_tile : m_use;
-        const float corr = (grow && m_use != -INFINITY) ? exp2f(m_use - m_new) : 1.f;
-        if (active && ok) {
-          // P = 2^(x - m) in bf16; the row sum adds the rounded values
-          float lt = 0.f;
-          uint32_t pk[kKeysPer / 2];
-          const float neg_m = m_new == -INFINITY ? 0.f : -m_new;
+    for (int u = 0; u < kCps; ++u)
 #pragma unroll
-          for (int h = 0; h < kKeysPer / 32; ++h) {   // pass 2: P = 2^(x - m), 32 keys at a time
-            uint32_t s[32];
-            cols_ld<32>(s_addr + h * 32, s);
-            tmem_ld_wait();
+      for (int j = 0; j < 8; ++j) l[u][j] = 0.f;
+    const uint32_t tO = tmem + kColO + lb;
+    int ver = 0;   // buffer of the current offsets (slice-uniform)
+    bool ok = true;
+
+    // One 128-key tile, compiled for this slice's chunk count NU and for
+    // whether keys are masked (tree tile, ragged last tile), so that the
+    // common tile carries no per-element mask or bound logic.
+    auto tile = [&](auto nu_c, auto masked_c, int tl) {
+      constexpr int NU = decltype(nu_c)::value;
+      constexpr int NA = NU < 3 ? NU : 3;   // chunks of the first TMEM load wave
+      constexpr bool MASKED = decltype(masked_c)::value;
+      const int b = tl & 1;
+      const bool tree_t = is_tree(tl);
+      const int kvalid = tile_keys(tl);
+      const bool kin = kl < kvalid;
+      const uint32_t sb = tmem + (uint32_t)(b ? kColS1 : kColS0) + lb;
+      // visible keys: bit j of chunk u's mask = column (cs + 4u) 8 + j sees key kl
+      auto vis_mask = [&](int u) -> uint32_t {
+        return tree_t ? (uint32_t)(vis >> (8 * u)) & 0xffu : (kin ? 0xffu : 0u);
+      };
+      // this thread's scores of chunks [U0, U0 + NW), one TMEM round trip, then
+      // f(u, scores) for each chunk
+      auto scores = [&](auto u0_c, auto nw_c, auto&& f) {
+        constexpr int U0 = decltype(u0_c)::value, NW = decltype(nw_c)::value;
+        if constexpr (NW > 0) {
+          uint32_t sv[NW][8];
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              float p0 = ex2(fmaf(__uint_as_float(s[j]), scale_log2, neg_m));
-              float p1 = ex2(fmaf(__uint_as_float(s[j + 1]), scale_log2, neg_m));
-              if (!full) {
-                const int key = cs * kKeysPer + h * 32 + j;
-                if (!(key < kvalid && (!tree || ((anc >> key) & 1u)))) p0 = 0.f;
-                if (!(key + 1 < kvalid && (!tree || ((anc >> (key + 1)) & 1u)))) p1 = 0.f;
-              }
-              lt += p0 + p1;
-              const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-              pk[h * 16 + (j >> 1)] = *reinterpret_cast<const uint32_t*>(&pb);
-            }
-          }
-          l_run = l_run * corr + lt;
-          m_use = m_new;
-          // the P buffer and O are free once O += P V of the previous tile is done
-          if (tl > 0) {
-            if (!mbar_wait(o_ready, (uint32_t)(tl - 1) & 1u)) ok = false;
-            tc_fence_after();
-          }
-          // keys kKeysPer cs .. : 16-byte chunks (8 keys) of row i in the 64-key slabs
-#pragma unroll
-          for (int u = 0; u < kKeysPer / 8; ++u) {
-            const int key8 = cs * kKeysPer + u * 8;
-            *reinterpret_cast<uint4*>(smem + L::OFF_P + (key8 >> 6) * kAtom + swz(i, (key8 & 63) >> 3)) =
-                make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-          }
-          // a grown offset: O (complete up to tile tl-1) gets the same factor
-          if (tl > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-#pragma unroll
-            for (int h = 0; h < OC / 16; ++h) {
-              uint32_t o[16];
-              cols_ld<16>(tO + lane_base + cs * OC + h * 16, o);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
-              cols_st<16>(tO + lane_base + cs * OC + h * 16, o);
-            }
-            tmem_st_wait();
-          }
-        } else if (tl > 0 && ok) {
-          // an idle quarter still waits, so that no warp runs ahead of the O MMA
-          if (!mbar_wait(o_ready, (uint32_t)(tl - 1) & 1u)) ok = false;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[b]);
-      }
-      if (ok) ok = mbar_wait(o_ready, (uint32_t)(T - 1) & 1u);
-      s_l[cs][i] = active ? l_run : 0.f;
-      soft_barrier();
-      if (!ok) {
-        if (lane == 0) status_set(status, TV_E_TIMEOUT);
-      } else if (active) {
-        tc_fence_after();
-        const int hq = g * G + (valid_q ? qi % G : 0);
-        const size_t base = ((size_t)(row0 + local) * Hq + hq) * kChunkSlots + slot;
-        float4* dst = reinterpret_cast<float4*>(part_o + base * D + cs * OC);
-#pragma unroll
-        for (int h = 0; h < OC / 16; ++h) {
-          uint32_t o[16];
-          cols_ld<16>(tO + lane_base + cs * OC + h * 16, o);
+          for (int i = 0; i < NW; ++i) ld8(sb + (cs + kSlices * (U0 + i)) * 8, sv[i]);
           tmem_ld_wait();
-          if (valid_q) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[h * 4 + j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
-                                           __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+          for (int i = 0; i < NW; ++i) f(U0 + i, sv[i]);
+        }
+      };
+      auto all_scores = [&](auto&& f) {
+        scores(std::integral_constant<int, 0>{}, std::integral_constant<int, NA>{}, f);
+        scores(std::integral_constant<int, NA>{}, std::integral_constant<int, NU - NA>{}, f);
+      };
+
+      if (ok && !mbar_wait(&s_full[b], (uint32_t)(tl >> 1) & 1u)) ok = false;
+      tc_fence_after();
+
+      // Pass 1: the largest x = s scale - m of a visible key.  An offset must
+      // move when an x passes 8 (on the first tile no offset is set): the
+      // slice agrees on that with one barrier reduction, and only then are
+      // the tile's column maxima taken.
+      bool moved = tl == 0;
+      if (!moved) {
+        float xmax = -INFINITY;
+        const float* negm = s_negm[ver];
+        all_scores([&](int u, const uint32_t (&sv)[8]) {
+          const int c0 = (cs + kSlices * u) * 8;
+          const float4 m0 = *reinterpret_cast<const float4*>(&negm[c0]);
+          const float4 m1 = *reinterpret_cast<const float4*>(&negm[c0 + 4]);
+          const float nm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+          const uint32_t vm = MASKED ? vis_mask(u) : 0xffu;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float x = fmaf(__uint_as_float(sv[j]), scale_log2, nm[j]);
+            if (!MASKED || ((vm >> j) & 1u)) xmax = fmaxf(xmax, x);
+          }
+        });
+        moved = slice_any(xmax > kRescaleLog2, cs);
+      }
+      if (moved) {
+        // the tile's column maxima over all 128 keys (raw scores)
+        all_scores([&](int u, const uint32_t (&sv)[8]) {
+          const uint32_t vm = MASKED ? vis_mask(u) : 0xffu;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float x = redux_max(((vm >> j) & 1u) ? __uint_as_float(sv[j]) : -INFINITY);
+            if (lane == 0) s_red[qd][(cs + kSlices * u) * 8 + j] = x;
+          }
+        });
+        slice_sync(cs);
+        // one thread per column of the slice: its new offset and factor
+        const int st = qd * 32 + lane;
+        if (st < NU * 8) {
+          const int c = (cs + kSlices * (st >> 3)) * 8 + (st & 7);
+          const float cm = fmaxf(fmaxf(s_red[0][c], s_red[1][c]), fmaxf(s_red[2][c], s_red[3][c])) * scale_log2;
+          const float mo = s_m[ver][c];
+          const float mn = cm > mo + kRescaleLog2 ? cm : mo;
+          s_m[ver ^ 1][c] = mn;
+          s_negm[ver ^ 1][c] = -mn;
+          s_alpha[c] = mn == mo ? 1.f : ex2(mo - mn);
+        }
+        slice_sync(cs);
+        ver ^= 1;
+        if (tl > 0) {   // the sums move to the new offsets
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            const int c0 = (cs + kSlices * u) * 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) l[u][j] *= s_alpha[c0 + j];
           }
         }
-        if (valid_q) {
-          if (cs == 0) {
-            float l = s_l[0][i];
+      }
+
+      // Pass 2: P = 2^(s scale - m) rounded to bf16, a chunk at a time (one
+      // TMEM round trip each, which keeps the live scores to 8 registers);
+      // the column sums add the rounded values, the weights O^T gets, so that
+      // a key that dominates its column passes its V row through unchanged.
+      // This pass overlaps O^T of the previous tile, which still reads P^T:
+      // each chunk's P is parked in TMEM over the scores it came from (this
+      // thread's lane, this slice's columns) until P^T is free.
+      {
+        const float* negm = s_negm[ver];
 #pragma unroll
-            for (int c = 1; c < kSlices; ++c) l += s_l[c][i];
-            part_ml[base * 2] = m_use;
-            part_ml[base * 2 + 1] = l;
+        for (int u = 0; u < NU; ++u) {
+          const int c0 = (cs + kSlices * u) * 8;
+          uint32_t sv[8];
+          ld8(sb + c0, sv);
+          const float4 m0 = *reinterpret_cast<const float4*>(&negm[c0]);
+          const float4 m1 = *reinterpret_cast<const float4*>(&negm[c0 + 4]);
+          const float nm[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+          const uint32_t vm = MASKED ? vis_mask(u) : 0xffu;
+          tmem_ld_wait();
+          uint32_t pk[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            float x0 = fmaf(__uint_as_float(sv[j]), scale_log2, nm[j]);
+            float x1 = fmaf(__uint_as_float(sv[j + 1]), scale_log2, nm[j + 1]);
+            if (MASKED && !((vm >> j) & 1u)) x0 = -INFINITY;
+            if (MASKED && !((vm >> (j + 1)) & 1u)) x1 = -INFINITY;
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2(x0), ex2(x1));
+            pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+            l[u][j] += __uint_as_float(pk[j >> 1] << 16);
+            l[u][j + 1] += __uint_as_float(pk[j >> 1] & 0xffff0000u);
+          }
+          st4(sb + c0, pk);
+        }
+        tmem_st_wait();
+      }
+
+      // keys past the tile's valid ones: zero their V rows so that 0 * V stays 0
+      // whatever those slots hold (all softmax threads share the rows)
+      if (MASKED && kvalid < 128) {
+        if (ok && !mbar_wait(&v_full[b], (uint32_t)(tl >> 1) & 1u)) ok = false;
+        uint8_t* vd = smem + L::OFF_V + b * L::KV_BYTES;
+        const int per_row = (D / 64) * 8;
+        for (int idx = threadIdx.x; idx < (128 - kvalid) * per_row; idx += kAtSoftThreads) {
+          const int row = kvalid + idx / per_row, rem = idx % per_row;
+          *reinterpret_cast<uint4*>(vd + (rem >> 3) * kAtom + row * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // P^T and O^T are free once O^T += V^T P^T of the previous tile is done
+      if (tl > 0) {
+        if (ok && !mbar_wait(o_done, (uint32_t)(tl - 1) & 1u)) ok = false;
+        tc_fence_after();
+        if (moved) {   // O^T columns (complete up to tile tl-1) move to the new offsets
+#pragma unroll
+          for (int u = 0; u < NU; ++u) {
+            const int c0 = (cs + kSlices * u) * 8;
+            uint32_t o[8];
+            ld8(tO + c0, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * s_alpha[c0 + j]);
+            st8(tO + c0, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      {   // the parked P into key kl's row of P^T (8 query columns = one 16-byte chunk)
+        uint32_t pk[NU > 0 ? NU : 1][4];
+#pragma unroll
+        for (int u = 0; u < NU; ++u) ld4(sb + (cs + kSlices * u) * 8, pk[u]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          const int k = cs + kSlices * u;
+          *reinterpret_cast<uint4*>(smem + L::OFF_P + (k >> 3) * kAtom + swz(kl, k & 7)) =
+              make_uint4(pk[u][0], pk[u][1], pk[u][2], pk[u][3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[b]);   // S^T[b] may take tile tl + 2
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    };
+    using std::integral_constant;
+    auto tile_nu = [&](auto nu_c, int tl) {
+      const bool masked = is_tree(tl) || tile_keys(tl) < 128;
+      if (masked) tile(nu_c, integral_constant<bool, true>{}, tl);
+      else tile(nu_c, integral_constant<bool, false>{}, tl);
+    };
+    for (int tl = 0; tl < T; ++tl) {
+      switch (nu) {   // slice-uniform
+        case 5: tile_nu(integral_constant<int, 5>{}, tl); break;
+        case 4: tile_nu(integral_constant<int, 4>{}, tl); break;
+        case 3: tile_nu(integral_constant<int, 3>{}, tl); break;
+        case 2: tile_nu(integral_constant<int, 2>{}, tl); break;
+        case 1: tile_nu(integral_constant<int, 1>{}, tl); break;
+        default: tile_nu(integral_constant<int, 0>{}, tl); break;
+      }
+    }
+
+    // ---- epilogue: unnormalised O, offsets and sums of this chunk --------------
+    if (ok && !mbar_wait(o_done, (uint32_t)(T - 1) & 1u)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    // column sums over the 128 keys: every MMA and load is done, so the K/V
+    // stages hold a [key][column] table (row stride 161 words: no bank conflicts)
+    float* lsum = reinterpret_cast<float*>(smem + L::OFF_K);
+    if (ok) {
+#pragma unroll
+      for (int u = 0; u < kCps; ++u) {
+        if (u < nu) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) lsum[kl * (kNqMax + 1) + (cs + kSlices * u) * 8 + j] = l[u][j];
+        }
+      }
+    }
+    soft_sync();
+    if (ok) {
+      for (int c = warp; c < NQ; c += kAtSoftWarps) {
+        float x = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x += lsum[(lane + 32 * i) * (kNqMax + 1) + c];
+        x = warp_sum(x);
+        if (lane == 0) s_red[0][c] = x;
+      }
+    }
+    soft_sync();
+    if (!ok) {
+      if (lane == 0) status_set(status, TV_E_TIMEOUT);
+    } else {
+      for (int u = 0; u < nu; ++u) {
+        const int c0 = (cs + kSlices * u) * 8;
+        uint32_t o[8];
+        ld8(tO + c0, o);
+        tmem_ld_wait();
+        if (kl < D) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int qr = s_qrow[c0 + j];
+            if (qr >= 0) part_o[((size_t)qr * kChunkSlots + chunk) * D + kl] = __uint_as_float(o[j]);
+          }
+        }
+      }
+      if (qd == 0 && lane < 8) {
+        for (int u = 0; u < nu; ++u) {
+          const int c = (cs + kSlices * u) * 8 + lane;
+          const int qr = s_qrow[c];
+          if (qr >= 0) {
+            const size_t base = (size_t)qr * kChunkSlots + chunk;
+            part_ml[base * 2] = s_m[ver][c];
+            part_ml[base * 2 + 1] = s_red[0][c];
           }
         }
       }
@@ -506,28 +692,28 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kAtSoftWarps) {
+  if (warp == kWarpIssue) {
     tc_fence_after();
     tmem_dealloc(tmem, kAtTmemCols);
   }
 }
 
 // out[row][h*D + d] = bf16( sum_c o_c[d] 2^(m_c - M) / sum_c l_c 2^(m_c - M) ),
-// chunks in order 0..nch-1, then the tree slot.  grid (rows, Hq), block D.
-__global__ void attn_merge_kernel(ReqTable t, const RowMeta* meta, int Hq, int D, const float* part_ml,
-                                  const float* part_o, __nv_bfloat16* out, const int32_t* status) {
+// chunks in order.  grid (rows, Hq), block D.
+__global__ void attn_merge_kernel(ReqTable t, const RowMeta* meta, int Hq, int D, int chunk_target,
+                                  const float* part_ml, const float* part_o, __nv_bfloat16* out,
+                                  const int32_t* status) {
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x, hq = blockIdx.y, d = threadIdx.x;
-  const int nch = attn_n_chunks(t.ctx[meta[row].req]);
+  const int nch = attn_plan(t.ctx[meta[row].req], chunk_target).n_chunks;
   const size_t base = ((size_t)row * Hq + hq) * kChunkSlots;
-  float M = part_ml[(base + kTreeSlot) * 2];
+  float M = -INFINITY;
   for (int c = 0; c < nch; ++c) M = fmaxf(M, part_ml[(base + c) * 2]);
   float L = 0.f, O = 0.f;
-  for (int k = 0; k <= nch; ++k) {
-    const int c = k < nch ? k : kTreeSlot;
-    const float w = exp2f(part_ml[(base + c) * 2] - M);   // maxima are in log2 units
+  for (int c = 0; c < nch; ++c) {
+    const float w = exp2f(part_ml[(base + c) * 2] - M);   // offsets are in log2 units
     L = fmaf(part_ml[(base + c) * 2 + 1], w, L);
     O = fmaf(part_o[(base + c) * D + d], w, O);
   }
@@ -535,40 +721,40 @@ __global__ void attn_merge_kernel(ReqTable t, const RowMeta* meta, int Hq, int D
 }
 
 template <int D>
-int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b, int32_t* status,
+int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b, int sms, int32_t* status,
                        cudaStream_t st) {
   AttnMaps maps;
   memset(&maps, 0, sizeof(maps));
-  int nch_max = 0, nq_max = 0;
-  const int G = dm.n_q_heads / dm.n_kv_heads;
+  const int target = attn_chunk_target(sms, dm.n_kv_heads);
+  int nch_max = 0;
   for (int r = 0; r < t.n_req; ++r) {
     const int rows = dm.n_kv_heads * t.capacity[r];
     int rc = make_tmap_bf16(&maps.k[r], t.k[r], D, rows, 64, 128);
     if (rc) return rc;
     rc = make_tmap_bf16(&maps.v[r], t.v[r], D, rows, 64, 128);
     if (rc) return rc;
-    nch_max = max(nch_max, attn_n_chunks(t.ctx[r]));
-    nq_max = max(nq_max, t.n[r] * G);
+    nch_max = max(nch_max, attn_plan(t.ctx[r], target).n_chunks);
   }
-  const int q_tiles = (nq_max + 127) / 128;
   const size_t smem = AtSmem<D>::BYTES;
   static bool attr[64] = {false};
   if (ensure_smem_limit(attn_tc_kernel<D>, smem, attr)) return TV_E_CUDA;
-  dim3 grid(q_tiles, nch_max + 1, t.n_req * dm.n_kv_heads);
+  dim3 grid(nch_max, dm.n_kv_heads, t.n_req);
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));   // log2(e) / sqrt(D)
   int rc = launch_pdl(attn_tc_kernel<D>, grid, dim3(kAtThreads), smem, st, maps, t, (const RowMeta*)b.meta,
-                      (const __nv_bfloat16*)b.q, dm.n_q_heads, dm.n_kv_heads, scale_log2, b.attn_ml, b.attn_o,
-                      status);
+                      (const __nv_bfloat16*)b.q, dm.n_q_heads, dm.n_kv_heads, target, scale_log2, b.attn_ml,
+                      b.attn_o, status);
   if (rc) return rc;
   return launch_pdl(attn_merge_kernel, dim3(t.total_rows, dm.n_q_heads), dim3(D), 0, st, t, (const RowMeta*)b.meta,
-                    dm.n_q_heads, D, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn, (const int32_t*)status);
+                    dm.n_q_heads, D, target, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn,
+                    (const int32_t*)status);
 }
 
 }  // namespace
 
-int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st) {
-  if (d.head_dim == 128) return launch_attention_d<128>(t, d, b, status, st);
-  if (d.head_dim == 64) return launch_attention_d<64>(t, d, b, status, st);
+int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int sms, int32_t* status,
+                     cudaStream_t st) {
+  if (d.head_dim == 128) return launch_attention_d<128>(t, d, b, sms, status, st);
+  if (d.head_dim == 64) return launch_attention_d<64>(t, d, b, sms, status, st);
   return TV_E_UNSUPPORTED;
 }
 

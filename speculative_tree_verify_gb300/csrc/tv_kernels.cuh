@@ -7,20 +7,30 @@
 
 namespace tv {
 
-// ---- attention chunking: a function of the context length only ------------
-constexpr int kMaxChunks = 32;               // cache chunks per request
-constexpr int kTreeSlot = kMaxChunks;        // partial slot of the tree keys
-constexpr int kChunkSlots = kMaxChunks + 1;
+// ---- attention chunking ------------------------------------------------------
+// The cached keys of a request are cut into chunks of whole 128-key tiles.  The
+// number of chunks aims at `target` = SMs / KV heads (at most kMaxChunks), so
+// that one request's chunks x KV heads fill the GPU once; it depends on the
+// context length, the model and the GPU only, never on the other rows or
+// requests of the pass.  The tree keys get a chunk of their own while the
+// cached tiles are fewer than the target (short contexts: one more CTA in the
+// same wave), and otherwise join the last chunk.
+constexpr int kMaxChunks = 32;
+constexpr int kChunkSlots = kMaxChunks + 1;   // partial slots per (row, head) in the workspace
 
-// keys per chunk: a multiple of the attention kernel's 128-key tile
-__host__ __device__ inline int attn_chunk_len(int ctx) {
-  const int per = (ctx + kMaxChunks - 1) / kMaxChunks;
-  const int ch = ((per + 127) / 128) * 128;
-  return ch < 128 ? 128 : ch;
+struct AttnPlan {
+  int tiles_per_chunk;
+  int n_chunks;    // chunks in all, the tree's own chunk included
+  bool tree_own;   // the last chunk holds only the tree keys
+};
+__host__ __device__ inline AttnPlan attn_plan(int ctx, int target) {
+  const int tiles = ctx > 0 ? (ctx + 127) / 128 : 0;
+  target = target < 1 ? 1 : (target > kMaxChunks ? kMaxChunks : target);
+  if (tiles < target) return AttnPlan{1, tiles + 1, true};
+  const int per = (tiles + target - 1) / target;
+  return AttnPlan{per, (tiles + per - 1) / per, false};
 }
-__host__ __device__ inline int attn_n_chunks(int ctx) {
-  return ctx <= 0 ? 0 : (ctx + attn_chunk_len(ctx) - 1) / attn_chunk_len(ctx);
-}
+inline int attn_chunk_target(int sms, int n_kv_heads) { return n_kv_heads > 0 ? sms / n_kv_heads : 1; }
 
 // ---- residual walk: per-row statistics over vocabulary chunks --------------
 constexpr int kVChunk = 4096;
@@ -79,8 +89,8 @@ struct LayerBufs {
   __nv_bfloat16* h;        // [32][H]
   __nv_bfloat16* q;        // [32][Hq][D]
   float* part_qkv;
-  float* attn_ml;          // [32][Hq][kChunkSlots][2]
-  float* attn_o;           // [32][Hq][kChunkSlots][D]
+  float* attn_ml;          // [32][Hq][kChunkSlots][2]: chunk max (log2 units), chunk sum
+  float* attn_o;           // [32][Hq][kChunkSlots][D]: chunk output, not normalised
   __nv_bfloat16* attn;     // [rows][Hq D]
   float* part_o;
   __nv_bfloat16* hf;       // [32][H]
@@ -90,7 +100,8 @@ int launch_prologue(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int
 int launch_embed_norm(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status, cudaStream_t st);
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
                         cudaStream_t st);
-int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st);
+int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int sms, int32_t* status,
+                     cudaStream_t st);
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st);
 
