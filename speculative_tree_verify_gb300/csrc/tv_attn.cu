@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   // ---- TMA issue ------------------------------------------------------------------
   int kiss = 0, viss = 0;   // K / V tiles issued (in tile order)
-  uint32_t pre = 0;         // bit j: K_j and V_j issued before the wait
+  uint32_t pre = 0;         // bit j: K_j issued before the wait
   const uint64_t pol = policy_evict_first();
   auto issue = [&](bool is_v, int j) {
     const int st = j & 1;
@@ -274,10 +274,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     // its predecessor before it completes, so every earlier writer of the
     // cache is done.  The tree slots (written by the previous kernel) and the
     // queries are read after the wait.
-    for (int j = 0; j < 2 && j < T; ++j)
+    for (int j = 0; j < 2 && j < T; ++j)   // K only: the V tiles wait until the queries are staged
       if (pre_ok(j)) {
         issue(false, j);
-        issue(true, j);
         pre |= 1u << j;
       }
   }
@@ -297,11 +296,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       const uint32_t idesc_s = idesc_bf16_f32(128, NQ);
       const uint32_t idesc_o = idesc_bf16_f32(128, NQ) | (1u << 15) | (1u << 16);   // A = V^T, B = P^T: MN-major
       for (int j = 0; j < 2 && j < T; ++j)
-        if (!((pre >> j) & 1u)) {
-          issue(false, j);
-          issue(true, j);
-        }
-      kiss = viss = T < 2 ? T : 2;
+        if (!((pre >> j) & 1u)) issue(false, j);
+      kiss = T < 2 ? T : 2;
+      viss = 0;
       int ns = 0, no = 0;   // S^T / O^T MMAs issued
       bool qready = false, ok = true;
       unsigned long long t_last = globaltimer();
@@ -349,7 +346,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         // V of tile viss: its stage held tile viss-2, whose O^T is done (O^T
         // of tile viss cannot have run yet, so the parity names tile viss-2)
-        if (viss < T && viss - 2 < no && mbar_test(&v_free[viss & 1], (uint32_t)((viss - 2) >> 1) & 1u)) {
+        // (the first two once the queries are staged, so that the query loads
+        // do not queue behind them)
+        if (viss < T && (viss < 2 ? qready : viss - 2 < no && mbar_test(&v_free[viss & 1], (uint32_t)((viss - 2) >> 1) & 1u))) {
           issue(true, viss);
           ++viss;
           progress = true;
@@ -375,10 +374,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       if (ns > 0) mbar_wait(&s_full[(ns - 1) & 1], (uint32_t)((ns - 1) >> 1) & 1u);
     } else if (issuer) {
       for (int j = 0; j < 2 && j < T; ++j)   // loads issued before the wait land before the CTA leaves
-        if ((pre >> j) & 1u) {
-          mbar_wait(&k_full[j & 1], 0);
-          mbar_wait(&v_full[j & 1], 0);
-        }
+        if ((pre >> j) & 1u) mbar_wait(&k_full[j & 1], 0);
     }
   } else if (run) {
     // ---------------- softmax / epilogue (warps 0-15) ----------------
@@ -397,12 +393,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       s_canc[c] = c < nq ? s_anc[c / G] : 0u;
     }
     soft_sync();
-    for (int idx = threadIdx.x; idx < NQ * (D / 8); idx += kAtSoftThreads) {
-      const int c = idx / (D / 8), e = idx % (D / 8);
-      const int qr = s_qrow[c];
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (qr >= 0) v = reinterpret_cast<const uint4*>(q + (size_t)qr * D)[e];
-      *reinterpret_cast<uint4*>(sQ + (e >> 3) * L::QSLAB + swz(c, e & 7)) = v;
+    {   // all of this thread's 16-byte pieces are loaded before any is stored
+      constexpr int kPer = (kNqMax * (D / 8) + kAtSoftThreads - 1) / kAtSoftThreads;
+      uint4 v[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int idx = threadIdx.x + kAtSoftThreads * i;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < NQ * (D / 8)) {
+          const int qr = s_qrow[idx / (D / 8)];
+          if (qr >= 0) v[i] = reinterpret_cast<const uint4*>(q + (size_t)qr * D)[idx % (D / 8)];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int idx = threadIdx.x + kAtSoftThreads * i;
+        if (idx < NQ * (D / 8)) {
+          const int c = idx / (D / 8), e = idx % (D / 8);
+          *reinterpret_cast<uint4*>(sQ + (e >> 3) * L::QSLAB + swz(c, e & 7)) = v[i];
+        }
+      }
     }
     if constexpr (D == 64) {   // O^T is M = 128: dimensions 64..127 read a zero slab
       for (int idx = threadIdx.x; idx < 2 * kAtom / 16; idx += kAtSoftThreads) {
@@ -650,42 +660,63 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
       }
     }
-    soft_sync();
+    // O^T of this thread's dimension and columns, loaded while the sums are formed
+    uint32_t o[kCps][8];
     if (ok) {
-      for (int c = warp; c < NQ; c += kAtSoftWarps) {
-        float x = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) x += lsum[(lane + 32 * i) * (kNqMax + 1) + c];
-        x = warp_sum(x);
-        if (lane == 0) s_red[0][c] = x;
+      for (int u = 0; u < kCps; ++u)
+        if (u < nu) ld8(tO + (cs + kSlices * u) * 8, o[u]);
+    }
+    soft_sync();
+    if (ok) {   // warp w sums columns w, w + 16, ...: all loads, then the shuffles, interleaved
+      constexpr int kCols = kNqMax / kAtSoftWarps;
+      float x[kCols];
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) {
+        const int c = warp + kAtSoftWarps * i;
+        x[i] = 0.f;
+        if (c < NQ) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) x[i] += lsum[(lane + 32 * k) * (kNqMax + 1) + c];
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], off);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kCols; ++i)
+          if (warp + kAtSoftWarps * i < NQ) s_red[0][warp + kAtSoftWarps * i] = x[i];
+      }
+    }
+    if (ok) {
+      tmem_ld_wait();
+      if (kl < D) {
+#pragma unroll
+        for (int u = 0; u < kCps; ++u) {
+          if (u < nu) {
+            const int c0 = (cs + kSlices * u) * 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int qr = s_qrow[c0 + j];
+              if (qr >= 0) part_o[((size_t)qr * kChunkSlots + chunk) * D + kl] = __uint_as_float(o[u][j]);
+            }
+          }
+        }
       }
     }
     soft_sync();
     if (!ok) {
       if (lane == 0) status_set(status, TV_E_TIMEOUT);
-    } else {
+    } else if (qd == 0 && lane < 8) {
       for (int u = 0; u < nu; ++u) {
-        const int c0 = (cs + kSlices * u) * 8;
-        uint32_t o[8];
-        ld8(tO + c0, o);
-        tmem_ld_wait();
-        if (kl < D) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int qr = s_qrow[c0 + j];
-            if (qr >= 0) part_o[((size_t)qr * kChunkSlots + chunk) * D + kl] = __uint_as_float(o[j]);
-          }
-        }
-      }
-      if (qd == 0 && lane < 8) {
-        for (int u = 0; u < nu; ++u) {
-          const int c = (cs + kSlices * u) * 8 + lane;
-          const int qr = s_qrow[c];
-          if (qr >= 0) {
-            const size_t base = (size_t)qr * kChunkSlots + chunk;
-            part_ml[base * 2] = s_m[ver][c];
-            part_ml[base * 2 + 1] = s_red[0][c];
-          }
+        const int c = (cs + kSlices * u) * 8 + lane;
+        const int qr = s_qrow[c];
+        if (qr >= 0) {
+          const size_t base = (size_t)qr * kChunkSlots + chunk;
+          part_ml[base * 2] = s_m[ver][c];
+          part_ml[base * 2 + 1] = s_red[0][c];
         }
       }
     }
@@ -703,20 +734,37 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 __global__ void attn_merge_kernel(ReqTable t, const RowMeta* meta, int Hq, int D, int chunk_target,
                                   const float* part_ml, const float* part_o, __nv_bfloat16* out,
                                   const int32_t* status) {
+  __shared__ float s_mc[kChunkSlots], s_lc[kChunkSlots], s_w[kChunkSlots];
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x, hq = blockIdx.y, d = threadIdx.x;
   const int nch = attn_plan(t.ctx[meta[row].req], chunk_target).n_chunks;
   const size_t base = ((size_t)row * Hq + hq) * kChunkSlots;
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, part_ml[(base + c) * 2]);
-  float L = 0.f, O = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float w = exp2f(part_ml[(base + c) * 2] - M);   // offsets are in log2 units
-    L = fmaf(part_ml[(base + c) * 2 + 1], w, L);
-    O = fmaf(part_o[(base + c) * D + d], w, O);
+  // every chunk's offset and sum at once (one load each), then the weights
+  for (int c = d; c < nch; c += blockDim.x) {
+    s_mc[c] = part_ml[(base + c) * 2];
+    s_lc[c] = part_ml[(base + c) * 2 + 1];
   }
+  __syncthreads();
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, s_mc[c]);
+  for (int c = d; c < nch; c += blockDim.x) s_w[c] = exp2f(s_mc[c] - M);   // offsets are in log2 units
+  __syncthreads();
+  float L = 0.f;
+  for (int c = 0; c < nch; ++c) L = fmaf(s_lc[c], s_w[c], L);
+  // the chunks' outputs, eight loads in flight, summed in chunk order
+  const float* po = part_o + base * D + d;
+  float O = 0.f;
+  int c = 0;
+  for (; c + 8 <= nch; c += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = po[(size_t)(c + i) * D];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) O = fmaf(v[i], s_w[c + i], O);
+  }
+  for (; c < nch; ++c) O = fmaf(po[(size_t)c * D], s_w[c], O);
   out[(size_t)row * Hq * D + (size_t)hq * D + d] = f2bf(O / L);
 }
 

@@ -147,6 +147,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Wait for the phase with the given parity to complete; false after the limit.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   unsigned long long t0 = 0;
   uint32_t spins = 0;
