@@ -74,6 +74,9 @@ extern "C" {
 #define TV_E_UNSUPPORTED -11   /* a shape these kernels do not handle (see tv_dims)     */
 #define TV_E_TIMEOUT     -12   /* a bounded device wait gave up                         */
 #define TV_E_PATH        -13   /* commit: accept_len or a path entry out of range       */
+#define TV_E_CHAIN       -14   /* single-path sampling on a tree that is not a chain    */
+#define TV_E_PROPOSAL    -15   /* a proposal row not finite, negative, off unit mass, or
+                                  zero at its draft                                     */
 
 typedef uint16_t tv_bf16;
 
@@ -234,6 +237,109 @@ TV_API int tv_accept_residual_noalloc(const tv_tree *trees, int n_req, const flo
 TV_API int tv_commit_kv(const tv_kv *kv, const tv_dims *dims, const tv_tree *trees, int n_req,
                  const int32_t *path, const int32_t *accept_len,
                  int32_t *committed_src, int32_t *new_ctx, int32_t *dev_status, void *stream);
+
+/*
+ * Sampled variants [Exactness, §Sampling; Drafters and tree verify,
+ * §Sampling; Algorithm and correctness contract, §Single-path sampling].
+ * They read the verify's fp32 logits (or the output of tv_sample_filter with
+ * temperature 1) and need a workspace of tv_sample_workspace_size() bytes.
+ */
+
+/* Bytes of workspace the sampled entry points need for up to max_rows rows
+ * (<= 32) of this vocabulary.  Host-only. */
+TV_API int tv_sample_workspace_size(int32_t vocab, int max_rows, size_t *bytes);
+
+/*
+ * Sampling filters through one function [Exactness, §Sampling, second
+ * paragraph]: filtered[row][y] = logits[row][y] / temperature for the tokens
+ * the filters keep and -inf for the rest, so that softmax(filtered) is the
+ * filtered, renormalised distribution and every sampled walk can run on it
+ * with temperature 1 (drafted rows and plain rows see the same filters).
+ * Applied in this order, each on the distribution the previous ones left:
+ *   top_k (0 = off)  keep the tokens whose logit is at least the k-th largest
+ *                    (tokens tied with it are all kept);
+ *   top_p (1 = off)  keep the fewest largest-probability tokens whose mass
+ *                    reaches top_p (ties at the boundary all kept);
+ *   min_p (0 = off)  keep the tokens with p >= min_p * max p.
+ * The k-th largest logit and the top-p boundary are found exactly (radix
+ * selection on the logits' bits), so the result does not depend on the run.
+ *
+ *   logits    device fp32 [rows][vocab];  filtered  device fp32 [rows][vocab]
+ *             (may not alias logits)
+ * Host checks: TV_E_ARG (null pointers, rows outside 1..32, vocab < 2,
+ * top_k < 0, top_p outside (0, 1], min_p outside [0, 1)), TV_E_TEMP.
+ */
+TV_API int tv_sample_filter(const float *logits, float *filtered, int rows, int32_t vocab, float temperature,
+                            int32_t top_k, float top_p, float min_p, int32_t *dev_status, void *stream);
+
+/*
+ * Single-draw sampled verify [Exactness, §Sampling, first paragraph; Drafters
+ * and tree verify, §Sampling]: at each node of the walk the target draws its
+ * own token y from p = softmax(logits_row / temperature); if a child of the
+ * node carries y the walk moves there, otherwise y is the round's last token
+ * (at a leaf the draw is the last token).  Same law as tv_accept_residual.
+ * Every row draws once, with its own uniform, by the inverse CDF (the smallest
+ * y with sum_{j<=y} p(j) > u); the walk then follows these draws.
+ *
+ *   uniforms     device fp32 [total_rows], one per row
+ *   row_tokens   device int32 [total_rows]: every row's draw
+ *   path, accept_len  as tv_accept_greedy
+ *   out_tokens   device int32 [total_rows]: the a_r accepted drafts, then the
+ *                draw at the stopping node (a_r + 1 tokens)
+ * Host checks: TV_E_TEMP, TV_E_ARG, TV_E_ROWS, TV_E_WORKSPACE.  Device checks:
+ * TV_E_ORDER, TV_E_DUP_SIBLING, TV_E_UNIFORM.
+ */
+TV_API int tv_accept_single_draw(const tv_tree *trees, int n_req, const float *logits, int32_t vocab,
+                                 float temperature, const float *uniforms, int32_t *row_tokens,
+                                 int32_t *path, int32_t *accept_len, int32_t *out_tokens,
+                                 int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Seeded sampled verify [Exactness, §Sampling, third paragraph; Drafters and
+ * tree verify, §Sampling]: the token at sequence index t is
+ * argmax_y (logits_row[y] / temperature + G_t(y)), G_t(y) = -log(-log U) with
+ * U = (w + 0.5) / 2^32, w the first word of Philox4x32-10 (Salmon et al., SC
+ * 2011) at counter (y, t, 0, 0) under key (seed low 32 bits, seed high 32 bits).
+ * Row i (node i at position positions[r] + depth(i)) scores the token at
+ * t = positions[r] + depth(i) + 1, so a request's text depends on its seed
+ * and its logits only, never on what was drafted.  The walk follows these
+ * draws as tv_accept_single_draw does.
+ *
+ *   seeds        host uint64 [n_req]
+ *   positions    host int32 [n_req]: sequence index of each root's token
+ *   row_tokens, path, accept_len, out_tokens  as tv_accept_single_draw
+ * Host checks: TV_E_TEMP, TV_E_ARG, TV_E_ROWS, TV_E_WORKSPACE.  Device checks:
+ * TV_E_ORDER, TV_E_DUP_SIBLING.
+ */
+TV_API int tv_accept_gumbel(const tv_tree *trees, int n_req, const float *logits, int32_t vocab,
+                            float temperature, const uint64_t *seeds, const int32_t *positions,
+                            int32_t *row_tokens, int32_t *path, int32_t *accept_len, int32_t *out_tokens,
+                            int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Single-path rejection sampling [Algorithm and correctness contract,
+ * §Single-path sampling]: the tree must be a chain (parent[i] = i - 1).  Node
+ * i carries draft x_i, drawn by the caller's drafter from the proposal row
+ * proposals[row_off(r) + i]; its target is p = softmax(logits of row i - 1 /
+ * temperature).  Draft i is accepted iff uniforms[row_off(r) + i] < p(x_i) /
+ * q(x_i) (probability min(1, p/q)).  At the first rejection one token is drawn
+ * from normalize(max(p - q, 0)) by the inverse CDF with
+ * uniforms[row_off(r)] and the round ends; a fully accepted chain ends with no
+ * extra token.
+ *
+ *   proposals    device fp32 [total_rows][vocab]; the root's row is not read.
+ *                Every other row must be finite, nonnegative, of unit mass
+ *                (|sum - 1| <= 1e-3, summed in fp64) and nonzero at its draft
+ *   uniforms     device fp32 [total_rows], all validated
+ *   path, accept_len, out_tokens, out_count  as tv_accept_residual
+ * Host checks: TV_E_TEMP, TV_E_ARG, TV_E_ROWS, TV_E_WORKSPACE.  Device checks:
+ * TV_E_ORDER, TV_E_DUP_SIBLING, TV_E_TOKEN, TV_E_CHAIN, TV_E_UNIFORM,
+ * TV_E_PROPOSAL.
+ */
+TV_API int tv_accept_rejection(const tv_tree *trees, int n_req, const float *logits, int32_t vocab,
+                               float temperature, const float *proposals, const float *uniforms,
+                               int32_t *path, int32_t *accept_len, int32_t *out_tokens, int32_t *out_count,
+                               int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Optional stage timing of tv_verify_tree (for price tables and roofline

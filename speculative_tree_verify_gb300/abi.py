@@ -19,13 +19,16 @@ TV_OK = 0
 STATUS = {
     0: "TV_OK", -1: "TV_E_ARG", -2: "TV_E_ORDER", -3: "TV_E_DUP_SIBLING", -4: "TV_E_TOKEN",
     -5: "TV_E_CAPACITY", -6: "TV_E_ROWS", -7: "TV_E_UNIFORM", -8: "TV_E_TEMP", -9: "TV_E_WORKSPACE",
-    -10: "TV_E_CUDA", -11: "TV_E_UNSUPPORTED", -12: "TV_E_TIMEOUT", -13: "TV_E_PATH",
+    -10: "TV_E_CUDA", -11: "TV_E_UNSUPPORTED", -12: "TV_E_TIMEOUT", -13: "TV_E_PATH", -14: "TV_E_CHAIN",
+    -15: "TV_E_PROPOSAL",
 }
 CODES = {v: k for k, v in STATUS.items()}
 
 # entry points declared in include/tv.h
 SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv",
-           "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc")
+           "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc",
+           "tv_sample_workspace_size", "tv_sample_filter", "tv_accept_single_draw", "tv_accept_gumbel",
+           "tv_accept_rejection")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -78,6 +81,16 @@ def load():
                                      P, P, P, P, P, P]
         lib.tv_profile_start.argtypes = [I]
         lib.tv_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I), ctypes.POINTER(I)]
+        lib.tv_sample_workspace_size.argtypes = [ctypes.c_int32, I, ctypes.POINTER(Z)]
+        lib.tv_sample_filter.argtypes = [P, P, I, ctypes.c_int32, ctypes.c_float, ctypes.c_int32, ctypes.c_float,
+                                         ctypes.c_float, P, P]
+        lib.tv_accept_single_draw.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float, P, P,
+                                              P, P, P, P, P, Z, P]
+        lib.tv_accept_gumbel.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float,
+                                         ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_int32), P, P, P,
+                                         P, P, P, Z, P]
+        lib.tv_accept_rejection.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float, P, P,
+                                            P, P, P, P, P, P, Z, P]
         lib.tv_status_string.argtypes = [I]
         lib.tv_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -147,6 +160,46 @@ def tv_accept_residual_noalloc(trees: Sequence[TvTree], logits, vocab: int, temp
                                              float(temperature), _p(uniforms), 1 if bonus_at_leaf else 0,
                                              _p(path), _p(accept_len), _p(out_tokens), _p(out_count),
                                              _p(dev_status), _stream(stream))
+
+
+def tv_sample_workspace_size(vocab: int, max_rows: int):
+    """(rc, bytes) of workspace the sampled entry points need."""
+    z = ctypes.c_size_t(0)
+    rc = load().tv_sample_workspace_size(int(vocab), int(max_rows), ctypes.byref(z))
+    return rc, int(z.value)
+
+
+def tv_sample_filter(logits, filtered, rows: int, vocab: int, temperature: float, top_k: int, top_p: float,
+                     min_p: float, dev_status, stream=None) -> int:
+    return load().tv_sample_filter(_p(logits), _p(filtered), int(rows), int(vocab), float(temperature), int(top_k),
+                                   float(top_p), float(min_p), _p(dev_status), _stream(stream))
+
+
+def tv_accept_single_draw(trees: Sequence[TvTree], logits, vocab: int, temperature: float, uniforms, row_tokens,
+                          path, accept_len, out_tokens, dev_status, workspace, workspace_bytes: int,
+                          stream=None) -> int:
+    return load().tv_accept_single_draw(_arr(TvTree, trees), len(trees), _p(logits), int(vocab), float(temperature),
+                                        _p(uniforms), _p(row_tokens), _p(path), _p(accept_len), _p(out_tokens),
+                                        _p(dev_status), _p(workspace), int(workspace_bytes), _stream(stream))
+
+
+def tv_accept_gumbel(trees: Sequence[TvTree], logits, vocab: int, temperature: float, seeds: Sequence[int],
+                     positions: Sequence[int], row_tokens, path, accept_len, out_tokens, dev_status, workspace,
+                     workspace_bytes: int, stream=None) -> int:
+    sd = (ctypes.c_uint64 * len(trees))(*[int(x) & 0xFFFFFFFFFFFFFFFF for x in seeds])
+    ps = (ctypes.c_int32 * len(trees))(*[int(x) for x in positions])
+    return load().tv_accept_gumbel(_arr(TvTree, trees), len(trees), _p(logits), int(vocab), float(temperature), sd,
+                                   ps, _p(row_tokens), _p(path), _p(accept_len), _p(out_tokens), _p(dev_status),
+                                   _p(workspace), int(workspace_bytes), _stream(stream))
+
+
+def tv_accept_rejection(trees: Sequence[TvTree], logits, vocab: int, temperature: float, proposals, uniforms,
+                        path, accept_len, out_tokens, out_count, dev_status, workspace, workspace_bytes: int,
+                        stream=None) -> int:
+    return load().tv_accept_rejection(_arr(TvTree, trees), len(trees), _p(logits), int(vocab), float(temperature),
+                                      _p(proposals), _p(uniforms), _p(path), _p(accept_len), _p(out_tokens),
+                                      _p(out_count), _p(dev_status), _p(workspace), int(workspace_bytes),
+                                      _stream(stream))
 
 
 def tv_commit_kv(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], path, accept_len, committed_src,

@@ -241,6 +241,107 @@ int tv_accept_residual(const tv_tree* trees, int n_req, const float* logits, int
                                 dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---- sampled variants -------------------------------------------------------------
+namespace {
+struct SampleWs {   // byte offsets in the sampled entry points' workspace
+  size_t stats, gumbel, rej, total;
+};
+SampleWs sample_ws(int vocab, int rows) {
+  const size_t nvc = (size_t)n_vchunks(vocab);
+  SampleWs w;
+  w.stats = 0;
+  w.gumbel = align256(w.stats + rows * nvc * sizeof(RowStat));
+  w.rej = align256(w.gumbel + rows * nvc * sizeof(GumbelPart));
+  w.total = align256(w.rej + rows * nvc * sizeof(RejStat));
+  return w;
+}
+}  // namespace
+
+int tv_sample_workspace_size(int32_t vocab, int max_rows, size_t* bytes) {
+  if (!bytes || vocab < 2) return TV_E_ARG;
+  if (max_rows < 1 || max_rows > kMaxRows) return TV_E_ROWS;
+  *bytes = sample_ws(vocab, max_rows).total;
+  return TV_OK;
+}
+
+int tv_sample_filter(const float* logits, float* filtered, int rows, int32_t vocab, float temperature, int32_t top_k,
+                     float top_p, float min_p, int32_t* dev_status, void* stream) {
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return TV_E_TEMP;
+  if (!logits || !filtered || logits == filtered || !dev_status || vocab < 2 || rows < 1 || rows > kMaxRows)
+    return TV_E_ARG;
+  if (top_k < 0 || !(top_p > 0.f && top_p <= 1.f) || !(min_p >= 0.f && min_p < 1.f)) return TV_E_ARG;
+  return launch_filter(logits, filtered, rows, vocab, temperature, top_k, top_p, min_p, dev_status,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tv_accept_single_draw(const tv_tree* trees, int n_req, const float* logits, int32_t vocab, float temperature,
+                          const float* uniforms, int32_t* row_tokens, int32_t* path, int32_t* accept_len,
+                          int32_t* out_tokens, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return TV_E_TEMP;
+  if (!logits || !uniforms || !row_tokens || !path || !accept_len || !out_tokens || !dev_status || vocab < 2)
+    return TV_E_ARG;
+  ReqTable t;
+  int rc = build_table(t, trees, nullptr, n_req, true);
+  if (rc) return rc;
+  const SampleWs w = sample_ws(vocab, t.total_rows);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return TV_E_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  rc = launch_draw_rows(t, logits, vocab, temperature, uniforms, reinterpret_cast<RowStat*>(ws + w.stats), row_tokens,
+                        dev_status, st);
+  if (rc) return rc;
+  return launch_accept_greedy(t, row_tokens, path, accept_len, out_tokens, dev_status, st);
+}
+
+int tv_accept_gumbel(const tv_tree* trees, int n_req, const float* logits, int32_t vocab, float temperature,
+                     const uint64_t* seeds, const int32_t* positions, int32_t* row_tokens, int32_t* path,
+                     int32_t* accept_len, int32_t* out_tokens, int32_t* dev_status, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return TV_E_TEMP;
+  if (!logits || !seeds || !positions || !row_tokens || !path || !accept_len || !out_tokens || !dev_status ||
+      vocab < 2)
+    return TV_E_ARG;
+  ReqTable t;
+  int rc = build_table(t, trees, nullptr, n_req, true);
+  if (rc) return rc;
+  SeedTable sd;
+  memset(&sd, 0, sizeof(sd));
+  for (int r = 0; r < n_req; ++r) {
+    if (positions[r] < 0) return TV_E_ARG;
+    sd.seed[r] = seeds[r];
+    sd.pos[r] = positions[r];
+  }
+  const SampleWs w = sample_ws(vocab, t.total_rows);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return TV_E_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  rc = launch_gumbel_rows(t, logits, vocab, temperature, sd, reinterpret_cast<GumbelPart*>(ws + w.gumbel), row_tokens,
+                          dev_status, st);
+  if (rc) return rc;
+  return launch_accept_greedy(t, row_tokens, path, accept_len, out_tokens, dev_status, st);
+}
+
+int tv_accept_rejection(const tv_tree* trees, int n_req, const float* logits, int32_t vocab, float temperature,
+                        const float* proposals, const float* uniforms, int32_t* path, int32_t* accept_len,
+                        int32_t* out_tokens, int32_t* out_count, int32_t* dev_status, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!(std::isfinite(temperature) && temperature > 0.f)) return TV_E_TEMP;
+  if (!logits || !proposals || !uniforms || !path || !accept_len || !out_tokens || !out_count || !dev_status ||
+      vocab < 2)
+    return TV_E_ARG;
+  ReqTable t;
+  const int rc = build_table(t, trees, nullptr, n_req, true);
+  if (rc) return rc;
+  const SampleWs w = sample_ws(vocab, t.total_rows);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return TV_E_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return launch_accept_rejection(t, logits, vocab, temperature, proposals, uniforms,
+                                 reinterpret_cast<RowStat*>(ws + w.stats), reinterpret_cast<RejStat*>(ws + w.rej),
+                                 path, accept_len, out_tokens, out_count, dev_status,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 int tv_commit_kv(const tv_kv* kv, const tv_dims* dims, const tv_tree* trees, int n_req, const int32_t* path,
                  const int32_t* accept_len, int32_t* committed_src, int32_t* new_ctx, int32_t* dev_status,
                  void* stream) {
@@ -311,6 +412,8 @@ const char* tv_status_string(int code) {
     case TV_E_UNSUPPORTED: return "shape not supported by these kernels";
     case TV_E_TIMEOUT: return "a bounded device wait gave up";
     case TV_E_PATH: return "accept length or path entry out of range";
+    case TV_E_CHAIN: return "single-path sampling needs a chain";
+    case TV_E_PROPOSAL: return "proposal row not finite, negative, off unit mass or zero at its draft";
     default: return "unknown status";
   }
 }

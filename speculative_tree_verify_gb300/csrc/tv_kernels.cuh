@@ -40,6 +40,23 @@ struct RowStat {
 };
 inline int n_vchunks(int vocab) { return (vocab + kVChunk - 1) / kVChunk; }
 
+// ---- sampled walks ------------------------------------------------------------
+// per request: the Gumbel seed and the sequence index of the root's token
+struct SeedTable {
+  unsigned long long seed[kMaxReq];
+  int pos[kMaxReq];
+};
+struct GumbelPart {   // a vocabulary chunk's best x + G and its index
+  float s;
+  int idx;
+};
+struct RejStat {      // a vocabulary chunk of a draft's proposal row
+  double resid;       // sum of max(p - q, 0), p the target row of the draft's parent
+  double qsum;        // sum of q
+  int bad;            // a q entry not finite or negative
+  int pad;
+};
+
 // ---- block-uniform status check -------------------------------------------
 __device__ __forceinline__ bool block_skip(const int32_t* status) {
   __shared__ int s_stat;
@@ -113,5 +130,16 @@ int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, fl
                            cudaStream_t st);
 int launch_commit(const ReqTable& t, const tv_dims& d, const int32_t* path, const int32_t* accept_len,
                   int32_t* committed_src, int32_t* new_ctx, int32_t* status, cudaStream_t st);
+
+int launch_filter(const float* logits, float* out, int rows, int vocab, float temperature, int top_k, float top_p,
+                  float min_p, int32_t* status, cudaStream_t st);
+int launch_gumbel_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const SeedTable& sd,
+                       GumbelPart* part, int32_t* row_tokens, int32_t* status, cudaStream_t st);
+int launch_draw_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const float* uniforms,
+                     RowStat* stats, int32_t* row_tokens, int32_t* status, cudaStream_t st);
+int launch_accept_rejection(const ReqTable& t, const float* logits, int vocab, float temperature,
+                            const float* proposals, const float* uniforms, RowStat* stats, RejStat* rstats,
+                            int32_t* path, int32_t* accept_len, int32_t* out_tokens, int32_t* out_count,
+                            int32_t* status, cudaStream_t st);
 
 }  // namespace tv

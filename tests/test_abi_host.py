@@ -119,6 +119,37 @@ def test_walk_and_commit_host_checks(lib):
     assert abi.tv_commit_kv([_kv(64, 96)], dims, [_tree(33)], FAKE, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ROWS"]
 
 
+def test_sampled_host_checks(lib):
+    rc, wsb = abi.tv_sample_workspace_size(151936, 32)
+    assert rc == abi.TV_OK and wsb > 0 and wsb % 256 == 0
+    assert abi.tv_sample_workspace_size(151936, 33)[0] == abi.CODES["TV_E_ROWS"]
+    assert abi.tv_sample_workspace_size(1, 8)[0] == abi.CODES["TV_E_ARG"]
+    # filters: temperature, then the filter parameters, then in-place use
+    for t in (0.0, -1.0, float("nan"), float("inf")):
+        assert abi.tv_sample_filter(FAKE, FAKE + 256, 2, 16, t, 0, 1.0, 0.0, FAKE) == abi.CODES["TV_E_TEMP"]
+    for k, p, mp in ((-1, 1.0, 0.0), (0, 0.0, 0.0), (0, 1.5, 0.0), (0, float("nan"), 0.0), (0, 1.0, 1.0),
+                     (0, 1.0, -0.1)):
+        assert abi.tv_sample_filter(FAKE, FAKE + 256, 2, 16, 1.0, k, p, mp, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_sample_filter(FAKE, FAKE, 2, 16, 1.0, 0, 1.0, 0.0, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_sample_filter(FAKE, FAKE + 256, 33, 16, 1.0, 0, 1.0, 0.0, FAKE) == abi.CODES["TV_E_ARG"]
+    # the walks: temperature, row count, workspace size, positions
+    trees = [_tree(8)]
+    _, ws8 = abi.tv_sample_workspace_size(1024, 8)
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert abi.tv_accept_single_draw(trees, FAKE, 1024, 0.0, FAKE, *args, FAKE, ws8) == abi.CODES["TV_E_TEMP"]
+    assert abi.tv_accept_single_draw([_tree(33)], FAKE, 1024, 1.0, FAKE, *args, FAKE, ws8) == abi.CODES["TV_E_ROWS"]
+    assert abi.tv_accept_single_draw(trees, FAKE, 1024, 1.0, FAKE, *args, FAKE, ws8 - 256) == \
+        abi.CODES["TV_E_WORKSPACE"]
+    assert abi.tv_accept_gumbel(trees, FAKE, 1024, 1.0, [1], [-1], *args, FAKE, ws8) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_accept_gumbel(trees, FAKE, 1024, float("nan"), [1], [0], *args, FAKE, ws8) == \
+        abi.CODES["TV_E_TEMP"]
+    assert abi.tv_accept_gumbel(trees, FAKE, 1024, 1.0, [1], [0], *args, None, ws8) == abi.CODES["TV_E_WORKSPACE"]
+    assert abi.tv_accept_rejection(trees, FAKE, 1024, 1.0, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   ws8) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_accept_rejection(trees, FAKE, 1024, 1.0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   16) == abi.CODES["TV_E_WORKSPACE"]
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(abi, "_lib", None)
     monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "missing.so"))
