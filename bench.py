@@ -10,7 +10,8 @@ timing) so the walk and the commit do real work.  Inputs are synthetic.
 
 Printed: one JSON line (rank 0).  value = ms per round from CUDA-graph replay
 (the served configuration keeps verify in graphs); the eager number, the row
-sweep 8/16/24/32, a sampled round (residual walk), per-stage times, the
+sweep 8/16/24/32, a sampled round (residual walk), the sampled variants (filter,
+single-draw, Gumbel and rejection walks alone and in rounds), per-stage times, the
 roofline of the LM head kernel, end-to-end latency with host buffers, clocks
 and the CPU oracle baseline ride along.
 
@@ -427,6 +428,59 @@ def run_ours(args, world, rank, local):
     gs = _graph(sround)
     out["sampled_round_ms"] = round(_time_graph(gs, max(200, args.steps // 4)), 4)
     del gs
+
+    # ---- sampled variants: each walk alone on the round's logits (L2-resident,
+    #      as they are right after the LM head), then whole rounds with them ----------
+    def ok_status(what):
+        torch.cuda.synchronize()
+        st = int(b.status.item())
+        if st != 0:
+            raise RuntimeError(f"{what}: device status {abi.STATUS.get(st, st)}")
+
+    sb = dv.SampleBuffers.alloc(D.vocab, rows, device=dev)
+    seeds, positions = [0x5EED5EED5EED], [ctx]
+    filt = dict(temperature=0.8, top_k=50, top_p=0.9, min_p=0.02)
+    cur = torch.cuda.current_stream
+    sv = {"rows": rows, "vocab": D.vocab, "filter_params": filt}
+    walks = {
+        "filter": lambda: dv.check(dv.sample_filter(b, sb, rows, stream=cur(), **filt), "filter"),
+        "single_draw": lambda: dv.check(dv.accept_single_draw([req], b, sb, 1.0, stream=cur()), "single_draw"),
+        "gumbel": lambda: dv.check(dv.accept_gumbel([req], b, sb, 1.0, seeds, positions, stream=cur()), "gumbel"),
+    }
+    # single-path rejection: a chain of `rows` drafts, each drawn as its proposal row's mode
+    gq = torch.Generator(device=dev)
+    gq.manual_seed(17)
+    prop = torch.softmax(2.0 * torch.randn(rows, D.vocab, device=dev, generator=gq), dim=1)
+    ch_tok = torch.argmax(prop, dim=1).to(torch.int32)
+    ch_tok[0] = 0
+    chain = dv.DeviceRequest(req.k, req.v, ctx, torch.arange(-1, rows - 1, device=dev, dtype=torch.int32), ch_tok)
+    walks["rejection"] = lambda: dv.check(dv.accept_rejection([chain], b, sb, 1.0, prop, stream=cur()), "rejection")
+    for name, fn in walks.items():
+        gw = _graph(fn)
+        sv[name + "_us"] = round(1e3 * _time_graph(gw, 500), 2)
+        del gw
+        ok_status(name)
+    lg = rows * D.vocab * 4
+    sv["filter_GB_per_s"] = round(2 * lg / sv["filter_us"] / 1e3, 1)
+
+    def gumbel_round():
+        dv.check(dv.verify(dm, [req], b, stream=cur()), "verify")
+        dv.check(dv.accept_gumbel([req], b, sb, 1.0, seeds, positions, stream=cur()), "gumbel")
+        dv.check(dv.commit([req], b, stream=cur()), "commit")
+
+    def filtered_round():
+        dv.check(dv.verify(dm, [req], b, stream=cur()), "verify")
+        dv.check(dv.sample_filter(b, sb, rows, stream=cur(), **filt), "filter")
+        dv.check(dv.accept_single_draw([req], b, sb, 1.0, filtered=True, stream=cur()), "single_draw")
+        dv.check(dv.commit([req], b, stream=cur()), "commit")
+
+    for name, fn in (("gumbel_round_ms", gumbel_round), ("filtered_single_draw_round_ms", filtered_round)):
+        gw = _graph(fn)
+        sv[name] = round(_time_graph(gw, max(200, args.steps // 4)), 4)
+        del gw
+        ok_status(name)
+    out["sampled_variants"] = sv
+    del sb, prop, chain
 
     # ---- end to end through the C ABI with host buffers --------------------------
     par_h = torch.from_numpy(req.parent.cpu().numpy()).pin_memory()

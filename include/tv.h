@@ -205,7 +205,7 @@ TV_API int tv_accept_residual(const tv_tree *trees, int n_req, const float *logi
  * another framework's executor that may not call cudaMalloc, a real-time loop
  * with a no-allocation rule, a caller holding only a stream and the round's
  * buffers.  Same walk, same kernels and same results as tv_accept_residual; the
- * per-row softmax statistics live instead in a 16 KB array inside the
+ * per-row softmax statistics live instead in a 272 KB array inside the
  * library's device image (one per GPU, held until the process exits), so:
  *   - vocab may be at most 262144 (TV_E_UNSUPPORTED above that);
  *   - the first call on a device looks up that array's address
@@ -261,13 +261,17 @@ TV_API int tv_sample_workspace_size(int32_t vocab, int max_rows, size_t *bytes);
  *   top_p (1 = off)  keep the fewest largest-probability tokens whose mass
  *                    reaches top_p (ties at the boundary all kept);
  *   min_p (0 = off)  keep the tokens with p >= min_p * max p.
- * The k-th largest logit and the top-p boundary are found exactly (radix
- * selection on the logits' bits), so the result does not depend on the run.
+ * The k-th largest logit and the top-p boundary are found exactly (integer
+ * histograms over the logits' bits; probability masses in units of 2^-40),
+ * so the result does not depend on the run.  Each row is handled by a
+ * cluster of 8 CTAs holding the row in shared memory, hence the vocabulary
+ * limit.
  *
  *   logits    device fp32 [rows][vocab];  filtered  device fp32 [rows][vocab]
  *             (may not alias logits)
  * Host checks: TV_E_ARG (null pointers, rows outside 1..32, vocab < 2,
- * top_k < 0, top_p outside (0, 1], min_p outside [0, 1)), TV_E_TEMP.
+ * top_k < 0, top_p outside (0, 1], min_p outside [0, 1)), TV_E_TEMP,
+ * TV_E_UNSUPPORTED (vocab > 262144).
  */
 TV_API int tv_sample_filter(const float *logits, float *filtered, int rows, int32_t vocab, float temperature,
                             int32_t top_k, float top_p, float min_p, int32_t *dev_status, void *stream);

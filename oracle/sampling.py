@@ -156,12 +156,17 @@ def philox4x32_10(ctr, key):
 
 
 def gumbel_uniform(seed: int, t: int, idx) -> np.ndarray:
-    """U in (0, 1) for token ``idx`` at sequence index ``t``: the first word of
-    Philox4x32-10 at counter (idx, t, 0, 0) under key (seed low, seed high),
-    as (w + 0.5) / 2^32."""
+    """U in (0, 1) for token ``idx`` at sequence index ``t``: word ``idx mod 4``
+    of Philox4x32-10 at counter (idx div 4, t, 0, 0) under key (seed low,
+    seed high), as (w + 0.5) / 2^32.  One generator block serves four
+    consecutive tokens (the pages fix only that the noise is keyed by
+    (seed, t); the layout of the generator's output is this reading)."""
     idx = np.asarray(idx, np.uint64)
-    w, _, _, _ = philox4x32_10((idx, np.full_like(idx, int(t) & _MASK), np.zeros_like(idx), np.zeros_like(idx)),
-                               (int(seed) & _MASK, (int(seed) >> 32) & _MASK))
+    blk = idx >> np.uint64(2)
+    words = philox4x32_10((blk, np.full_like(blk, int(t) & _MASK), np.zeros_like(blk), np.zeros_like(blk)),
+                          (int(seed) & _MASK, (int(seed) >> 32) & _MASK))
+    sel = (idx & np.uint64(3)).astype(np.int64)
+    w = np.choose(sel, words)
     return (w.astype(np.float64) + 0.5) / 4294967296.0
 
 

@@ -155,7 +155,7 @@ def tv_accept_residual_noalloc(trees: Sequence[TvTree], logits, vocab: int, temp
                                bonus_at_leaf: bool, path, accept_len, out_tokens, out_count, dev_status,
                                stream=None) -> int:
     """tv_accept_residual for callers that cannot provide a workspace (the
-    statistics live in a fixed 16 KB array inside the library; vocab <= 262144)."""
+    statistics live in a fixed 272 KB array inside the library; vocab <= 262144)."""
     return load().tv_accept_residual_noalloc(_arr(TvTree, trees), len(trees), _p(logits), int(vocab),
                                              float(temperature), _p(uniforms), 1 if bonus_at_leaf else 0,
                                              _p(path), _p(accept_len), _p(out_tokens), _p(out_count),

@@ -32,11 +32,17 @@ __host__ __device__ inline AttnPlan attn_plan(int ctx, int target) {
 }
 inline int attn_chunk_target(int sms, int n_kv_heads) { return n_kv_heads > 0 ? sms / n_kv_heads : 1; }
 
-// ---- residual walk: per-row statistics over vocabulary chunks --------------
+// ---- sampled walks: per-row statistics over vocabulary chunks ---------------
+// A draw from a row searches its CDF in three steps, each one warp-wide:
+// the row's chunks of 4096 tokens, the chunk's 32 segments of 128 tokens, the
+// segment's 128 tokens (4 per lane).
 constexpr int kVChunk = 4096;
+constexpr int kVSeg = 128;
+constexpr int kSegsPerChunk = kVChunk / kVSeg;   // 32: one per lane
 struct RowStat {
-  float m;   // max logit of the chunk
-  float s;   // sum over the chunk of exp((logit - m) / T)
+  float m;                    // max logit of the chunk
+  float s;                    // sum of seg[]
+  float seg[kSegsPerChunk];   // per segment: sum of exp((logit - m) / T)
 };
 inline int n_vchunks(int vocab) { return (vocab + kVChunk - 1) / kVChunk; }
 
@@ -50,10 +56,11 @@ struct GumbelPart {   // a vocabulary chunk's best x + G and its index
   float s;
   int idx;
 };
-struct RejStat {      // a vocabulary chunk of a draft's proposal row
-  double resid;       // sum of max(p - q, 0), p the target row of the draft's parent
-  double qsum;        // sum of q
-  int bad;            // a q entry not finite or negative
+struct RejStat {               // a vocabulary chunk of a draft's proposal row
+  float seg[kSegsPerChunk];   // per segment: sum of max(p - q, 0), p the target row of the draft's parent
+  float resid;                // sum of seg[]
+  float qsum;                 // sum of q
+  int bad;                    // a q entry not finite or negative
   int pad;
 };
 

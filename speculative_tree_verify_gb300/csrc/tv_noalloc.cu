@@ -12,7 +12,7 @@
 // device image instead.
 //
 // The array is a file-scope __device__ global: every GPU that loads the
-// library holds one copy (16 KB) until the process exits.  Its size fixes the
+// library holds one copy (272 KB) until the process exits.  Its size fixes the
 // largest vocabulary this entry point accepts (kNoAllocMaxVocab); larger
 // vocabularies are rejected with TV_E_UNSUPPORTED.  Nothing in it needs to
 // start at zero: every statistic the walk reads is written earlier in the same
@@ -36,6 +36,7 @@ constexpr int kNoAllocMaxVocab = 262144;
 constexpr int kNoAllocStats = kMaxRows * ((kNoAllocMaxVocab + kVChunk - 1) / kVChunk);
 
 static __device__ __align__(256) RowStat g_residual_stats[kNoAllocStats];
+static_assert(sizeof(g_residual_stats) == 272 * 1024, "the size the header documents");
 
 namespace {
 

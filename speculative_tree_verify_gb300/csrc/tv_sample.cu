@@ -1,15 +1,21 @@
 // Sampling filters and seeded Gumbel-max draws.
 //
-//  - filter: temperature, top_k, top_p and min_p through one function, one CTA
-//    per row [Exactness, §Sampling, second paragraph].  The k-th largest
-//    logit and the top-p boundary are found by radix selection on an
-//    order-preserving integer key of the logit (four 8-bit passes each), with
-//    integer histograms, so the result is exact and the same on every run.
+//  - filter: temperature, top_k, top_p and min_p through one function
+//    [Exactness, §Sampling, second paragraph].  One thread-block cluster of
+//    8 CTAs per row; each CTA keeps a slice of the row in shared memory and
+//    the cluster sums its histograms through distributed shared memory.  The
+//    k-th largest logit and the top-p boundary are found in two levels: a
+//    256-bin histogram of (l_max - l) / T, which places the boundary in one
+//    bin, then radix selection (four 8-bit passes) on an order-preserving
+//    integer key of the logits in that bin.  Histograms hold integer weights
+//    (counts, or probability masses in units of 2^-40), so the result is exact
+//    and the same on every run.
 //  - Gumbel: the token at sequence index t is argmax_i (x_i + G_i), G_i Gumbel
 //    noise from Philox4x32-10 keyed by (seed, t) [Exactness, §Sampling, third
-//    paragraph]; one pass of (vocab chunk, row) blocks and a per-row pick.
-//    Philox4x32-10 follows Salmon, Moraes, Dror and Shaw, "Parallel random
-//    numbers: as easy as 1, 2, 3" (SC 2011).
+//    paragraph]; token i takes word i mod 4 of the generator block at counter
+//    (i div 4, t, 0, 0).  One pass of (vocab chunk, row) blocks and a per-row
+//    pick.  Philox4x32-10 follows Salmon, Moraes, Dror and Shaw, "Parallel
+//    random numbers: as easy as 1, 2, 3" (SC 2011).
 #include <climits>
 #include <cmath>
 
@@ -21,7 +27,46 @@ namespace tv {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int kFilterThreads = 1024;
+
+// ---- thread-block cluster helpers ------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes before
+// it against reads after it, in this CTA and the others
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ double ld_dsmem_f64(uint32_t a) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// ---- filter --------------------------------------------------------------------------
+constexpr int kFCluster = 8;            // CTAs per row
+constexpr int kFThreads = 512;
+constexpr int kFWarps = kFThreads / 32;
+constexpr int kFBins = 256;
+constexpr float kFBinsPerUnit = 8.f;    // level-1 bin width: 1/8 of a unit of (l_max - l) / T
+constexpr int kFilterMaxVocab = 262144;
 
 // order-preserving key: larger float -> larger unsigned (NaN sorts lowest)
 __device__ __forceinline__ uint32_t fkey(float x) {
@@ -30,128 +75,208 @@ __device__ __forceinline__ uint32_t fkey(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The radix selection shared by top_k (weights 1) and top_p (weights = the
-// quantised probability): over the tokens with key >= floor_key, the largest
-// key K such that the total weight of tokens with key >= K reaches `need`.
-// Returns floor_key when the whole weight falls short of need.
+struct FilterShared {
+  unsigned long long hist[2][kFBins];   // this CTA's histogram (two, used in turn); the cluster reads them
+  unsigned long long tot[kFBins];       // the cluster's histogram
+  unsigned long long res[2];            // selected bin and the weight before it
+  double pub_z;                         // this CTA's part of Z (read by the cluster)
+  double redd[kFWarps];
+  double Z;
+  float pub_max;                        // this CTA's slice maximum (read by the cluster)
+  float redf[kFWarps];
+  float M;
+  int cnt;
+};
+
+// The cluster's histogram tot[] from every CTA's hist[hb] (after a cluster barrier).
+__device__ __forceinline__ void cluster_hist(FilterShared& sh, int hb) {
+  if (threadIdx.x < kFBins) {
+    unsigned long long s = 0ull;
+#pragma unroll
+    for (int r = 0; r < kFCluster; ++r) s += ld_dsmem_u64(dsmem_addr(&sh.hist[hb][threadIdx.x], r));
+    sh.tot[threadIdx.x] = s;
+  }
+  __syncthreads();
+}
+
+// One warp: the first bin, counted from bin 0 upward (descending = false) or
+// from bin 255 downward, at which the running weight reaches need; res[0] = the
+// bin (~0 when the total falls short), res[1] = the weight before it.
+__device__ __forceinline__ void find_bin(FilterShared& sh, unsigned long long need, bool descending) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  unsigned long long above = 0ull, before = 0ull;
+  int found = -1;
+  for (int b0 = 0; b0 < kFBins && found < 0; b0 += 32) {
+    const int b = descending ? kFBins - 1 - (b0 + lane) : b0 + lane;
+    const unsigned long long h = sh.tot[b];
+    unsigned long long incl = h;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const unsigned hit = __ballot_sync(FULL, above + incl >= need);
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      found = descending ? kFBins - 1 - (b0 + L) : b0 + L;
+      before = above + __shfl_sync(FULL, incl - h, L);
+    }
+    above += __shfl_sync(FULL, incl, 31);
+  }
+  if (lane == 0) {
+    sh.res[0] = found < 0 ? ~0ull : (unsigned long long)found;
+    sh.res[1] = before;
+  }
+}
+
+// Over the tokens with key >= floor: the largest key K such that the weight of
+// the tokens with key >= K reaches need (floor when the total falls short).
+// Level 1 places K in one bin of (M - l) / T, which falls as l rises, so every
+// token of a lower bin has a larger key than every token of that bin; level 2
+// selects K among the keys of that bin, 8 bits at a time from the top.
 template <typename Weight>
-__device__ uint32_t radix_select(const float* lr, int V, uint32_t floor_key, unsigned long long need, Weight w,
-                                 unsigned long long* hist, unsigned long long* s_scalar) {
+__device__ uint32_t select_key(FilterShared& sh, const float* xs, uint16_t* cand, int n_loc, float M, float inv_t,
+                               uint32_t floor_key, unsigned long long need, Weight wt, int& hb) {
+  auto bin_of = [&](float x) { return (int)fminf((M - x) * inv_t * kFBinsPerUnit, (float)(kFBins - 1)); };
+  for (int b = threadIdx.x; b < kFBins; b += kFThreads) sh.hist[hb][b] = 0ull;
+  if (threadIdx.x == 0) sh.cnt = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
+    const float x = xs[i];
+    if (fkey(x) >= floor_key) atomicAdd(&sh.hist[hb][bin_of(x)], wt(x));
+  }
+  cluster_sync_all();
+  cluster_hist(sh, hb);
+  hb ^= 1;
+  find_bin(sh, need, false);
+  __syncthreads();
+  const unsigned long long B = sh.res[0];
+  if (B == ~0ull) return floor_key;   // the weight falls short: no cut
+  need -= sh.res[1];
+  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
+    const float x = xs[i];
+    if (fkey(x) >= floor_key && bin_of(x) == (int)B) cand[atomicAdd(&sh.cnt, 1)] = (uint16_t)i;
+  }
+  __syncthreads();
+  const int nc = sh.cnt;
   uint32_t prefix = 0u, mask = 0u;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0ull;
+    for (int b = threadIdx.x; b < kFBins; b += kFThreads) sh.hist[hb][b] = 0ull;
     __syncthreads();
-    for (int y = threadIdx.x; y < V; y += blockDim.x) {
-      const uint32_t k = fkey(lr[y]);
-      if (k >= floor_key && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], w(y, lr[y]));
+    for (int j = threadIdx.x; j < nc; j += kFThreads) {
+      const float x = xs[cand[j]];
+      const uint32_t k = fkey(x);
+      if ((k & mask) == prefix) atomicAdd(&sh.hist[hb][(k >> shift) & 255u], wt(x));
     }
+    cluster_sync_all();
+    cluster_hist(sh, hb);
+    hb ^= 1;
+    find_bin(sh, need, true);
     __syncthreads();
-    if (threadIdx.x < 32) {   // one warp: the bin where the weight from the top reaches need
-      const int lane = threadIdx.x;
-      unsigned long long above = 0ull;
-      int found = -1;
-      unsigned long long above_found = 0ull;
-      for (int b0 = 255; b0 >= 0 && found < 0; b0 -= 32) {
-        const int b = b0 - lane;
-        const unsigned long long h = b >= 0 ? hist[b] : 0ull;
-        unsigned long long incl = h;   // inclusive scan from the top (lane 0 = highest bin)
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long u = __shfl_up_sync(FULL, incl, o);
-          if (lane >= o) incl += u;
-        }
-        const unsigned hit = __ballot_sync(FULL, b >= 0 && above + incl >= need);
-        if (hit) {
-          const int L = __ffs(hit) - 1;
-          found = b0 - L;
-          above_found = above + __shfl_sync(FULL, incl - h, L);
-        }
-        above += __shfl_sync(FULL, incl, 31);
-      }
-      if (lane == 0) {
-        s_scalar[0] = found < 0 ? ~0ull : (unsigned long long)found;
-        s_scalar[1] = above_found;
-      }
-    }
-    __syncthreads();
-    const unsigned long long f = s_scalar[0];
-    const unsigned long long ab = s_scalar[1];
-    __syncthreads();
-    if (f == ~0ull) return floor_key;   // the weight falls short: keep every token
+    const unsigned long long f = sh.res[0];
+    if (f == ~0ull) return floor_key;   // not reached: the bin holds at least need
     prefix |= (uint32_t)f << shift;
     mask |= 255u << shift;
-    need -= ab;
+    need -= sh.res[1];
   }
   return prefix;
 }
 
-__device__ float block_max(float v, float* red) {
+__device__ __forceinline__ float block_max(float v, float* red) {
   v = warp_max(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) red[w] = v;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
   float m = red[0];
-  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
-  __syncthreads();
+  for (int i = 1; i < kFWarps; ++i) m = fmaxf(m, red[i]);
   return m;
 }
 
-__device__ double block_sum_d(double v, double* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) red[w] = v;
+__device__ __forceinline__ double block_sum_d(float v, double* red) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = (double)v;
   __syncthreads();
   double s = 0.0;
-  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];   // fixed order
-  __syncthreads();
+  for (int i = 0; i < kFWarps; ++i) s += red[i];   // fixed order
   return s;
 }
 
-// One row per CTA.  out = x = logit / T where kept, -inf elsewhere; selection
-// on the raw logits (the scale by 1/T keeps their order).
-__global__ void __launch_bounds__(kFilterThreads) filter_kernel(const float* logits, float* out, int V, float inv_t,
-                                                                int top_k, double top_p, float log_min_p,
-                                                                const int32_t* status) {
-  __shared__ unsigned long long hist[256];
-  __shared__ unsigned long long s_scalar[2];
-  __shared__ float redf[kFilterThreads / 32];
-  __shared__ double redd[kFilterThreads / 32];
+// One cluster per row; CTA `rank` holds tokens [rank * slice, rank * slice + slice).
+// out = x = logit / T where kept, -inf elsewhere; selection on the raw logits
+// (the scale by 1/T keeps their order).
+__global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
+    filter_kernel(const float* logits, float* out, int V, int slice, float inv_t, int top_k,
+                  unsigned long long need_p, float log_min_p, const int32_t* status) {
+  __shared__ FilterShared sh;
+  extern __shared__ __align__(16) unsigned char dyn[];
+  float* xs = reinterpret_cast<float*>(dyn);
+  uint16_t* cand = reinterpret_cast<uint16_t*>(dyn + (size_t)slice * sizeof(float));
   pdl_wait();
   pdl_trigger();
-  if (block_skip(status)) return;
-  const float* lr = logits + (size_t)blockIdx.x * V;
-  float* orow = out + (size_t)blockIdx.x * V;
-  float lmax = -INFINITY;
-  for (int y = threadIdx.x; y < V; y += blockDim.x) lmax = fmaxf(lmax, lr[y]);
-  lmax = block_max(lmax, redf);
+  if (block_skip(status)) return;   // the same status for every CTA of the cluster
+  const uint32_t rank = cluster_ctarank();
+  const int row = blockIdx.y;
+  const int lo = (int)rank * slice;
+  const int n_loc = max(0, min(V - lo, slice));
+  const float* lr = logits + (size_t)row * V + lo;
+  float* orow = out + (size_t)row * V + lo;
+
+  float mx = -INFINITY;
+  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
+    const float v = lr[i];
+    xs[i] = v;
+    mx = fmaxf(mx, v);
+  }
+  mx = block_max(mx, sh.redf);
+  if (threadIdx.x == 0) sh.pub_max = mx;
+  cluster_sync_all();
+  if (threadIdx.x < 32) {
+    float m = threadIdx.x < kFCluster ? ld_dsmem_f32(dsmem_addr(&sh.pub_max, threadIdx.x)) : -INFINITY;
+    m = warp_max(m);
+    if (threadIdx.x == 0) sh.M = m;
+  }
+  __syncthreads();
+  const float M = sh.M;
+  int hb = 0;
   uint32_t kfloor = 1u;   // above every NaN key
-  if (top_k > 0 && top_k < V)
-    kfloor = radix_select(lr, V, kfloor, (unsigned long long)top_k, [](int, float) { return 1ull; }, hist,
-                          s_scalar);
-  if (top_p < 1.0) {
-    // probabilities over the tokens kept so far, quantised to 2^-40 steps
-    double z = 0.0;
-    for (int y = threadIdx.x; y < V; y += blockDim.x)
-      if (fkey(lr[y]) >= kfloor) z += (double)expf((lr[y] - lmax) * inv_t);
-    z = block_sum_d(z, redd);
-    const double scale = 1099511627776.0 / z;   // 2^40 / Z
-    auto qmass = [&](int, float l) { return (unsigned long long)((double)expf((l - lmax) * inv_t) * scale + 0.5); };
-    unsigned long long need = (unsigned long long)(top_p * 1099511627776.0);
-    if (need == 0ull) need = 1ull;   // the largest token always stays
-    kfloor = radix_select(lr, V, kfloor, need, qmass, hist, s_scalar);
+  if (M != -INFINITY) {
+    if (top_k > 0 && top_k < V)
+      kfloor = select_key(sh, xs, cand, n_loc, M, inv_t, kfloor, (unsigned long long)top_k,
+                          [](float) { return 1ull; }, hb);
+    if (need_p != 0ull) {
+      // probabilities over the tokens kept so far, as integers in units of 2^-40
+      float z = 0.f;
+      for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
+        const float x = xs[i];
+        if (fkey(x) >= kfloor) z += expf((x - M) * inv_t);
+      }
+      const double zc = block_sum_d(z, sh.redd);
+      if (threadIdx.x == 0) sh.pub_z = zc;
+      cluster_sync_all();
+      if (threadIdx.x == 0) {
+        double Z = 0.0;
+        for (int r = 0; r < kFCluster; ++r) Z += ld_dsmem_f64(dsmem_addr(&sh.pub_z, r));
+        sh.Z = Z;
+      }
+      __syncthreads();
+      const float scale = (float)(1099511627776.0 / sh.Z);   // 2^40 / Z
+      kfloor = select_key(
+          sh, xs, cand, n_loc, M, inv_t, kfloor, need_p,
+          [=](float x) { return (unsigned long long)__float2ull_rn(__fmul_rn(expf((x - M) * inv_t), scale)); }, hb);
+    }
   }
   // min_p: x >= x_max + log(min_p), i.e. (l - l_max) / T >= log(min_p)
-  for (int y = threadIdx.x; y < V; y += blockDim.x) {
-    const float l = lr[y];
-    const bool keep = fkey(l) >= kfloor && (l - lmax) * inv_t >= log_min_p;
-    orow[y] = keep ? l * inv_t : -INFINITY;
+  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
+    const float l = xs[i];
+    const bool keep = M != -INFINITY && fkey(l) >= kfloor && (l - M) * inv_t >= log_min_p;
+    orow[i] = keep ? l * inv_t : -INFINITY;
   }
+  cluster_sync_all();   // no CTA leaves while the cluster may still read its shared memory
 }
 
 // ---- Philox4x32-10 -------------------------------------------------------------
-__device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
-                                              uint32_t k1) {
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
     if (r > 0) {
@@ -166,65 +291,88 @@ __device__ __forceinline__ uint32_t philox_w0(uint32_t c0, uint32_t c1, uint32_t
     c2 = n2;
     c3 = lo0;
   }
-  return c0;
+  return make_uint4(c0, c1, c2, c3);
 }
 
-// G = -log(-log U), U = (w + 0.5) / 2^32, with -log U formed from whichever of
-// U and 1 - U is small, so that it keeps its precision in fp32 at both ends
+// G = -log(E), E = -log U, U = (w + 0.5) / 2^32.  Near U = 1, E is formed
+// from v = 1 - U = (2^32 - 1 - w + 0.5) / 2^32 by the series
+// -log(1 - v) = v + v^2/2 + v^3/3 + ... (to v^5; the rest is below 2^-25 of
+// E for v < 2^-5), so E keeps its relative precision at both ends.
 __device__ __forceinline__ float gumbel_from_word(uint32_t w) {
-  float e;
-  if (w < 0x80000000u) {
-    e = -logf(((float)w + 0.5f) * 2.3283064365386963e-10f);
-  } else {
-    const float um = ((float)(0xFFFFFFFFu - w) + 0.5f) * 2.3283064365386963e-10f;   // 1 - U
-    e = -log1pf(-um);
-  }
-  return -logf(e);
+  const float u = ((float)w + 0.5f) * 2.3283064365386963e-10f;
+  const float v = ((float)(~w) + 0.5f) * 2.3283064365386963e-10f;
+  const float e_series = v * (1.f + v * (0.5f + v * (0.33333334f + v * (0.25f + v * 0.2f))));
+  const float e = v < 0.03125f ? e_series : -__logf(u);
+  return -__logf(e);
 }
 
 // per (vocab chunk, row): the largest x_i + G_i and its index (lowest on ties)
 __global__ void __launch_bounds__(256) gumbel_partial_kernel(ReqTable t, const float* logits, int V, float inv_t,
-                                                             SeedTable sd, int nvc, GumbelPart* part,
+                                                             SeedTable sd, int nvc, int vec4, GumbelPart* part,
                                                              const int32_t* status) {
   __shared__ float sv[8];
   __shared__ int si[8];
+  __shared__ int s_par[32];
   __shared__ uint32_t s_pos;
+  __shared__ int s_req;
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
   const int c = blockIdx.x, row = blockIdx.y;
-  if (threadIdx.x == 0) {   // request of the row, and the sequence index of the token the row scores
+  if (threadIdx.x < 32) {   // request of the row, and the sequence index of the token the row scores
+    const int lane = threadIdx.x;
     int r = 0;
     while (r + 1 < t.n_req && t.row_off[r + 1] <= row) ++r;
-    // depth of the row's node (parents read as given; a malformed tree, which the
-    // walk rejects, only stops the climb early)
-    int i = row - t.row_off[r], d = 0;
-    while (i > 0 && d < kMaxRows) {
-      const int p = t.parent[r][i];
-      if (p < 0 || p >= i) break;
-      i = p;
-      ++d;
+    const int n = t.n[r];
+    s_par[lane] = lane < n ? t.parent[r][lane] : -1;
+    __syncwarp();
+    if (lane == 0) {
+      // depth of the row's node (a malformed tree, which the walk rejects, only
+      // stops the climb early)
+      int i = row - t.row_off[r], d = 0;
+      while (i > 0 && d < kMaxRows) {
+        const int p = s_par[i];
+        if (p < 0 || p >= i) break;
+        i = p;
+        ++d;
+      }
+      s_pos = (uint32_t)(sd.pos[r] + d + 1);
+      s_req = r;
     }
-    s_pos = (uint32_t)(sd.pos[r] + d + 1);
-    si[0] = r;
   }
   __syncthreads();
-  const int r = si[0];
+  const int r = s_req;
   const uint32_t tpos = s_pos;
   const uint32_t k0 = (uint32_t)(sd.seed[r] & 0xFFFFFFFFull), k1 = (uint32_t)(sd.seed[r] >> 32);
-  __syncthreads();
   const float* lr = logits + (size_t)row * V;
   float best = -INFINITY;
   int bi = INT_MAX;
-  for (int k = 0; k < kVChunk / 256; ++k) {
-    const int y = c * kVChunk + k * 256 + threadIdx.x;
-    if (y < V) {
-      const float x = lr[y] * inv_t;
+#pragma unroll
+  for (int k = 0; k < kVChunk / 1024; ++k) {
+    const int g = c * (kVChunk / 4) + k * 256 + threadIdx.x;   // generator block: tokens 4g .. 4g + 3
+    const int y0 = 4 * g;
+    if (y0 >= V) continue;
+    float l[4];
+    if (vec4) {
+      const float4 q = *reinterpret_cast<const float4*>(lr + y0);
+      l[0] = q.x;
+      l[1] = q.y;
+      l[2] = q.z;
+      l[3] = q.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) l[j] = y0 + j < V ? lr[y0 + j] : -INFINITY;
+    }
+    const uint4 w = philox4x32_10((uint32_t)g, tpos, 0u, 0u, k0, k1);
+    const uint32_t wj[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float x = l[j] * inv_t;
       if (x != -INFINITY) {
-        const float s = x + gumbel_from_word(philox_w0((uint32_t)y, tpos, 0u, 0u, k0, k1));
-        if (s > best || (s == best && y < bi)) {
+        const float s = x + gumbel_from_word(wj[j]);
+        if (s > best) {   // tokens in increasing order: the first of equal scores stays
           best = s;
-          bi = y;
+          bi = y0 + j;
         }
       }
     }
@@ -281,22 +429,40 @@ __global__ void gumbel_pick_kernel(const GumbelPart* part, int nvc, int32_t* row
   if (lane == 0) row_tokens[row] = bi == INT_MAX ? 0 : bi;
 }
 
+bool g_filter_smem_set[64] = {false};
+
+// tokens per CTA of a row's cluster (a multiple of 8, so the index array that
+// follows the slice stays 16-byte aligned)
+int filter_slice(int vocab) { return ((vocab + kFCluster - 1) / kFCluster + 7) / 8 * 8; }
+
 }  // namespace
 
 int launch_filter(const float* logits, float* out, int rows, int vocab, float temperature, int top_k, float top_p,
                   float min_p, int32_t* status, cudaStream_t st) {
+  if (vocab > kFilterMaxVocab) return TV_E_UNSUPPORTED;
   const float inv_t = (float)(1.0 / (double)temperature);
   const float log_min_p = min_p > 0.f ? (float)std::log((double)min_p) : -INFINITY;
-  return launch_pdl(filter_kernel, dim3(rows), dim3(kFilterThreads), 0, st, logits, out, vocab, inv_t, top_k,
-                    (double)top_p, log_min_p, (const int32_t*)status);
+  unsigned long long need_p = 0ull;
+  if (top_p < 1.f) {
+    need_p = (unsigned long long)((double)top_p * 1099511627776.0);
+    if (need_p == 0ull) need_p = 1ull;   // the largest token always stays
+  }
+  const int slice = filter_slice(vocab);
+  const size_t smem = (size_t)slice * (sizeof(float) + sizeof(uint16_t));
+  // the limit is raised once per device, to what the largest vocabulary needs
+  const int rc = ensure_smem_limit(filter_kernel, (size_t)filter_slice(kFilterMaxVocab) * 6, g_filter_smem_set);
+  if (rc) return rc;
+  return launch_pdl(filter_kernel, dim3(kFCluster, rows), dim3(kFThreads), smem, st, logits, out, vocab, slice,
+                    inv_t, top_k, need_p, log_min_p, (const int32_t*)status);
 }
 
 int launch_gumbel_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const SeedTable& sd,
                        GumbelPart* part, int32_t* row_tokens, int32_t* status, cudaStream_t st) {
   const int nvc = n_vchunks(vocab);
   const float inv_t = (float)(1.0 / (double)temperature);
+  const int vec4 = (vocab % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0) ? 1 : 0;
   int rc = launch_pdl(gumbel_partial_kernel, dim3(nvc, t.total_rows), dim3(256), 0, st, t, logits, vocab, inv_t, sd,
-                      nvc, part, (const int32_t*)status);
+                      nvc, vec4, part, (const int32_t*)status);
   if (rc) return rc;
   return launch_pdl(gumbel_pick_kernel, dim3(t.total_rows), dim3(32), 0, st, (const GumbelPart*)part, nvc, row_tokens,
                     (const int32_t*)status);

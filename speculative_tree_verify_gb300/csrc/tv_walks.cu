@@ -2,10 +2,11 @@
 //
 //  - greedy walk: one warp per request, lanes = tree nodes [Drafters and tree
 //    verify, §The round, step 3];
-//  - residual walk: a multi-CTA pass of per-chunk softmax statistics over the
-//    logits, then one warp per request walks the tree [Algorithm and
-//    correctness contract, §Deterministic tree candidates and residual
-//    verification];
+//  - residual walk: a multi-CTA pass of per-chunk and per-segment softmax
+//    statistics over the logits, then one warp per request walks the tree
+//    [Algorithm and correctness contract, §Deterministic tree candidates and
+//    residual verification];
+//  - single-draw and single-path rejection walks on the same statistics;
 //  - commit: gathers the accepted rows down into place [Drafters and tree
 //    verify, §Tree verify through recurrent layers, last paragraph].
 #include <climits>
@@ -57,47 +58,65 @@ __global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t*
 }
 
 // ---------------------------------------------------------------------------
-// residual walk, pass 1: per (row, vocab chunk) the chunk max m and
-// s = sum exp((l - m) / T).  grid (chunks, rows), block 256.
+// Pass 1 of every sampled walk: per (row, vocab chunk) the chunk max m and,
+// per 128-token segment, sum exp((l - m) / T).  grid (chunks, rows), block
+// 256: warp w reads the chunk's tokens 512w .. 512w + 511 (its segments
+// 4w .. 4w + 3) in coalesced 128-byte rows.  fp32 throughout: the GPU's FP64
+// rate is a small fraction of its FP32 rate, so FP64 appears below only where
+// a handful of per-chunk values are combined.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float softmax_term(float l, float m, float inv_t) { return expf((l - m) * inv_t); }
+
+// exp((m_c - M) / T): chunk units -> row units (0 for a chunk with no finite logit)
+__device__ __forceinline__ float chunk_scale(float mc, float M, float inv_t) {
+  return mc == -INFINITY ? 0.f : softmax_term(mc, M, inv_t);
+}
+
 __global__ void __launch_bounds__(256) row_stats_kernel(const float* logits, int V, float inv_t, int nvc,
                                                         RowStat* stats, const int32_t* status) {
   __shared__ float red[8];
+  __shared__ float s_seg[kSegsPerChunk];
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
   const int c = blockIdx.x, row = blockIdx.y;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* lr = logits + (size_t)row * V;
-  const int y0 = c * kVChunk;
-  float v[kVChunk / 256];
+  const int yw = c * kVChunk + w * (4 * kVSeg);
+  float v[16];
   float mx = -INFINITY;
 #pragma unroll
-  for (int k = 0; k < kVChunk / 256; ++k) {
-    const int y = y0 + k * 256 + threadIdx.x;
-    v[k] = y < V ? lr[y] : -INFINITY;
-    mx = fmaxf(mx, v[k]);
+  for (int j = 0; j < 16; ++j) {
+    const int y = yw + j * 32 + lane;
+    v[j] = y < V ? lr[y] : -INFINITY;
+    mx = fmaxf(mx, v[j]);
   }
   mx = warp_max(mx);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) red[w] = mx;
+  if (lane == 0) red[w] = mx;
   __syncthreads();
   mx = red[0];
-  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
-  __syncthreads();
-  float s = 0.f;
 #pragma unroll
-  for (int k = 0; k < kVChunk / 256; ++k)
-    if (v[k] != -INFINITY) s += expf((v[k] - mx) * inv_t);
-  s = warp_sum(s);
-  if (l == 0) red[w] = s;
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j >> 2] += softmax_term(v[j], mx, inv_t);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float sq = warp_sum(acc[q]);
+    if (lane == 0) s_seg[w * 4 + q] = sq;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < 8; ++i) tot += red[i];
-    RowStat st;
-    st.m = mx;
-    st.s = tot;
-    stats[(size_t)row * nvc + c] = st;
+  if (w == 0) {
+    const float sg = s_seg[lane];
+    const float tot = warp_sum(sg);
+    RowStat* o = stats + (size_t)row * nvc + c;
+    o->seg[lane] = sg;
+    if (lane == 0) {
+      o->m = mx;
+      o->s = tot;
+    }
   }
 }
 
@@ -107,44 +126,95 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   return v;
 }
 
-__device__ __forceinline__ double warp_incl_scan_d(double v) {
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double u = __shfl_up_sync(FULL, v, o);
+    const T u = __shfl_up_sync(FULL, v, o);
     if (lane >= o) v += u;
   }
   return v;
 }
 
-__device__ __forceinline__ bool is_rejected(int y, const int* rej, int nrej) {
-  for (int k = 0; k < nrej; ++k)
-    if (rej[k] == y) return true;
-  return false;
+// The row max M and Z = sum over the row of exp((l - M) / T), from the row's
+// chunk statistics; one warp, the same arithmetic in every kernel that needs them.
+__device__ __forceinline__ void row_mz(const RowStat* st, int nvc, float inv_t, float& M, double& Z) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int c = lane; c < nvc; c += 32) m = fmaxf(m, st[c].m);
+  m = warp_max(m);
+  double z = 0.0;
+  for (int c = lane; c < nvc; c += 32) z += (double)st[c].s * (double)chunk_scale(st[c].m, m, inv_t);
+  Z = warp_sum_d(z);
+  M = m;
 }
 
-// One draw y from r = p with the rejected tokens removed: the smallest y with
-// sum_{j<=y} r~(j) > target, r~ the unnormalised residual; if rounding leaves
-// none, the last y with r~(y) > 0.  Chunk masses first, then one chunk in
-// lane-contiguous segments of 128 entries.
-__device__ int residual_draw(const float* lr, int V, float M, float inv_t, const RowStat* st, int nvc,
-                             const int* rej, int nrej, double target) {
+// p = softmax(l / T) over a row with the tokens rej[0 .. nrej) removed
+struct SoftmaxRow {
+  const float* lr;
+  const RowStat* st;
+  const int* rej;
+  int nrej, V;
+  float M, inv_t;
+  __device__ float scale(int c) const { return chunk_scale(st[c].m, M, inv_t); }
+  __device__ double chunk_mass(int c) const {   // row units
+    double w = (double)st[c].s * (double)scale(c);
+    for (int k = 0; k < nrej; ++k)
+      if (rej[k] / kVChunk == c) w -= (double)softmax_term(lr[rej[k]], M, inv_t);
+    return w > 0.0 ? w : 0.0;
+  }
+  __device__ float seg_mass(int c, int s) const {   // chunk units
+    float w = st[c].seg[s];
+    const int g = c * kSegsPerChunk + s;
+    for (int k = 0; k < nrej; ++k)
+      if (rej[k] / kVSeg == g) w -= softmax_term(lr[rej[k]], st[c].m, inv_t);
+    return fmaxf(w, 0.f);
+  }
+  __device__ float tok_mass(int c, int y) const {   // chunk units
+    if (y >= V) return 0.f;
+    for (int k = 0; k < nrej; ++k)
+      if (rej[k] == y) return 0.f;
+    const float m = st[c].m;
+    return m == -INFINITY ? 0.f : softmax_term(lr[y], m, inv_t);
+  }
+};
+
+// r = max(p - q, 0) of a draft: p = softmax(l / T) of its parent's row, q its
+// proposal row; izf = 1 / Z of the parent's row, rounded to fp32 once
+__device__ __forceinline__ float resid_term(float l, float q, float M, float inv_t, float izf) {
+  return fmaxf(__fmaf_rn(softmax_term(l, M, inv_t), izf, -q), 0.f);
+}
+
+struct ResidRow {
+  const float* lp;
+  const float* qr;
+  const RejStat* rs;
+  int V;
+  float M, inv_t, izf;
+  __device__ float scale(int) const { return 1.f; }
+  __device__ double chunk_mass(int c) const { return (double)rs[c].resid; }
+  __device__ float seg_mass(int c, int s) const { return rs[c].seg[s]; }
+  __device__ float tok_mass(int, int y) const { return y < V ? resid_term(lp[y], qr[y], M, inv_t, izf) : 0.f; }
+};
+
+// One draw by the inverse CDF: the smallest y whose cumulative mass exceeds
+// target.  Searched chunk -> segment -> token, each step one warp-wide scan;
+// where rounding leaves the target at or past a step's total, the last token
+// with mass is taken.  Row supplies chunk_mass(c) in row units, scale(c) (row
+// units per chunk unit), seg_mass(c, s) and tok_mass(c, y) in chunk units.
+template <class Row>
+__device__ int cdf_draw(const Row& R, int nvc, double target) {
   const int lane = threadIdx.x & 31;
+  bool tail = false;
   double base = 0.0, before = 0.0;
-  int chunk = -1, last_pos = -1;
+  int chunk = -1, last_c = -1;
   for (int c0 = 0; c0 < nvc; c0 += 32) {
     const int c = c0 + lane;
-    double w = 0.0;
-    if (c < nvc) {
-      w = (double)st[c].s * (double)expf((st[c].m - M) * inv_t);
-      for (int k = 0; k < nrej; ++k)
-        if (rej[k] / kVChunk == c) w -= (double)expf((lr[rej[k]] - M) * inv_t);
-      if (w < 0.0) w = 0.0;
-    }
-    const int lp = __reduce_max_sync(FULL, (c < nvc && w > 0.0) ? c : -1);
-    if (lp > last_pos) last_pos = lp;
-    const double incl = warp_incl_scan_d(w);
-    const unsigned hm = __ballot_sync(FULL, c < nvc && w > 0.0 && base + incl > target);
+    const double w = c < nvc ? R.chunk_mass(c) : 0.0;
+    last_c = max(last_c, __reduce_max_sync(FULL, w > 0.0 ? c : -1));
+    const double incl = warp_incl_scan(w);
+    const unsigned hm = __ballot_sync(FULL, w > 0.0 && base + incl > target);
     if (hm != 0u) {
       const int L = __ffs(hm) - 1;
       chunk = c0 + L;
@@ -153,47 +223,65 @@ __device__ int residual_draw(const float* lr, int V, float M, float inv_t, const
     }
     base += __shfl_sync(FULL, incl, 31);
   }
-  double t2 = target - before;
-  if (chunk < 0) {   // rounding: fall back to the last entry with mass
-    chunk = last_pos < 0 ? 0 : last_pos;
-    t2 = INFINITY;
+  if (chunk < 0) {
+    if (last_c < 0) return 0;   // no mass anywhere
+    chunk = last_c;
+    tail = true;
   }
-  const int y0 = chunk * kVChunk + lane * (kVChunk / 32);
-  double mine = 0.0;
-  int last_valid = -1;
-  for (int k = 0; k < kVChunk / 32; ++k) {
-    const int y = y0 + k;
-    if (y < V && !is_rejected(y, rej, nrej)) {
-      const float e = expf((lr[y] - M) * inv_t);
-      mine += (double)e;
-      if (e > 0.f) last_valid = y;
+  const double t2 = tail ? 0.0 : (target - before) / (double)R.scale(chunk);
+  const float ws = R.seg_mass(chunk, lane);
+  const double incl2 = warp_incl_scan((double)ws);
+  const unsigned hm2 = __ballot_sync(FULL, !tail && ws > 0.f && incl2 > t2);
+  int seg;
+  double before2 = 0.0;
+  if (hm2 != 0u) {
+    seg = __ffs(hm2) - 1;
+    before2 = __shfl_sync(FULL, incl2 - (double)ws, seg);
+  } else {
+    seg = __reduce_max_sync(FULL, ws > 0.f ? lane : -1);
+    if (seg < 0) seg = kSegsPerChunk - 1;
+    tail = true;
+  }
+  const float t3 = (float)(t2 - before2);
+  for (int sg = seg; sg >= 0; --sg) {   // past `seg` only when rounding left a segment without mass
+    const int yb = chunk * kVChunk + sg * kVSeg + lane * 4;
+    float e[4], mine = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      e[j] = R.tok_mass(chunk, yb + j);
+      mine += e[j];
     }
-  }
-  const double incl = warp_incl_scan_d(mine);
-  const unsigned hm = __ballot_sync(FULL, mine > 0.0 && incl > t2);
-  if (hm == 0u) {
-    const int lv = __reduce_max_sync(FULL, last_valid);
-    return lv < 0 ? chunk * kVChunk : lv;
-  }
-  const int L = __ffs(hm) - 1;
-  int y_found = -1;
-  if (lane == L) {
-    double cum = incl - mine;
-    for (int k = 0; k < kVChunk / 32; ++k) {
-      const int y = y0 + k;
-      if (y < V && !is_rejected(y, rej, nrej)) {
-        const float e = expf((lr[y] - M) * inv_t);
-        cum += (double)e;
-        last_valid = e > 0.f ? y : last_valid;
-        if (cum > t2) {
-          y_found = y;
-          break;
+    if (!tail) {
+      const float incl3 = warp_incl_scan(mine);
+      const unsigned hm3 = __ballot_sync(FULL, mine > 0.f && incl3 > t3);
+      if (hm3 != 0u) {
+        const int L = __ffs(hm3) - 1;
+        int yf = -1;
+        if (lane == L) {
+          float cum = incl3 - mine;
+          int lastv = -1;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            cum += e[j];
+            if (e[j] > 0.f) {
+              lastv = yb + j;
+              if (cum > t3 && yf < 0) yf = yb + j;
+            }
+          }
+          if (yf < 0) yf = lastv;
         }
+        return __shfl_sync(FULL, yf, L);
       }
     }
-    if (y_found < 0) y_found = last_valid;
+    int lv = -1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e[j] > 0.f) lv = yb + j;
+    lv = __reduce_max_sync(FULL, lv);
+    if (lv >= 0) return lv;
+    tail = true;
   }
-  return __shfl_sync(FULL, y_found, L);
+  return chunk * kVChunk;   // the chunk's statistics said mass, its tokens said none
 }
 
 // residual walk, pass 2: one warp per request
@@ -225,12 +313,9 @@ __global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, f
   for (;;) {
     const float* lr = logits + (size_t)(row0 + cur) * V;
     const RowStat* st = stats + (size_t)(row0 + cur) * nvc;
-    float M = -INFINITY;
-    for (int c = lane; c < nvc; c += 32) M = fmaxf(M, st[c].m);
-    M = warp_max(M);
-    double Z = 0.0;
-    for (int c = lane; c < nvc; c += 32) Z += (double)st[c].s * (double)expf((st[c].m - M) * inv_t);
-    Z = warp_sum_d(Z);
+    float M;
+    double Z;
+    row_mz(st, nvc, inv_t, M, Z);
 
     // candidates: the children of cur, in increasing node index
     unsigned kids = __ballot_sync(FULL, lane > 0 && lane < n && par == cur);
@@ -242,7 +327,7 @@ __global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, f
       const int x = __shfl_sync(FULL, tok, c);
       const float u = __shfl_sync(FULL, uu, draw);
       ++draw;
-      const double ex = (double)expf((lr[x] - M) * inv_t);
+      const double ex = (double)softmax_term(lr[x], M, inv_t);
       if ((double)u < ex / (Z - R)) {   // accept x with probability r(x)
         acc = c;
         break;
@@ -266,7 +351,8 @@ __global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, f
     if (nrej > 0 || bonus_at_leaf) {
       const float u = __shfl_sync(FULL, uu, draw);
       ++draw;
-      const int y = residual_draw(lr, V, M, inv_t, st, nvc, s_rej, nrej, (double)u * (Z - R));
+      const SoftmaxRow row{lr, st, s_rej, nrej, V, M, inv_t};
+      const int y = cdf_draw(row, nvc, (double)u * (Z - R));
       if (lane == 0) out_tokens[row0 + nout] = y;
       ++nout;
     }
@@ -295,15 +381,12 @@ __global__ void draw_rows_kernel(ReqTable t, const float* logits, int V, float i
     if (lane == 0) status_set(status, TV_E_UNIFORM);
     return;
   }
-  const float* lr = logits + (size_t)row * V;
   const RowStat* st = stats + (size_t)row * nvc;
-  float M = -INFINITY;
-  for (int c = lane; c < nvc; c += 32) M = fmaxf(M, st[c].m);
-  M = warp_max(M);
-  double Z = 0.0;
-  for (int c = lane; c < nvc; c += 32) Z += (double)st[c].s * (double)expf((st[c].m - M) * inv_t);
-  Z = warp_sum_d(Z);
-  const int y = residual_draw(lr, V, M, inv_t, st, nvc, nullptr, 0, (double)u * Z);
+  float M;
+  double Z;
+  row_mz(st, nvc, inv_t, M, Z);
+  const SoftmaxRow R{logits + (size_t)row * V, st, nullptr, 0, V, M, inv_t};
+  const int y = cdf_draw(R, nvc, (double)u * Z);
   if (lane == 0) row_tokens[row] = y;
 }
 
@@ -311,16 +394,17 @@ __global__ void draw_rows_kernel(ReqTable t, const float* logits, int V, float i
 // single-path rejection sampler [Algorithm and correctness contract,
 // §Single-path sampling]: node i of a chain carries draft x_i drawn from the
 // proposal row q_i; the target row of x_i is its parent's, p = softmax(l / T).
-// Pass 1, per (vocab chunk, row i >= 1): sum max(p - q_i, 0), sum q_i, and a
-// flag for q entries that are not finite or negative.  grid (chunks, rows).
+// Pass 2, per (vocab chunk, row i >= 1): per segment sum max(p - q_i, 0), sum
+// q_i, and a flag for q entries that are not finite or negative.  grid
+// (chunks, rows), block 256, the token layout of pass 1.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rej_stats_kernel(ReqTable t, const float* logits, int V, float inv_t,
                                                         const float* proposals, const RowStat* stats, int nvc,
                                                         RejStat* rstats, const int32_t* status) {
-  __shared__ double rd[8], qd[8];
-  __shared__ int bd[8];
-  __shared__ float s_M;
-  __shared__ double s_Z;
+  __shared__ float s_seg[kSegsPerChunk];
+  __shared__ float s_q[8];
+  __shared__ int s_bad[8];
+  __shared__ float s_M, s_izf;
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
@@ -329,130 +413,63 @@ __global__ void __launch_bounds__(256) rej_stats_kernel(ReqTable t, const float*
   while (r + 1 < t.n_req && t.row_off[r + 1] <= row) ++r;
   if (row == t.row_off[r]) return;   // the root carries no draft
   const int prow = row - 1;           // a chain: the parent's row is the previous row
-  const RowStat* st = stats + (size_t)prow * nvc;
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    float M = -INFINITY;
-    for (int k = lane; k < nvc; k += 32) M = fmaxf(M, st[k].m);
-    M = warp_max(M);
-    double Z = 0.0;
-    for (int k = lane; k < nvc; k += 32) Z += (double)st[k].s * (double)expf((st[k].m - M) * inv_t);
-    Z = warp_sum_d(Z);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (w == 0) {
+    float M;
+    double Z;
+    row_mz(stats + (size_t)prow * nvc, nvc, inv_t, M, Z);
     if (lane == 0) {
       s_M = M;
-      s_Z = Z;
+      s_izf = (float)(1.0 / Z);
     }
   }
   __syncthreads();
-  const float M = s_M;
-  const double iz = 1.0 / s_Z;
+  const float M = s_M, izf = s_izf;
   const float* lp = logits + (size_t)prow * V;
   const float* qr = proposals + (size_t)row * V;
-  double resid = 0.0, qs = 0.0;
+  const int yw = c * kVChunk + w * (4 * kVSeg);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float qs = 0.f;
   int bad = 0;
-  for (int k = 0; k < kVChunk / 256; ++k) {
-    const int y = c * kVChunk + k * 256 + threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int y = yw + j * 32 + lane;
     if (y < V) {
       const float q = qr[y];
       if (!(q >= 0.f) || isinf(q)) bad = 1;
-      const double p = (double)expf((lp[y] - M) * inv_t) * iz;
-      resid += fmax(p - (double)q, 0.0);
-      qs += (double)q;
+      acc[j >> 2] += resid_term(lp[y], q, M, inv_t, izf);
+      qs += q;
     }
   }
-  resid = warp_sum_d(resid);
-  qs = warp_sum_d(qs);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float sq = warp_sum(acc[q]);
+    if (lane == 0) s_seg[w * 4 + q] = sq;
+  }
+  qs = warp_sum(qs);
   bad = __any_sync(FULL, bad);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) {
-    rd[w] = resid;
-    qd[w] = qs;
-    bd[w] = bad;
+  if (lane == 0) {
+    s_q[w] = qs;
+    s_bad[w] = bad;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    RejStat o;
-    o.resid = 0.0;
-    o.qsum = 0.0;
-    o.bad = 0;
-    o.pad = 0;
-    for (int i = 0; i < 8; ++i) {
-      o.resid += rd[i];
-      o.qsum += qd[i];
-      o.bad |= bd[i];
+  if (w == 0) {
+    const float sg = s_seg[lane];
+    const float tot = warp_sum(sg);
+    const float qt = warp_sum(lane < 8 ? s_q[lane] : 0.f);
+    const int bd = __any_sync(FULL, lane < 8 && s_bad[lane] != 0);
+    RejStat* o = rstats + (size_t)row * nvc + c;
+    o->seg[lane] = sg;
+    if (lane == 0) {
+      o->resid = tot;
+      o->qsum = qt;
+      o->bad = bd;
+      o->pad = 0;
     }
-    rstats[(size_t)row * nvc + c] = o;
   }
 }
 
-// One draw from r = max(p - q, 0): the smallest y with sum_{j<=y} r(j) >
-// target (target = u * sum r), chunk masses first, then one chunk; if rounding
-// leaves none, the last y with r(y) > 0.
-__device__ int rejection_draw(const float* lp, const float* qr, int V, float M, double iz, float inv_t,
-                              const RejStat* rs, int nvc, double target) {
-  const int lane = threadIdx.x & 31;
-  double base = 0.0, before = 0.0;
-  int chunk = -1, last_pos = -1;
-  for (int c0 = 0; c0 < nvc; c0 += 32) {
-    const int c = c0 + lane;
-    const double w = c < nvc ? rs[c].resid : 0.0;
-    const int lp2 = __reduce_max_sync(FULL, (c < nvc && w > 0.0) ? c : -1);
-    if (lp2 > last_pos) last_pos = lp2;
-    const double incl = warp_incl_scan_d(w);
-    const unsigned hm = __ballot_sync(FULL, c < nvc && w > 0.0 && base + incl > target);
-    if (hm != 0u) {
-      const int L = __ffs(hm) - 1;
-      chunk = c0 + L;
-      before = base + __shfl_sync(FULL, incl - w, L);
-      break;
-    }
-    base += __shfl_sync(FULL, incl, 31);
-  }
-  double t2 = target - before;
-  if (chunk < 0) {
-    chunk = last_pos < 0 ? 0 : last_pos;
-    t2 = INFINITY;
-  }
-  auto mass = [&](int y) { return fmax((double)expf((lp[y] - M) * inv_t) * iz - (double)qr[y], 0.0); };
-  const int y0 = chunk * kVChunk + lane * (kVChunk / 32);
-  double mine = 0.0;
-  int last_valid = -1;
-  for (int k = 0; k < kVChunk / 32; ++k) {
-    const int y = y0 + k;
-    if (y < V) {
-      const double m = mass(y);
-      mine += m;
-      if (m > 0.0) last_valid = y;
-    }
-  }
-  const double incl = warp_incl_scan_d(mine);
-  const unsigned hm = __ballot_sync(FULL, mine > 0.0 && incl > t2);
-  if (hm == 0u) {
-    const int lv = __reduce_max_sync(FULL, last_valid);
-    return lv < 0 ? chunk * kVChunk : lv;
-  }
-  const int L = __ffs(hm) - 1;
-  int y_found = -1;
-  if (lane == L) {
-    double cum = incl - mine;
-    for (int k = 0; k < kVChunk / 32; ++k) {
-      const int y = y0 + k;
-      if (y < V) {
-        const double m = mass(y);
-        cum += m;
-        if (m > 0.0) last_valid = y;
-        if (cum > t2) {
-          y_found = y;
-          break;
-        }
-      }
-    }
-    if (y_found < 0) y_found = last_valid;
-  }
-  return __shfl_sync(FULL, y_found, L);
-}
-
-// Pass 2, one warp per request: validate, then test the drafts in order.
+// Pass 3, one warp per request: validate, then test the drafts in order.
 __global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, float inv_t, const float* proposals,
                                         const float* uniforms, const RowStat* stats, const RejStat* rstats, int nvc,
                                         int32_t* path, int32_t* accept_len, int32_t* out_tokens,
@@ -485,7 +502,7 @@ __global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, 
     double qs = 0.0;
     int fl = 0;
     for (int c = lane; c < nvc; c += 32) {
-      qs += rs[c].qsum;
+      qs += (double)rs[c].qsum;
       fl |= rs[c].bad;
     }
     qs = warp_sum_d(qs);
@@ -502,17 +519,13 @@ __global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, 
   if (lane == 0) path[row0] = 0;
   for (int i = 1; i < n; ++i) {
     const int prow = row0 + i - 1;
-    const RowStat* st = stats + (size_t)prow * nvc;
-    float M = -INFINITY;
-    for (int c = lane; c < nvc; c += 32) M = fmaxf(M, st[c].m);
-    M = warp_max(M);
-    double Z = 0.0;
-    for (int c = lane; c < nvc; c += 32) Z += (double)st[c].s * (double)expf((st[c].m - M) * inv_t);
-    Z = warp_sum_d(Z);
+    float M;
+    double Z;
+    row_mz(stats + (size_t)prow * nvc, nvc, inv_t, M, Z);
     const float* lp = logits + (size_t)prow * V;
     const float* qr = proposals + (size_t)(row0 + i) * V;
     const int x = __shfl_sync(FULL, tok, i);
-    const double px = (double)expf((lp[x] - M) * inv_t) / Z;
+    const double px = (double)softmax_term(lp[x], M, inv_t) / Z;
     const double qx = (double)qr[x];
     const float u = __shfl_sync(FULL, uu, i);
     if ((double)u < px / qx) {   // accept with probability min(1, p/q)
@@ -526,11 +539,12 @@ __global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, 
     }
     // the first rejection: one draw from normalize(max(p - q, 0)), then stop
     const RejStat* rs = rstats + (size_t)(row0 + i) * nvc;
-    double R = 0.0;
-    for (int c = lane; c < nvc; c += 32) R += rs[c].resid;
-    R = warp_sum_d(R);
+    double Rm = 0.0;
+    for (int c = lane; c < nvc; c += 32) Rm += (double)rs[c].resid;
+    Rm = warp_sum_d(Rm);
     const float u0 = __shfl_sync(FULL, uu, 0);
-    const int y = rejection_draw(lp, qr, V, M, 1.0 / Z, inv_t, rs, nvc, (double)u0 * R);
+    const ResidRow row{lp, qr, rs, V, M, inv_t, (float)(1.0 / Z)};
+    const int y = cdf_draw(row, nvc, (double)u0 * Rm);
     if (lane == 0) out_tokens[row0 + nout] = y;
     ++nout;
     break;

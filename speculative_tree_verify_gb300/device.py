@@ -142,6 +142,50 @@ def commit(reqs: Sequence[DeviceRequest], b: RoundBuffers, stream=None) -> int:
                             b.accept_len, b.committed_src, b.new_ctx, b.status, stream)
 
 
+@dataclass
+class SampleBuffers:
+    """Workspace and outputs of the sampled entry points (filters, single-draw,
+    Gumbel and rejection walks) for up to ``rows`` tree rows."""
+    ws: torch.Tensor
+    row_tokens: torch.Tensor
+    filtered: torch.Tensor
+
+    @classmethod
+    def alloc(cls, vocab: int, rows: int, device="cuda") -> "SampleBuffers":
+        rc, nbytes = abi.tv_sample_workspace_size(vocab, rows)
+        check(rc, "tv_sample_workspace_size")
+        return cls(ws=torch.empty(nbytes, device=device, dtype=torch.uint8),
+                   row_tokens=torch.empty(rows, device=device, dtype=torch.int32),
+                   filtered=torch.empty(rows, vocab, device=device, dtype=torch.float32))
+
+
+def sample_filter(b: RoundBuffers, sb: SampleBuffers, rows: int, temperature: float, top_k: int = 0,
+                  top_p: float = 1.0, min_p: float = 0.0, stream=None) -> int:
+    return abi.tv_sample_filter(b.logits, sb.filtered, rows, b.dims.vocab, temperature, top_k, top_p, min_p,
+                                b.status, stream)
+
+
+def accept_single_draw(reqs: Sequence[DeviceRequest], b: RoundBuffers, sb: SampleBuffers, temperature: float,
+                       filtered: bool = False, stream=None) -> int:
+    return abi.tv_accept_single_draw([r.tree() for r in reqs], sb.filtered if filtered else b.logits, b.dims.vocab,
+                                     temperature, b.uniforms, sb.row_tokens, b.path, b.accept_len, b.out_tokens,
+                                     b.status, sb.ws, sb.ws.numel(), stream)
+
+
+def accept_gumbel(reqs: Sequence[DeviceRequest], b: RoundBuffers, sb: SampleBuffers, temperature: float,
+                  seeds: Sequence[int], positions: Sequence[int], filtered: bool = False, stream=None) -> int:
+    return abi.tv_accept_gumbel([r.tree() for r in reqs], sb.filtered if filtered else b.logits, b.dims.vocab,
+                                temperature, seeds, positions, sb.row_tokens, b.path, b.accept_len, b.out_tokens,
+                                b.status, sb.ws, sb.ws.numel(), stream)
+
+
+def accept_rejection(reqs: Sequence[DeviceRequest], b: RoundBuffers, sb: SampleBuffers, temperature: float,
+                     proposals: torch.Tensor, stream=None) -> int:
+    return abi.tv_accept_rejection([r.tree() for r in reqs], b.logits, b.dims.vocab, temperature, proposals,
+                                   b.uniforms, b.path, b.accept_len, b.out_tokens, b.out_count, b.status, sb.ws,
+                                   sb.ws.numel(), stream)
+
+
 def run_round(model: DeviceModel, reqs: Sequence[DeviceRequest], b: RoundBuffers, sampled: Optional[float] = None,
               stream=None):
     """One round on one stream: verify, accept (greedy, or residual sampling at

@@ -132,6 +132,7 @@ def test_sampled_host_checks(lib):
         assert abi.tv_sample_filter(FAKE, FAKE + 256, 2, 16, 1.0, k, p, mp, FAKE) == abi.CODES["TV_E_ARG"]
     assert abi.tv_sample_filter(FAKE, FAKE, 2, 16, 1.0, 0, 1.0, 0.0, FAKE) == abi.CODES["TV_E_ARG"]
     assert abi.tv_sample_filter(FAKE, FAKE + 256, 33, 16, 1.0, 0, 1.0, 0.0, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_sample_filter(FAKE, FAKE + 256, 2, 262145, 1.0, 0, 1.0, 0.0, FAKE) == abi.CODES["TV_E_UNSUPPORTED"]
     # the walks: temperature, row count, workspace size, positions
     trees = [_tree(8)]
     _, ws8 = abi.tv_sample_workspace_size(1024, 8)

@@ -91,6 +91,49 @@ def test_filter_parity(gpu, V, T, k, p, mp):
         np.testing.assert_allclose(g[r, both], o[both], rtol=3e-7, atol=0)
 
 
+def _filter_check(logits, T, k, p, mp):
+    rows, V = logits.shape
+    x = torch.from_numpy(np.ascontiguousarray(logits)).cuda()
+    out = torch.empty_like(x)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _ok(abi.tv_sample_filter(x, out, rows, V, T, k, p, mp, st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    g = out.cpu().numpy()
+    for r in range(rows):
+        o = S.sample_filter(logits[r], T, top_k=k, top_p=p, min_p=mp)
+        keep_o, keep_g = np.isfinite(o), np.isfinite(g[r])
+        for j in np.nonzero(keep_o != keep_g)[0]:
+            assert _on_boundary(logits[r], T, k, p, mp, j), (r, j)
+        both = keep_o & keep_g
+        np.testing.assert_allclose(g[r, both], o[both], rtol=3e-7, atol=0)
+        assert np.all(g[r, ~keep_g] == -np.inf)
+    return g
+
+
+@pytest.mark.parametrize("V", [2, 16, 4099, 262144])
+def test_filter_vocab_sizes(gpu, V):
+    logits = synth.logits_rows(3, V, 40 + V % 11, scale=2.0)
+    _filter_check(logits, 0.9, min(7, V - 1), 0.85, 0.01)
+
+
+def test_filter_ties_and_masked_rows(gpu):
+    V = 20000
+    rng = np.random.default_rng(3)
+    logits = (np.round(rng.standard_normal((4, V)) * 2) / 2).astype(np.float32)   # heavy ties
+    logits[1, rng.random(V) < 0.3] = -np.inf                                       # an already-filtered row
+    logits[2] = 1.25                                                               # one value everywhere
+    logits[3, :V // 2] = -np.inf
+    for T, k, p, mp in ((1.0, 10, 1.0, 0.0), (0.7, 0, 0.5, 0.0), (1.3, 300, 0.95, 0.1), (1.0, 0, 1e-6, 0.0)):
+        g = _filter_check(logits, T, k, p, mp)
+        if k == 10:   # every token tied with the 10th largest stays
+            r0 = logits[0]
+            kth = np.sort(r0)[::-1][9]
+            assert np.isfinite(g[0]).sum() == (r0 >= kth).sum() > 10
+        if p == 1e-6:   # only the largest logit (and its ties) stays
+            assert np.array_equal(np.isfinite(g[0]), logits[0] == logits[0].max())
+
+
 def test_filter_rejects_bad_arguments(gpu):
     x = torch.zeros(2, 16, device="cuda")
     out = torch.empty_like(x)
@@ -144,7 +187,7 @@ def test_single_draw_parity(gpu, V, T, seed):
 # ---------------------------------------------------------------------------
 # seeded Gumbel walk
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("V,T,seed", [(1024, 1.0, 0), (151936, 0.8, 1)])
+@pytest.mark.parametrize("V,T,seed", [(1024, 1.0, 0), (5003, 1.1, 2), (151936, 0.8, 1)])
 def test_gumbel_parity(gpu, V, T, seed):
     trees = _trees(V, 3, 400 + seed)
     rows = sum(t.n for t in trees)

@@ -27,6 +27,17 @@ def test_philox_known_answers():
         assert ["%08x" % int(w) for w in out] == v["out"]
 
 
+def test_gumbel_uniform_word_layout():
+    """token i uses word i mod 4 of the block at counter (i div 4, t, 0, 0)"""
+    seed, t = 0x0123456789ABCDEF, 41
+    u = S.gumbel_uniform(seed, t, np.arange(12))
+    for i in range(12):
+        w = S.philox4x32_10((i // 4, t, 0, 0), (seed & 0xFFFFFFFF, seed >> 32))[i % 4]
+        assert u[i] == (int(w) + 0.5) / 2.0 ** 32
+    # the all-zero known-answer vector of Salmon et al.: counter 0, key 0
+    kat = S.philox4x32_10((0, 0, 0, 0), (0, 0))
+    assert list(S.gumbel_uniform(0, 0, np.arange(4))) == [(int(w) + 0.5) / 2.0 ** 32 for w in kat]
+
 def test_gumbel_uniforms_open_interval_and_keyed():
     u = S.gumbel_uniform(7, 3, np.arange(100000))
     assert np.all(u > 0) and np.all(u < 1)
@@ -49,9 +60,11 @@ def test_gumbel_max_draws_follow_p():
     p = S.softmax_x(x)
     T = 200000
     t = np.arange(T, dtype=np.uint64)[:, None]
-    idx = np.arange(12, dtype=np.uint64)[None, :]
-    w, _, _, _ = S.philox4x32_10((np.broadcast_to(idx, (T, 12)), np.broadcast_to(t, (T, 12)),
-                                  np.zeros((T, 12), np.uint64), np.zeros((T, 12), np.uint64)), (99, 0))
+    z = np.zeros((T, 3), np.uint64)
+    # tokens 0..11 take the four words of the generator blocks 0, 1, 2
+    words = S.philox4x32_10((np.broadcast_to(np.arange(3, dtype=np.uint64)[None, :], (T, 3)),
+                             np.broadcast_to(t, (T, 3)), z, z), (99, 0))
+    w = np.stack(words, axis=2).reshape(T, 12)
     u = (w.astype(np.float64) + 0.5) / 4294967296.0
     y = np.argmax(x[None, :] - np.log(-np.log(u)), axis=1)
     assert _chi_ok(np.bincount(y, minlength=12), p, T)
