@@ -6,10 +6,11 @@
 //    the cluster sums its histograms through distributed shared memory.  The
 //    k-th largest logit and the top-p boundary are found in two levels: a
 //    256-bin histogram of (l_max - l) / T, which places the boundary in one
-//    bin, then radix selection (four 8-bit passes) on an order-preserving
-//    integer key of the logits in that bin.  Histograms hold integer weights
-//    (counts, or probability masses in units of 2^-40), so the result is exact
-//    and the same on every run.
+//    bin, then an exact pass over an order-preserving integer key of the
+//    logits in that bin (256 sub-bins, then ranking when the last bin is
+//    small; else radix selection, four 8-bit passes).  Weights are integers
+//    (counts, or exp((l - l_max) / T) in units of 2^-32), so the result is
+//    exact and the same on every run.
 //  - Gumbel: the token at sequence index t is argmax_i (x_i + G_i), G_i Gumbel
 //    noise from Philox4x32-10 keyed by (seed, t) [Exactness, §Sampling, third
 //    paragraph]; token i takes word i mod 4 of the generator block at counter
@@ -49,14 +50,19 @@ __device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t a) {
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return (int)v;
+}
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ double ld_dsmem_f64(uint32_t a) {
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(a) : "memory");
   return v;
 }
 
@@ -66,26 +72,33 @@ constexpr int kFThreads = 512;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kFBins = 256;
 constexpr float kFBinsPerUnit = 8.f;    // level-1 bin width: 1/8 of a unit of (l_max - l) / T
+constexpr float kFSubBins = 256.f;      // level-2 bins per level-1 bin
 constexpr int kFilterMaxVocab = 262144;
+constexpr int kFPriv = 4;               // private level-1 histograms per CTA (warp w adds into w mod 4)
+constexpr int kCandCap = 4096;          // tokens a CTA lists per level; past that it rescans its slice
+constexpr int kGatherMax = 512;         // last bins this small (cluster-wide) are finished by ranking
+constexpr int kFScratch = kFPriv * 2 * kFBins * 4;   // bytes: private histograms, or the gathered tokens
+static_assert(kGatherMax * 12 <= kFScratch, "gathered keys and weights fit the scratch area");
 
-// order-preserving key: larger float -> larger unsigned (NaN sorts lowest)
+// order-preserving key: larger float -> larger unsigned; -0 and +0 share a
+// key (they compare equal), NaN sorts lowest
 __device__ __forceinline__ uint32_t fkey(float x) {
   if (x != x) return 0u;
-  const uint32_t u = __float_as_uint(x);
+  const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 struct FilterShared {
   unsigned long long hist[2][kFBins];   // this CTA's histogram (two, used in turn); the cluster reads them
   unsigned long long tot[kFBins];       // the cluster's histogram
-  unsigned long long res[2];            // selected bin and the weight before it
-  double pub_z;                         // this CTA's part of Z (read by the cluster)
-  double redd[kFWarps];
-  double Z;
+  unsigned long long res[3];            // selected bin, the weight before it, the weight needed
   float pub_max;                        // this CTA's slice maximum (read by the cluster)
   float redf[kFWarps];
   float M;
-  int cnt;
+  int cnt1;                             // this CTA's level-1 boundary-bin tokens
+  int cnt2[2];                          // its level-2 boundary-bin tokens, per selection (read by the cluster)
+  int off[kFCluster + 1];               // the cluster's level-2 boundary-bin tokens, prefix by CTA
+  uint32_t key_sel;
 };
 
 // The cluster's histogram tot[] from every CTA's hist[hb] (after a cluster barrier).
@@ -100,11 +113,21 @@ __device__ __forceinline__ void cluster_hist(FilterShared& sh, int hb) {
 }
 
 // One warp: the first bin, counted from bin 0 upward (descending = false) or
-// from bin 255 downward, at which the running weight reaches need; res[0] = the
-// bin (~0 when the total falls short), res[1] = the weight before it.
-__device__ __forceinline__ void find_bin(FilterShared& sh, unsigned long long need, bool descending) {
+// from bin 255 downward, at which the running weight reaches need; with frac > 0
+// need is first set to ceil(frac * the histogram's total), at least 1.
+// res[0] = the bin (~0 when the total falls short), res[1] = the weight before
+// it, res[2] = need.
+__device__ __forceinline__ void find_bin(FilterShared& sh, unsigned long long need, double frac, bool descending) {
   if (threadIdx.x >= 32) return;
   const int lane = threadIdx.x;
+  if (frac > 0.0) {
+    unsigned long long s = 0ull;
+#pragma unroll
+    for (int k = 0; k < kFBins / 32; ++k) s += sh.tot[k * 32 + lane];
+    s = warp_sum(s);
+    const double want = ceil(frac * (double)s);
+    need = want < 1.0 ? 1ull : (want >= (double)s ? s : (unsigned long long)want);
+  }
   unsigned long long above = 0ull, before = 0ull;
   int found = -1;
   for (int b0 = 0; b0 < kFBins && found < 0; b0 += 32) {
@@ -127,52 +150,197 @@ __device__ __forceinline__ void find_bin(FilterShared& sh, unsigned long long ne
   if (lane == 0) {
     sh.res[0] = found < 0 ? ~0ull : (unsigned long long)found;
     sh.res[1] = before;
+    sh.res[2] = need;
+  }
+}
+
+// hist[digit(x)] += wt(x) over the tokens list[0..n) of the slice (all tokens
+// 0..n-1 when list is null) that pass keep; one atomic per warp where all of
+// the warp's tokens share a digit.
+template <typename Keep, typename Digit, typename Weight>
+__device__ __forceinline__ void hist_pass(unsigned long long* hist, const float* xs, const uint16_t* list, int n,
+                                          Keep keep, Digit digit, Weight wt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j0 = warp * 32; j0 < n; j0 += kFThreads) {
+    const int j = j0 + lane;
+    bool ok = false;
+    float x = 0.f;
+    if (j < n) {
+      x = xs[list ? (int)list[j] : j];
+      ok = keep(x);
+    }
+    const unsigned m = __ballot_sync(FULL, ok);
+    if (m == 0u) continue;
+    const int d = ok ? digit(x) : 0;
+    const int d0 = __shfl_sync(FULL, d, __ffs(m) - 1);
+    const unsigned long long w = ok ? wt(x) : 0ull;
+    if (__all_sync(FULL, !ok || d == d0)) {
+      const unsigned long long s = warp_sum(w);
+      if (lane == 0) atomicAdd(&hist[d0], s);
+    } else if (ok) {
+      atomicAdd(&hist[d], w);
+    }
+  }
+}
+
+// out[...] = the slice indices among list[0..n) (all 0..n-1 when list is null)
+// that pass keep, one slot allocation per warp; *count ends at the number found,
+// which may pass kCandCap (entries past it are not written).
+template <typename Keep>
+__device__ __forceinline__ void list_pass(uint16_t* out, int* count, const float* xs, const uint16_t* list, int n,
+                                          Keep keep) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int j0 = warp * 32; j0 < n; j0 += kFThreads) {
+    const int j = j0 + lane;
+    int i = 0;
+    bool in = false;
+    if (j < n) {
+      i = list ? (int)list[j] : j;
+      in = keep(xs[i]);
+    }
+    const unsigned m = __ballot_sync(FULL, in);
+    if (m == 0u) continue;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(count, __popc(m));
+    base = __shfl_sync(FULL, base, 0);
+    const int slot = base + __popc(m & ((1u << lane) - 1u));
+    if (in && slot < kCandCap) out[slot] = (uint16_t)i;
   }
 }
 
 // Over the tokens with key >= floor: the largest key K such that the weight of
-// the tokens with key >= K reaches need (floor when the total falls short).
-// Level 1 places K in one bin of (M - l) / T, which falls as l rises, so every
-// token of a lower bin has a larger key than every token of that bin; level 2
-// selects K among the keys of that bin, 8 bits at a time from the top.
+// the tokens with key >= K reaches need (need = ceil(frac * their total weight)
+// when frac > 0); floor when the total falls short.
+//  level 1: bins of d = (M - l) / T * 8, which falls as l rises, so every token
+//           of a lower bin has a larger key than every token of a higher one;
+//  level 2: 256 sub-bins of the level-1 boundary bin, by the same rule;
+//  level 3: the keys of the level-2 boundary bin: when the cluster holds at
+//           most kGatherMax of them every CTA gathers them all and ranks them;
+//           otherwise radix selection, 8 bits at a time from the top.
 template <typename Weight>
-__device__ uint32_t select_key(FilterShared& sh, const float* xs, uint16_t* cand, int n_loc, float M, float inv_t,
-                               uint32_t floor_key, unsigned long long need, Weight wt, int& hb) {
-  auto bin_of = [&](float x) { return (int)fminf((M - x) * inv_t * kFBinsPerUnit, (float)(kFBins - 1)); };
-  for (int b = threadIdx.x; b < kFBins; b += kFThreads) sh.hist[hb][b] = 0ull;
-  if (threadIdx.x == 0) sh.cnt = 0;
+__device__ uint32_t select_key(FilterShared& sh, const float* xs, uint16_t* cand1, uint16_t* cand2,
+                               unsigned char* scratch, int n_loc, float M, float inv_t, uint32_t floor_key,
+                               unsigned long long need, double frac, Weight wt, int sel, int& hb) {
+  const int warp = threadIdx.x >> 5;
+  auto dval = [&](float x) { return (M - x) * inv_t * kFBinsPerUnit; };
+  auto bin_of = [&](float x) { return (int)fminf(dval(x), (float)(kFBins - 1)); };
+
+  // level 1, in private histograms of 32-bit parts, weight = hi * 2^16 + lo:
+  // weights are at most 2^32 and a private histogram sees at most n_loc / 4
+  // tokens, so a part sums below 2^30
+  uint32_t* priv = reinterpret_cast<uint32_t*>(scratch);
+  for (int b = threadIdx.x; b < kFPriv * 2 * kFBins; b += kFThreads) priv[b] = 0u;
+  if (threadIdx.x == 0) {
+    sh.cnt1 = 0;
+    sh.cnt2[sel] = 0;
+    sh.key_sel = floor_key;
+  }
   __syncthreads();
+  uint32_t* ph = priv + (warp & (kFPriv - 1)) * 2 * kFBins;
   for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
     const float x = xs[i];
-    if (fkey(x) >= floor_key) atomicAdd(&sh.hist[hb][bin_of(x)], wt(x));
+    if (fkey(x) >= floor_key) {
+      const int b = bin_of(x);
+      const unsigned long long w = wt(x);
+      atomicAdd(&ph[b], (uint32_t)(w & 0xFFFFull));
+      const uint32_t hi = (uint32_t)(w >> 16);
+      if (hi != 0u) atomicAdd(&ph[kFBins + b], hi);
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kFBins; b += kFThreads) {
+    unsigned long long s = 0ull;
+#pragma unroll
+    for (int g = 0; g < kFPriv; ++g)
+      s += (unsigned long long)priv[g * 2 * kFBins + b] + ((unsigned long long)priv[g * 2 * kFBins + kFBins + b] << 16);
+    sh.hist[hb][b] = s;
   }
   cluster_sync_all();
   cluster_hist(sh, hb);
   hb ^= 1;
-  find_bin(sh, need, false);
+  find_bin(sh, need, frac, false);
   __syncthreads();
-  const unsigned long long B = sh.res[0];
-  if (B == ~0ull) return floor_key;   // the weight falls short: no cut
+  const unsigned long long B1 = sh.res[0];
+  if (B1 == ~0ull) return floor_key;   // the weight falls short: no cut
+  need = sh.res[2] - sh.res[1];
+  auto in1 = [&](float x) { return fkey(x) >= floor_key && bin_of(x) == (int)B1; };
+
+  // level 2
+  list_pass(cand1, &sh.cnt1, xs, nullptr, n_loc, in1);
+  for (int b = threadIdx.x; b < kFBins; b += kFThreads) sh.hist[hb][b] = 0ull;
+  __syncthreads();
+  const int c1 = sh.cnt1;
+  const bool listed1 = c1 <= kCandCap;
+  auto sub_of = [&](float x) { return (int)fminf((dval(x) - (float)B1) * kFSubBins, (float)(kFBins - 1)); };
+  auto keep1 = [&](float x) { return listed1 || in1(x); };
+  hist_pass(sh.hist[hb], xs, listed1 ? cand1 : nullptr, listed1 ? c1 : n_loc, keep1, sub_of, wt);
+  cluster_sync_all();
+  cluster_hist(sh, hb);
+  hb ^= 1;
+  find_bin(sh, need, 0.0, false);
+  __syncthreads();
+  const int B2 = (int)sh.res[0];   // found: bin B1 holds at least need
   need -= sh.res[1];
-  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
-    const float x = xs[i];
-    if (fkey(x) >= floor_key && bin_of(x) == (int)B) cand[atomicAdd(&sh.cnt, 1)] = (uint16_t)i;
+  auto keep2 = [&](float x) { return keep1(x) && sub_of(x) == B2; };
+
+  // level 3
+  list_pass(cand2, &sh.cnt2[sel], xs, listed1 ? cand1 : nullptr, listed1 ? c1 : n_loc, keep2);
+  cluster_sync_all();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int c = lane < kFCluster ? ld_dsmem_s32(dsmem_addr(&sh.cnt2[sel], lane)) : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(FULL, c, o);
+      if (lane >= o) c += u;
+    }
+    if (lane < kFCluster) sh.off[lane + 1] = c;
+    if (lane == 0) sh.off[0] = 0;
   }
   __syncthreads();
-  const int nc = sh.cnt;
+  const int total = sh.off[kFCluster];
+
+  if (total <= kGatherMax) {   // every CTA ranks the whole bin (each listed all of its tokens)
+    unsigned long long* gw = reinterpret_cast<unsigned long long*>(scratch);
+    uint32_t* gk = reinterpret_cast<uint32_t*>(scratch + kGatherMax * sizeof(unsigned long long));
+    for (int t = threadIdx.x; t < total; t += kFThreads) {
+      int r = 0;
+      while (t >= sh.off[r + 1]) ++r;
+      const int ci = ld_dsmem_u16(dsmem_addr(&cand2[t - sh.off[r]], r));
+      const float x = ld_dsmem_f32(dsmem_addr(&xs[ci], r));
+      gk[t] = fkey(x);
+      gw[t] = wt(x);
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < total; t += kFThreads) {
+      const uint32_t k = gk[t];
+      unsigned long long above = 0ull, eq = 0ull;
+      for (int j = 0; j < total; ++j) {
+        const uint32_t kj = gk[j];
+        const unsigned long long wj = gw[j];
+        above += kj > k ? wj : 0ull;
+        eq += kj == k ? wj : 0ull;
+      }
+      if (above < need && need <= above + eq) sh.key_sel = k;   // one key; its ties write the same value
+    }
+    __syncthreads();
+    return sh.key_sel;
+  }
+
+  const int c2 = sh.cnt2[sel];
+  const bool listed2 = c2 <= kCandCap;
   uint32_t prefix = 0u, mask = 0u;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int b = threadIdx.x; b < kFBins; b += kFThreads) sh.hist[hb][b] = 0ull;
     __syncthreads();
-    for (int j = threadIdx.x; j < nc; j += kFThreads) {
-      const float x = xs[cand[j]];
-      const uint32_t k = fkey(x);
-      if ((k & mask) == prefix) atomicAdd(&sh.hist[hb][(k >> shift) & 255u], wt(x));
-    }
+    hist_pass(
+        sh.hist[hb], xs, listed2 ? cand2 : nullptr, listed2 ? c2 : n_loc,
+        [&](float x) { return (listed2 || keep2(x)) && (fkey(x) & mask) == prefix; },
+        [&](float x) { return (int)((fkey(x) >> shift) & 255u); }, wt);
     cluster_sync_all();
     cluster_hist(sh, hb);
     hb ^= 1;
-    find_bin(sh, need, true);
+    find_bin(sh, need, 0.0, true);
     __syncthreads();
     const unsigned long long f = sh.res[0];
     if (f == ~0ull) return floor_key;   // not reached: the bin holds at least need
@@ -192,25 +360,19 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return m;
 }
 
-__device__ __forceinline__ double block_sum_d(float v, double* red) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = (double)v;
-  __syncthreads();
-  double s = 0.0;
-  for (int i = 0; i < kFWarps; ++i) s += red[i];   // fixed order
-  return s;
-}
-
 // One cluster per row; CTA `rank` holds tokens [rank * slice, rank * slice + slice).
 // out = x = logit / T where kept, -inf elsewhere; selection on the raw logits
-// (the scale by 1/T keeps their order).
+// (the scale by 1/T keeps their order).  Dynamic shared memory: the slice, the
+// level-1 and level-2 lists, the scratch area.
 __global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
-    filter_kernel(const float* logits, float* out, int V, int slice, float inv_t, int top_k,
-                  unsigned long long need_p, float log_min_p, const int32_t* status) {
+    filter_kernel(const float* logits, float* out, int V, int slice, float inv_t, int top_k, float top_p,
+                  float log_min_p, const int32_t* status) {
   __shared__ FilterShared sh;
   extern __shared__ __align__(16) unsigned char dyn[];
   float* xs = reinterpret_cast<float*>(dyn);
-  uint16_t* cand = reinterpret_cast<uint16_t*>(dyn + (size_t)slice * sizeof(float));
+  uint16_t* cand1 = reinterpret_cast<uint16_t*>(dyn + (size_t)slice * sizeof(float));
+  uint16_t* cand2 = cand1 + kCandCap;
+  unsigned char* scratch = reinterpret_cast<unsigned char*>(cand2 + kCandCap);
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;   // the same status for every CTA of the cluster
@@ -241,29 +403,12 @@ __global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
   uint32_t kfloor = 1u;   // above every NaN key
   if (M != -INFINITY) {
     if (top_k > 0 && top_k < V)
-      kfloor = select_key(sh, xs, cand, n_loc, M, inv_t, kfloor, (unsigned long long)top_k,
-                          [](float) { return 1ull; }, hb);
-    if (need_p != 0ull) {
-      // probabilities over the tokens kept so far, as integers in units of 2^-40
-      float z = 0.f;
-      for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
-        const float x = xs[i];
-        if (fkey(x) >= kfloor) z += expf((x - M) * inv_t);
-      }
-      const double zc = block_sum_d(z, sh.redd);
-      if (threadIdx.x == 0) sh.pub_z = zc;
-      cluster_sync_all();
-      if (threadIdx.x == 0) {
-        double Z = 0.0;
-        for (int r = 0; r < kFCluster; ++r) Z += ld_dsmem_f64(dsmem_addr(&sh.pub_z, r));
-        sh.Z = Z;
-      }
-      __syncthreads();
-      const float scale = (float)(1099511627776.0 / sh.Z);   // 2^40 / Z
+      kfloor = select_key(sh, xs, cand1, cand2, scratch, n_loc, M, inv_t, kfloor, (unsigned long long)top_k, 0.0,
+                          [](float) { return 1ull; }, 0, hb);
+    if (top_p < 1.f)   // weights: exp((l - l_max) / T) in units of 2^-32, at most 2^32
       kfloor = select_key(
-          sh, xs, cand, n_loc, M, inv_t, kfloor, need_p,
-          [=](float x) { return (unsigned long long)__float2ull_rn(__fmul_rn(expf((x - M) * inv_t), scale)); }, hb);
-    }
+          sh, xs, cand1, cand2, scratch, n_loc, M, inv_t, kfloor, 0ull, (double)top_p,
+          [=](float x) { return (unsigned long long)__float2ull_rn(expf((x - M) * inv_t) * 4294967296.f); }, 1, hb);
   }
   // min_p: x >= x_max + log(min_p), i.e. (l - l_max) / T >= log(min_p)
   for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
@@ -434,6 +579,9 @@ bool g_filter_smem_set[64] = {false};
 // tokens per CTA of a row's cluster (a multiple of 8, so the index array that
 // follows the slice stays 16-byte aligned)
 int filter_slice(int vocab) { return ((vocab + kFCluster - 1) / kFCluster + 7) / 8 * 8; }
+size_t filter_smem(int vocab) {
+  return (size_t)filter_slice(vocab) * sizeof(float) + 2 * kCandCap * sizeof(uint16_t) + kFScratch;
+}
 
 }  // namespace
 
@@ -442,18 +590,12 @@ int launch_filter(const float* logits, float* out, int rows, int vocab, float te
   if (vocab > kFilterMaxVocab) return TV_E_UNSUPPORTED;
   const float inv_t = (float)(1.0 / (double)temperature);
   const float log_min_p = min_p > 0.f ? (float)std::log((double)min_p) : -INFINITY;
-  unsigned long long need_p = 0ull;
-  if (top_p < 1.f) {
-    need_p = (unsigned long long)((double)top_p * 1099511627776.0);
-    if (need_p == 0ull) need_p = 1ull;   // the largest token always stays
-  }
   const int slice = filter_slice(vocab);
-  const size_t smem = (size_t)slice * (sizeof(float) + sizeof(uint16_t));
   // the limit is raised once per device, to what the largest vocabulary needs
-  const int rc = ensure_smem_limit(filter_kernel, (size_t)filter_slice(kFilterMaxVocab) * 6, g_filter_smem_set);
+  const int rc = ensure_smem_limit(filter_kernel, filter_smem(kFilterMaxVocab), g_filter_smem_set);
   if (rc) return rc;
-  return launch_pdl(filter_kernel, dim3(kFCluster, rows), dim3(kFThreads), smem, st, logits, out, vocab, slice,
-                    inv_t, top_k, need_p, log_min_p, (const int32_t*)status);
+  return launch_pdl(filter_kernel, dim3(kFCluster, rows), dim3(kFThreads), filter_smem(vocab), st, logits, out, vocab, slice,
+                    inv_t, top_k, top_p, log_min_p, (const int32_t*)status);
 }
 
 int launch_gumbel_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const SeedTable& sd,

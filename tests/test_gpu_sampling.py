@@ -134,6 +134,16 @@ def test_filter_ties_and_masked_rows(gpu):
             assert np.array_equal(np.isfinite(g[0]), logits[0] == logits[0].max())
 
 
+def test_filter_signed_zero_ties(gpu):
+    """-0.0 and +0.0 compare equal, so both stay when they tie at the boundary"""
+    V = 4096
+    logits = np.full((1, V), -5.0, np.float32)
+    logits[0, :3] = [3.0, 2.0, 1.0]
+    logits[0, 10] = 0.0
+    logits[0, 20] = -0.0
+    g = _filter_check(logits, 1.0, 4, 1.0, 0.0)
+    assert np.isfinite(g[0, 10]) and np.isfinite(g[0, 20]) and np.isfinite(g[0]).sum() == 5
+
 def test_filter_rejects_bad_arguments(gpu):
     x = torch.zeros(2, 16, device="cuda")
     out = torch.empty_like(x)
