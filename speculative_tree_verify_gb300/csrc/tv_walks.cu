@@ -138,16 +138,20 @@ __device__ __forceinline__ T warp_incl_scan(T v) {
 }
 
 // The row max M and Z = sum over the row of exp((l - M) / T), from the row's
-// chunk statistics; one warp, the same arithmetic in every kernel that needs them.
+// chunk statistics.  One warp (lanes stride over the chunks, then a butterfly
+// sum), explicit roundings: every kernel that needs a row's M and Z calls this
+// with a whole warp and gets the same bits.
 __device__ __forceinline__ void row_mz(const RowStat* st, int nvc, float inv_t, float& M, double& Z) {
   const int lane = threadIdx.x & 31;
   float m = -INFINITY;
   for (int c = lane; c < nvc; c += 32) m = fmaxf(m, st[c].m);
   m = warp_max(m);
   double z = 0.0;
-  for (int c = lane; c < nvc; c += 32) z += (double)st[c].s * (double)chunk_scale(st[c].m, m, inv_t);
-  Z = warp_sum_d(z);
+  for (int c = lane; c < nvc; c += 32) z = __dadd_rn(z, __dmul_rn((double)st[c].s, (double)chunk_scale(st[c].m, m, inv_t)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z = __dadd_rn(z, __shfl_xor_sync(FULL, z, o));
   M = m;
+  Z = z;
 }
 
 // p = softmax(l / T) over a row with the tokens rej[0 .. nrej) removed
@@ -284,17 +288,24 @@ __device__ int cdf_draw(const Row& R, int nvc, double target) {
   return chunk * kVChunk;   // the chunk's statistics said mass, its tokens said none
 }
 
-// residual walk, pass 2: one warp per request
-__global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, float inv_t, const float* uniforms,
-                                       int bonus_at_leaf, const RowStat* stats, int nvc, int32_t* path,
-                                       int32_t* accept_len, int32_t* out_tokens, int32_t* out_count,
-                                       int32_t* status) {
+// residual walk, pass 2: one CTA of 32 warps per request; warp w forms row w's
+// M and Z, then warp 0 walks
+__global__ void __launch_bounds__(1024) accept_residual_kernel(ReqTable t, const float* logits, int V, float inv_t,
+                                                               const float* uniforms, int bonus_at_leaf,
+                                                               const RowStat* stats, int nvc, int32_t* path,
+                                                               int32_t* accept_len, int32_t* out_tokens,
+                                                               int32_t* out_count, int32_t* status) {
   __shared__ int s_rej[32];
-  const int r = blockIdx.x, lane = threadIdx.x;
+  __shared__ float s_M[32];
+  __shared__ double s_Z[32];
+  const int r = blockIdx.x, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   pdl_wait();
   pdl_trigger();
   if (status_get(status) != 0) return;
   const int n = t.n[r], row0 = t.row_off[r];
+  if (wid < n) row_mz(stats + (size_t)(row0 + wid) * nvc, nvc, inv_t, s_M[wid], s_Z[wid]);
+  __syncthreads();
+  if (wid != 0) return;
   int par, tok;
   const int err = validate_tree_warp(t.parent[r], t.token[r], n, V, par, tok);
   if (err != TV_OK) {
@@ -313,9 +324,8 @@ __global__ void accept_residual_kernel(ReqTable t, const float* logits, int V, f
   for (;;) {
     const float* lr = logits + (size_t)(row0 + cur) * V;
     const RowStat* st = stats + (size_t)(row0 + cur) * nvc;
-    float M;
-    double Z;
-    row_mz(st, nvc, inv_t, M, Z);
+    const float M = s_M[cur];
+    const double Z = s_Z[cur];
 
     // candidates: the children of cur, in increasing node index
     unsigned kids = __ballot_sync(FULL, lane > 0 && lane < n && par == cur);
@@ -414,6 +424,16 @@ __global__ void __launch_bounds__(256) rej_stats_kernel(ReqTable t, const float*
   if (row == t.row_off[r]) return;   // the root carries no draft
   const int prow = row - 1;           // a chain: the parent's row is the previous row
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* lp = logits + (size_t)prow * V;
+  const float* qr = proposals + (size_t)row * V;
+  const int yw = c * kVChunk + w * (4 * kVSeg);
+  float lv[16], qv[16];   // loads in flight while warp 0 forms the row statistics
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int y = yw + j * 32 + lane;
+    lv[j] = y < V ? lp[y] : -INFINITY;
+    qv[j] = y < V ? qr[y] : 0.f;
+  }
   if (w == 0) {
     float M;
     double Z;
@@ -425,21 +445,15 @@ __global__ void __launch_bounds__(256) rej_stats_kernel(ReqTable t, const float*
   }
   __syncthreads();
   const float M = s_M, izf = s_izf;
-  const float* lp = logits + (size_t)prow * V;
-  const float* qr = proposals + (size_t)row * V;
-  const int yw = c * kVChunk + w * (4 * kVSeg);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float qs = 0.f;
   int bad = 0;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const int y = yw + j * 32 + lane;
-    if (y < V) {
-      const float q = qr[y];
-      if (!(q >= 0.f) || isinf(q)) bad = 1;
-      acc[j >> 2] += resid_term(lp[y], q, M, inv_t, izf);
-      qs += q;
-    }
+    const float q = qv[j];
+    if (!(q >= 0.f) || isinf(q)) bad = 1;
+    acc[j >> 2] += resid_term(lv[j], q, M, inv_t, izf);
+    qs += q;
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -469,16 +483,46 @@ __global__ void __launch_bounds__(256) rej_stats_kernel(ReqTable t, const float*
   }
 }
 
-// Pass 3, one warp per request: validate, then test the drafts in order.
-__global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, float inv_t, const float* proposals,
-                                        const float* uniforms, const RowStat* stats, const RejStat* rstats, int nvc,
-                                        int32_t* path, int32_t* accept_len, int32_t* out_tokens,
-                                        int32_t* out_count, int32_t* status) {
-  const int r = blockIdx.x, lane = threadIdx.x;
+// Pass 3, one CTA of 32 warps per request: warp w forms row w's M and Z and
+// checks node w's proposal row; warp 0 validates, then tests the drafts in order.
+__global__ void __launch_bounds__(1024) accept_rejection_kernel(ReqTable t, const float* logits, int V, float inv_t,
+                                                                const float* proposals, const float* uniforms,
+                                                                const RowStat* stats, const RejStat* rstats, int nvc,
+                                                                int32_t* path, int32_t* accept_len,
+                                                                int32_t* out_tokens, int32_t* out_count,
+                                                                int32_t* status) {
+  __shared__ float s_M[32];
+  __shared__ double s_Z[32];
+  __shared__ int s_bad[32];
+  const int r = blockIdx.x, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   pdl_wait();
   pdl_trigger();
   if (status_get(status) != 0) return;
   const int n = t.n[r], row0 = t.row_off[r];
+  // proposal row of node w >= 1: finite, nonnegative, unit mass (|sum - 1| <=
+  // 1e-3), and q(x) > 0 at the draft, which was drawn from q
+  if (wid < n) {
+    row_mz(stats + (size_t)(row0 + wid) * nvc, nvc, inv_t, s_M[wid], s_Z[wid]);
+    int bad = 0;
+    if (wid >= 1) {
+      const RejStat* rs = rstats + (size_t)(row0 + wid) * nvc;
+      double qs = 0.0;
+      int fl = 0;
+      for (int c = lane; c < nvc; c += 32) {
+        qs += (double)rs[c].qsum;
+        fl |= rs[c].bad;
+      }
+      qs = warp_sum_d(qs);
+      fl = __any_sync(FULL, fl);
+      int x = t.token[r][wid];
+      x = x < 0 ? 0 : (x >= V ? V - 1 : x);   // a token out of range is reported by the tree check
+      const float qx = proposals[(size_t)(row0 + wid) * V + x];
+      bad = (fl || fabs(qs - 1.0) > 1e-3 || !(qx > 0.f)) ? 1 : 0;
+    }
+    if (lane == 0) s_bad[wid] = bad;
+  }
+  __syncthreads();
+  if (wid != 0) return;
   int par, tok;
   const int err = validate_tree_warp(t.parent[r], t.token[r], n, V, par, tok);
   if (err != TV_OK) {
@@ -494,24 +538,7 @@ __global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, 
     if (lane == 0) status_set(status, TV_E_UNIFORM);
     return;
   }
-  // proposal rows of nodes 1..n-1: finite, nonnegative, unit mass (|sum - 1| <= 1e-3),
-  // and q(x) > 0 at the draft, which was drawn from q
-  bool bad = false;
-  for (int i = 1; i < n; ++i) {
-    const RejStat* rs = rstats + (size_t)(row0 + i) * nvc;
-    double qs = 0.0;
-    int fl = 0;
-    for (int c = lane; c < nvc; c += 32) {
-      qs += (double)rs[c].qsum;
-      fl |= rs[c].bad;
-    }
-    qs = warp_sum_d(qs);
-    fl = __any_sync(FULL, fl);
-    const int x = __shfl_sync(FULL, tok, i);
-    const float qx = proposals[(size_t)(row0 + i) * V + x];
-    if (fl || fabs(qs - 1.0) > 1e-3 || !(qx > 0.f)) bad = true;
-  }
-  if (bad) {
+  if (__any_sync(FULL, lane < n && s_bad[lane] != 0)) {
     if (lane == 0) status_set(status, TV_E_PROPOSAL);
     return;
   }
@@ -519,9 +546,8 @@ __global__ void accept_rejection_kernel(ReqTable t, const float* logits, int V, 
   if (lane == 0) path[row0] = 0;
   for (int i = 1; i < n; ++i) {
     const int prow = row0 + i - 1;
-    float M;
-    double Z;
-    row_mz(stats + (size_t)prow * nvc, nvc, inv_t, M, Z);
+    const float M = s_M[i - 1];
+    const double Z = s_Z[i - 1];
     const float* lp = logits + (size_t)prow * V;
     const float* qr = proposals + (size_t)(row0 + i) * V;
     const int x = __shfl_sync(FULL, tok, i);
@@ -617,7 +643,7 @@ int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, fl
   const int rc = launch_pdl(row_stats_kernel, dim3(nvc, t.total_rows), dim3(256), 0, st, logits, vocab, inv_t, nvc,
                             stats, (const int32_t*)status);
   if (rc) return rc;
-  return launch_pdl(accept_residual_kernel, dim3(t.n_req), dim3(32), 0, st, t, logits, vocab, inv_t, uniforms,
+  return launch_pdl(accept_residual_kernel, dim3(t.n_req), dim3(1024), 0, st, t, logits, vocab, inv_t, uniforms,
                     bonus_at_leaf, (const RowStat*)stats, nvc, path, accept_len, out_tokens, out_count, status);
 }
 
@@ -644,7 +670,7 @@ int launch_accept_rejection(const ReqTable& t, const float* logits, int vocab, f
   rc = launch_pdl(rej_stats_kernel, dim3(nvc, t.total_rows), dim3(256), 0, st, t, logits, vocab, inv_t, proposals,
                   (const RowStat*)stats, nvc, rstats, (const int32_t*)status);
   if (rc) return rc;
-  return launch_pdl(accept_rejection_kernel, dim3(t.n_req), dim3(32), 0, st, t, logits, vocab, inv_t, proposals,
+  return launch_pdl(accept_rejection_kernel, dim3(t.n_req), dim3(1024), 0, st, t, logits, vocab, inv_t, proposals,
                     uniforms, (const RowStat*)stats, (const RejStat*)rstats, nvc, path, accept_len, out_tokens,
                     out_count, status);
 }
