@@ -365,6 +365,69 @@ TV_API int tv_accept_rejection(const tv_tree *trees, int n_req, const float *log
 TV_API int tv_profile_start(int max_calls);
 TV_API int tv_profile_stop(float *stage_ms, int max_stages, int *n_stages, int *n_calls);
 
+/*
+ * Gated DeltaNet tree verify [Drafters and tree verify, §Tree verify through
+ * recurrent layers].  The recurrent core of one Gated DeltaNet layer over a
+ * draft tree: per value head the state S is a d_k x d_v fp32 matrix (keys to
+ * values) and one step of the gated delta rule is
+ *     S <- exp(g) (I - beta k k^T) S + beta k v^T,   o = S^T q.
+ * The state after node t is the state after t's parent updated by t; the
+ * state before the root is the layer's state before the round.  Value head h
+ * reads key head h / (n_v_heads / n_k_heads).  The inputs are the layer's
+ * per-node q, k (already normalised and scaled), v, beta in (0, 1) and
+ * g <= 0 (log decay); projections and the short convolution are the caller's.
+ *
+ * tv_dn_verify_tree writes every node's output o_t = S_t^T q_t, and, for the
+ * commit, the node's pseudo-value u_t and cumulative gate gc_t (the sum of g
+ * over its root path), with which the state after any root path ending at t is
+ *     exp(gc_t) S0 + sum over s on the path of exp(gc_t - gc_s) k_s u_s^T.
+ *
+ *   dims        host: n_k_heads >= 1, n_v_heads a multiple of it, d_k and d_v
+ *               multiples of 32 up to 128 (else TV_E_UNSUPPORTED)
+ *   trees       host array [n_req], as for tv_verify_tree (tokens are checked
+ *               only for duplicate siblings)
+ *   states      host array [n_req] of device pointers, 16-byte aligned: the
+ *               layer's state of each request, fp32 [n_v_heads][d_k][d_v];
+ *               read only
+ *   q, k        device fp32 [total_rows][n_k_heads][d_k]
+ *   v           device fp32 [total_rows][n_v_heads][d_v]
+ *   beta, g     device fp32 [total_rows][n_v_heads]
+ *   o, u        device fp32 [total_rows][n_v_heads][d_v]
+ *   gc          device fp32 [total_rows][n_v_heads]
+ * Host checks: TV_E_ARG (null or misaligned pointers), TV_E_ROWS,
+ * TV_E_UNSUPPORTED.  Device checks: the tree rules.
+ */
+typedef struct {
+    int32_t n_k_heads, n_v_heads, d_k, d_v;
+} tv_dn_dims;
+
+TV_API int tv_dn_verify_tree(const tv_dn_dims *dims, const tv_tree *trees, int n_req, float *const *states,
+                             const float *q, const float *k, const float *v, const float *beta, const float *g,
+                             float *o, float *u, float *gc, int32_t *dev_status, void *stream);
+
+/*
+ * Path-state commit of the Gated DeltaNet layers [Drafters and tree verify,
+ * §Tree verify through recurrent layers]: for every layer and value head,
+ *     S <- exp(gc_last) S + sum_{d = 0..a} exp(gc_last - gc_{p_d}) k_{p_d} u_{p_d}^T
+ * over the accepted root path p_0 = 0, ..., p_a (gc_last = gc_{p_a}), i.e. the
+ * state after the path's last node.  One read and one write of the state, no
+ * weights.  A chain rolled back to its first m nodes is the path 0..m-1.
+ *
+ *   n_layers    host >= 1: layers committed in one call
+ *   states      host array [n_req] of device pointers, 16-byte aligned: fp32
+ *               [n_layers][n_v_heads][d_k][d_v], updated in place
+ *   k           device fp32 [n_layers][total_rows][n_k_heads][d_k]
+ *   u           device fp32 [n_layers][total_rows][n_v_heads][d_v]
+ *   gc          device fp32 [n_layers][total_rows][n_v_heads]
+ *               (u and gc as tv_dn_verify_tree wrote them, layer by layer)
+ *   path, accept_len  device, from an accept walk
+ * Host checks: as tv_dn_verify_tree.  Device checks: TV_E_PATH (a_r outside
+ * 0..n_r - 1, path[0] != 0, or path[d] not a child of path[d - 1]).
+ */
+TV_API int tv_dn_commit(const tv_dn_dims *dims, const tv_tree *trees, int n_req, int n_layers, float *const *states,
+                        const float *k, const float *u, const float *gc, const int32_t *path,
+                        const int32_t *accept_len, int32_t *dev_status, void *stream);
+
 /* A short English name of a status code (static storage). */
 TV_API const char *tv_status_string(int code);
 

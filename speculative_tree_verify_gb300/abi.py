@@ -28,7 +28,7 @@ CODES = {v: k for k, v in STATUS.items()}
 SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv",
            "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc",
            "tv_sample_workspace_size", "tv_sample_filter", "tv_accept_single_draw", "tv_accept_gumbel",
-           "tv_accept_rejection")
+           "tv_accept_rejection", "tv_dn_verify_tree", "tv_dn_commit")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -51,6 +51,11 @@ class TvKv(ctypes.Structure):
 
 class TvTree(ctypes.Structure):
     _fields_ = [("parent", ctypes.c_void_p), ("token", ctypes.c_void_p), ("n", ctypes.c_int32)]
+
+
+class TvDnDims(ctypes.Structure):
+    _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32)]
 
 
 _lib = None
@@ -91,6 +96,10 @@ def load():
                                          P, P, P, Z, P]
         lib.tv_accept_rejection.argtypes = [ctypes.POINTER(TvTree), I, P, ctypes.c_int32, ctypes.c_float, P, P,
                                             P, P, P, P, P, P, Z, P]
+        lib.tv_dn_verify_tree.argtypes = [ctypes.POINTER(TvDnDims), ctypes.POINTER(TvTree), I, ctypes.POINTER(P), P,
+                                          P, P, P, P, P, P, P, P, P]
+        lib.tv_dn_commit.argtypes = [ctypes.POINTER(TvDnDims), ctypes.POINTER(TvTree), I, I, ctypes.POINTER(P), P, P,
+                                     P, P, P, P, P]
         lib.tv_status_string.argtypes = [I]
         lib.tv_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -200,6 +209,23 @@ def tv_accept_rejection(trees: Sequence[TvTree], logits, vocab: int, temperature
                                       _p(proposals), _p(uniforms), _p(path), _p(accept_len), _p(out_tokens),
                                       _p(out_count), _p(dev_status), _p(workspace), int(workspace_bytes),
                                       _stream(stream))
+
+
+def _ptrs(states):
+    return (ctypes.c_void_p * len(states))(*[_p(x) for x in states])
+
+
+def tv_dn_verify_tree(dims: TvDnDims, trees: Sequence[TvTree], states, q, k, v, beta, g, o, u, gc, dev_status,
+                      stream=None) -> int:
+    """states: one device buffer (tensor or address) per request."""
+    return load().tv_dn_verify_tree(ctypes.byref(dims), _arr(TvTree, trees), len(trees), _ptrs(states), _p(q), _p(k),
+                                    _p(v), _p(beta), _p(g), _p(o), _p(u), _p(gc), _p(dev_status), _stream(stream))
+
+
+def tv_dn_commit(dims: TvDnDims, trees: Sequence[TvTree], n_layers: int, states, k, u, gc, path, accept_len,
+                 dev_status, stream=None) -> int:
+    return load().tv_dn_commit(ctypes.byref(dims), _arr(TvTree, trees), len(trees), int(n_layers), _ptrs(states),
+                               _p(k), _p(u), _p(gc), _p(path), _p(accept_len), _p(dev_status), _stream(stream))
 
 
 def tv_commit_kv(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], path, accept_len, committed_src,

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtv.so")
-SOURCES = ["tv_api.cu", "tv_gemm.cu", "tv_layer.cu", "tv_attn.cu", "tv_walks.cu", "tv_noalloc.cu", "tv_sample.cu"]
+SOURCES = ["tv_api.cu", "tv_gemm.cu", "tv_layer.cu", "tv_attn.cu", "tv_walks.cu", "tv_noalloc.cu", "tv_sample.cu",
+           "tv_deltanet.cu"]
 HEADERS = ["tv_common.cuh", "tv_gemm.cuh", "tv_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

@@ -342,6 +342,54 @@ int tv_accept_rejection(const tv_tree* trees, int n_req, const float* logits, in
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---- Gated DeltaNet -----------------------------------------------------------------
+namespace {
+int dn_check(const tv_dn_dims* d) {
+  if (!d) return TV_E_ARG;
+  if (d->n_k_heads < 1 || d->n_v_heads < 1 || d->n_v_heads % d->n_k_heads != 0) return TV_E_UNSUPPORTED;
+  auto ok = [](int x) { return x >= 32 && x <= kDnMaxDim && x % 32 == 0; };
+  if (!ok(d->d_k) || !ok(d->d_v)) return TV_E_UNSUPPORTED;
+  return TV_OK;
+}
+int dn_states(DnStates& st, float* const* states, int n_req) {
+  if (!states) return TV_E_ARG;
+  memset(&st, 0, sizeof(st));
+  for (int r = 0; r < n_req; ++r) {
+    if (!states[r] || !aligned16(states[r])) return TV_E_ARG;
+    st.S[r] = states[r];
+  }
+  return TV_OK;
+}
+}  // namespace
+
+int tv_dn_verify_tree(const tv_dn_dims* dims, const tv_tree* trees, int n_req, float* const* states, const float* q,
+                      const float* k, const float* v, const float* beta, const float* g, float* o, float* u,
+                      float* gc, int32_t* dev_status, void* stream) {
+  int rc = dn_check(dims);
+  if (rc) return rc;
+  if (!q || !k || !v || !beta || !g || !o || !u || !gc || !dev_status) return TV_E_ARG;
+  ReqTable t;
+  if ((rc = build_table(t, trees, nullptr, n_req, true))) return rc;
+  DnStates st;
+  if ((rc = dn_states(st, states, n_req))) return rc;
+  return launch_dn_verify(t, st, dims->n_k_heads, dims->n_v_heads, dims->d_k, dims->d_v, q, k, v, beta, g, o, u, gc,
+                          dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int tv_dn_commit(const tv_dn_dims* dims, const tv_tree* trees, int n_req, int n_layers, float* const* states,
+                 const float* k, const float* u, const float* gc, const int32_t* path, const int32_t* accept_len,
+                 int32_t* dev_status, void* stream) {
+  int rc = dn_check(dims);
+  if (rc) return rc;
+  if (n_layers < 1 || !k || !u || !gc || !path || !accept_len || !dev_status) return TV_E_ARG;
+  ReqTable t;
+  if ((rc = build_table(t, trees, nullptr, n_req, true))) return rc;
+  DnStates st;
+  if ((rc = dn_states(st, states, n_req))) return rc;
+  return launch_dn_commit(t, st, dims->n_k_heads, dims->n_v_heads, dims->d_k, dims->d_v, n_layers, k, u, gc, path,
+                          accept_len, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int tv_commit_kv(const tv_kv* kv, const tv_dims* dims, const tv_tree* trees, int n_req, const int32_t* path,
                  const int32_t* accept_len, int32_t* committed_src, int32_t* new_ctx, int32_t* dev_status,
                  void* stream) {

@@ -64,6 +64,12 @@ struct RejStat {               // a vocabulary chunk of a draft's proposal row
   int pad;
 };
 
+// ---- Gated DeltaNet --------------------------------------------------------------
+constexpr int kDnMaxDim = 128;   // d_k, d_v: multiples of 32 up to this
+struct DnStates {                // per request: the layer's state, [H_v][d_k][d_v] fp32 (per layer for the commit)
+  float* S[kMaxReq];
+};
+
 // ---- block-uniform status check -------------------------------------------
 __device__ __forceinline__ bool block_skip(const int32_t* status) {
   __shared__ int s_stat;
@@ -144,6 +150,12 @@ int launch_gumbel_rows(const ReqTable& t, const float* logits, int vocab, float 
                        GumbelPart* part, int32_t* row_tokens, int32_t* status, cudaStream_t st);
 int launch_draw_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const float* uniforms,
                      RowStat* stats, int32_t* row_tokens, int32_t* status, cudaStream_t st);
+int launch_dn_verify(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, const float* q,
+                     const float* k, const float* v, const float* beta, const float* g, float* o, float* u, float* gc,
+                     int32_t* status, cudaStream_t s);
+int launch_dn_commit(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, int n_layers,
+                     const float* k, const float* u, const float* gc, const int32_t* path, const int32_t* accept_len,
+                     int32_t* status, cudaStream_t s);
 int launch_accept_rejection(const ReqTable& t, const float* logits, int vocab, float temperature,
                             const float* proposals, const float* uniforms, RowStat* stats, RejStat* rstats,
                             int32_t* path, int32_t* accept_len, int32_t* out_tokens, int32_t* out_count,

@@ -226,6 +226,34 @@ def logits_rows(n: int, vocab: int, seed: int, scale: float = 1.5) -> np.ndarray
 
 
 @dataclass
+class DnInputs:
+    q: np.ndarray      # [n][H_k][d_k] fp32, unit length / sqrt(d_k)
+    k: np.ndarray      # [n][H_k][d_k] fp32, unit length
+    v: np.ndarray      # [n][H_v][d_v] fp32 ~ N(0, 1)
+    beta: np.ndarray   # [n][H_v] fp32 in (0.05, 0.95)
+    g: np.ndarray      # [n][H_v] fp32 in (-0.4, -0.001)
+    S0: np.ndarray     # [H_v][d_k][d_v] fp32 ~ N(0, 0.3^2)
+
+
+def dn_inputs(n: int, n_k_heads: int, n_v_heads: int, d_k: int, d_v: int, seed: int) -> DnInputs:
+    """Per-node inputs of one Gated DeltaNet layer's recurrent core and the
+    state before the round, as fp32.  Keys and queries are unit vectors (the
+    layer normalises them), queries scaled by 1/sqrt(d_k); write strengths and
+    log decays span the ranges a sigmoid and a negative softplus give."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = rng.standard_normal((n, n_k_heads, d_k))
+    q /= np.linalg.norm(q, axis=2, keepdims=True) * np.sqrt(d_k)
+    k = rng.standard_normal((n, n_k_heads, d_k))
+    k /= np.linalg.norm(k, axis=2, keepdims=True)
+    v = rng.standard_normal((n, n_v_heads, d_v))
+    beta = rng.uniform(0.05, 0.95, (n, n_v_heads))
+    g = -rng.uniform(0.001, 0.4, (n, n_v_heads))
+    S0 = rng.standard_normal((n_v_heads, d_k, d_v)) * 0.3
+    f = lambda a: np.ascontiguousarray(a, dtype=np.float32)
+    return DnInputs(f(q), f(k), f(v), f(beta), f(g), f(S0))
+
+
+@dataclass
 class Request:
     tree: Tree
     cache: Cache

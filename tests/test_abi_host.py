@@ -151,6 +151,25 @@ def test_sampled_host_checks(lib):
                                    16) == abi.CODES["TV_E_WORKSPACE"]
 
 
+def test_deltanet_host_checks(lib):
+    trees = [_tree(8)]
+    ok = abi.TvDnDims(2, 4, 128, 128)
+    args = (FAKE,) * 9   # q, k, v, beta, g, o, u, gc, dev_status
+    call = lambda dims, trees=trees, states=(FAKE,): abi.tv_dn_verify_tree(dims, trees, list(states) * len(trees),
+                                                                           *args[:9])
+    for bad in (abi.TvDnDims(3, 4, 128, 128), abi.TvDnDims(0, 4, 128, 128), abi.TvDnDims(2, 4, 48, 128),
+                abi.TvDnDims(2, 4, 128, 160), abi.TvDnDims(2, 4, 0, 128)):
+        assert call(bad) == abi.CODES["TV_E_UNSUPPORTED"]
+    assert call(ok, states=(FAKE + 4,)) == abi.CODES["TV_E_ARG"]          # misaligned state
+    assert call(ok, trees=[_tree(40)]) == abi.CODES["TV_E_ROWS"]
+    assert call(ok, trees=[_tree(20), _tree(20)]) == abi.CODES["TV_E_ROWS"]
+    assert abi.tv_dn_verify_tree(ok, trees, [FAKE], None, *args[:8]) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_dn_commit(ok, trees, 0, [FAKE], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_dn_commit(abi.TvDnDims(2, 4, 96, 72), trees, 1, [FAKE], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE) == \
+        abi.CODES["TV_E_UNSUPPORTED"]
+    assert abi.tv_dn_commit(ok, trees, 1, [FAKE], FAKE, FAKE, FAKE, None, FAKE, FAKE) == abi.CODES["TV_E_ARG"]
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(abi, "_lib", None)
     monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "missing.so"))
