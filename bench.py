@@ -11,7 +11,8 @@ timing) so the walk and the commit do real work.  Inputs are synthetic.
 Printed: one JSON line (rank 0).  value = ms per round from CUDA-graph replay
 (the served configuration keeps verify in graphs); the eager number, the row
 sweep 8/16/24/32, a sampled round (residual walk), the sampled variants (filter,
-single-draw, Gumbel and rejection walks alone and in rounds), per-stage times, the
+single-draw, Gumbel and rejection walks alone and in rounds), the Gated DeltaNet
+recurrent core of 48 layers and their path-state commit, per-stage times, the
 roofline of the LM head kernel, end-to-end latency with host buffers, clocks
 and the CPU oracle baseline ride along.
 
@@ -481,6 +482,62 @@ def run_ours(args, world, rank, local):
         ok_status(name)
     out["sampled_variants"] = sv
     del sb, prop, chain
+
+    # ---- Gated DeltaNet: the recurrent core of 48 layers over the round's tree
+    #      (one launch per layer, each on its own state) and the path-state
+    #      commit of all 48 layers in one launch; 16 key / 32 value heads of 128 ----
+    Hk, Hv, dkn, dvn, NL = 16, 32, 128, 128, 48
+    dnd = abi.TvDnDims(Hk, Hv, dkn, dvn)
+    dni = synth.dn_inputs(rows, Hk, Hv, dkn, dvn, 808)
+    dq, dk_, dv_ = (torch.from_numpy(x).to(dev) for x in (dni.q, dni.k, dni.v))
+    dbeta, dg = torch.from_numpy(dni.beta).to(dev), torch.from_numpy(dni.g).to(dev)
+    gs = torch.Generator(device=dev)
+    gs.manual_seed(909)
+    dstate = torch.randn(NL, Hv, dkn, dvn, device=dev, generator=gs) * 0.3
+    do_ = torch.empty(rows, Hv, dvn, device=dev)
+    du = torch.empty(NL, rows, Hv, dvn, device=dev)
+    dgc = torch.empty(NL, rows, Hv, device=dev)
+    dks = dk_.unsqueeze(0).expand(NL, -1, -1, -1).contiguous()
+    ptr0 = dstate.data_ptr()
+    lbytes = Hv * dkn * dvn * 4
+
+    def dn_layers():
+        for l in range(NL):
+            dv.check(abi.tv_dn_verify_tree(dnd, [req.tree()], [ptr0 + l * lbytes], dq, dk_, dv_, dbeta, dg, do_,
+                                           du[l], dgc[l], b.status, stream=cur()), "tv_dn_verify_tree")
+
+    def dn_commit():
+        dv.check(abi.tv_dn_commit(dnd, [req.tree()], NL, [dstate], dks, du, dgc, b.path, b.accept_len, b.status,
+                                  stream=cur()), "tv_dn_commit")
+
+    round_()   # the greedy path of the round's tree
+    gw = _graph(dn_layers)
+    dn_v_us = 1e3 * _time_graph(gw, 100)
+    del gw
+    ok_status("dn verify")
+    gw = _graph(dn_commit)
+    reps = 200
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        gw.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    dn_c_us = 1e3 * e0.elapsed_time(e1) / reps
+    del gw
+    ok_status("dn commit")
+    a_len = int(b.accept_len[0])
+    cbytes = 2 * NL * lbytes + NL * (a_len + 1) * (Hk * dkn + Hv * dvn + Hv) * 4
+    out["deltanet"] = {
+        "dims": {"key_heads": Hk, "value_heads": Hv, "d_k": dkn, "d_v": dvn, "layers": NL, "rows": rows},
+        "verify_48_layers_us": round(dn_v_us, 2), "verify_per_layer_us": round(dn_v_us / NL, 2),
+        "verify_state_bytes_per_layer": lbytes,
+        "commit_48_layers_us": round(dn_c_us, 2), "commit_accept_len": a_len,
+        "commit_algorithmic_bytes": cbytes,
+        "commit_GB_per_s": round(cbytes / dn_c_us / 1e3, 1),
+        "commit_frac_of_peak": round(cbytes / dn_c_us / 1e3 / peak, 4)}
+    del dstate, du, dgc, dks
 
     # ---- end to end through the C ABI with host buffers --------------------------
     par_h = torch.from_numpy(req.parent.cpu().numpy()).pin_memory()

@@ -22,8 +22,8 @@
 //    request); every product in fp32 from shared memory, the triangular solve
 //    by forward substitution in node order (parents come first).
 //  - dn_commit_kernel: one CTA per (value head, layer, request); the whole
-//    d_k x d_v state is read, updated in place and written (HBM-bound: the
-//    state is the only large operand).
+//    d_k x d_v state comes in by one TMA bulk copy, is updated and written
+//    back in place (HBM-bound: the state is the only large operand).
 #include "tv_common.cuh"
 #include "tv_kernels.cuh"
 
@@ -35,25 +35,25 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int kDnCols = 32;        // value columns per verify CTA
 constexpr int kDnThreads = 256;    // verify CTA
 constexpr int kDnCommitThreads = 512;
-constexpr int kNodeStride = kMaxRows + 1;   // K^T / Q^T row stride: stores along d_k hit distinct banks
+constexpr int kNodeStride = kMaxRows + 4;   // K^T / Q^T row stride: 16-byte rows, staging stores spread over banks
 
 // dynamic shared memory of the verify CTA, in floats
 struct DnVerifyLayout {
-  int kt, qt, s0, vb, ks, qs, u, kk, qk, a, total;
+  int kt, qt, s0, vb, ks, qs, u, kk, c, a, total;
 };
 __host__ __device__ inline DnVerifyLayout dn_verify_layout(int dk) {
   DnVerifyLayout L;
   int o = 0;
-  L.kt = o; o += dk * kNodeStride;       // K^T of the key head: [d_k][32 nodes + 1]
+  L.kt = o; o += dk * kNodeStride;       // K^T of the key head: [d_k][32 nodes + 4]
   L.qt = o; o += dk * kNodeStride;       // Q^T
   L.s0 = o; o += dk * kDnCols;           // S0[:, column block]
   L.vb = o; o += kMaxRows * kDnCols;     // v[:, column block]
-  L.ks = o; o += kMaxRows * kDnCols;     // K S0 (then the right-hand side)
+  L.ks = o; o += kMaxRows * kDnCols;     // K S0, then the right-hand side
   L.qs = o; o += kMaxRows * kDnCols;     // Q S0
-  L.u = o; o += kMaxRows * kDnCols;      // pseudo-values
+  L.u = o; o += kMaxRows * kDnCols;      // pseudo-values (first: partial products)
   L.kk = o; o += kMaxRows * kMaxRows;    // k_t . k_s
-  L.qk = o; o += kMaxRows * kMaxRows;    // q_t . k_s
-  L.a = o; o += kMaxRows * kMaxRows;     // beta_t exp(gc_t - gc_s) (k_t . k_s), s a strict ancestor of t
+  L.c = o; o += kMaxRows * kMaxRows;     // q_t . k_s, then exp(gc_t - gc_s) (q_t . k_s) on t's path
+  L.a = o; o += kMaxRows * kMaxRows;     // beta_t exp(gc_t - gc_s) (k_t . k_s), s a strict ancestor (first: partials)
   L.total = o;
   return L;
 }
@@ -75,15 +75,54 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const DnVerifyLayout L = dn_verify_layout(dk);
   float *KT = dsm + L.kt, *QT = dsm + L.qt, *S0 = dsm + L.s0, *VB = dsm + L.vb, *KS = dsm + L.ks, *QS = dsm + L.qs,
-        *U = dsm + L.u, *KK = dsm + L.kk, *QK = dsm + L.qk, *A = dsm + L.a;
+        *U = dsm + L.u, *KK = dsm + L.kk, *C = dsm + L.c, *A = dsm + L.a;
+
+  // the loads on the critical path first (warp 0: the tree and the node gates),
+  // then every other load of the CTA, into registers
+  int par = 0, tok = 0;
+  float gl = 0.f, bl = 0.f;
+  if (warp == 0 && lane < n) {
+    par = t.parent[r][lane];
+    tok = t.token[r][lane];
+    gl = g[(size_t)(row0 + lane) * Hv + h];
+    bl = beta[(size_t)(row0 + lane) * Hv + h];
+  }
+  const int c0 = cb * kDnCols;
+  constexpr int kKQ = kMaxRows * kDnMaxDim / kDnThreads;   // 16
+  constexpr int kSB = kDnMaxDim * kDnCols / kDnThreads;    // 16
+  constexpr int kVB = kMaxRows * kDnCols / kDnThreads;     // 4
+  float kreg[kKQ], qreg[kKQ], sreg[kSB], vreg[kVB];
+  const float* S0g = st.S[r] + (size_t)h * dk * dv;
+#pragma unroll
+  for (int m = 0; m < kKQ; ++m) {
+    const int idx = threadIdx.x + m * kDnThreads;
+    const int s = idx / dk, i = idx - s * dk;   // node s, coordinate i (coalesced along i)
+    kreg[m] = 0.f;
+    qreg[m] = 0.f;
+    if (idx < kMaxRows * dk && s < n) {
+      const size_t off = ((size_t)(row0 + s) * Hk + kh) * dk + i;
+      kreg[m] = k[off];
+      qreg[m] = q[off];
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kSB; ++m) {
+    const int idx = threadIdx.x + m * kDnThreads;
+    const int i = idx / kDnCols, j = idx - i * kDnCols;
+    sreg[m] = idx < dk * kDnCols ? S0g[(size_t)i * dv + c0 + j] : 0.f;
+  }
+#pragma unroll
+  for (int m = 0; m < kVB; ++m) {
+    const int idx = threadIdx.x + m * kDnThreads;
+    const int s = idx / kDnCols, j = idx - s * kDnCols;
+    vreg[m] = s < n ? v[((size_t)(row0 + s) * Hv + h) * dv + c0 + j] : 0.f;
+  }
 
   if (warp == 0) {   // the tree: parent order; then cumulative gates and root paths
-    int par, tok;
-    const int err = validate_tree_warp(t.parent[r], t.token[r], n, 0, par, tok);
+    const int err = check_tree_warp(par, tok, n, 0);
     if (lane == 0) s_err = err;
     if (err == TV_OK) {
-      const float gl = lane < n ? g[(size_t)(row0 + lane) * Hv + h] : 0.f;
-      if (lane < n) s_beta[lane] = beta[(size_t)(row0 + lane) * Hv + h];
+      if (lane < n) s_beta[lane] = bl;
       // pointer doubling over the parent links: gc = sum of g over the root path
       float acc = gl;
       unsigned anc = lane < n ? (1u << lane) : 0u;
@@ -106,119 +145,168 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
       }
     }
   }
+  // stage K^T, Q^T, S0 and v in shared memory
+#pragma unroll
+  for (int m = 0; m < kKQ; ++m) {
+    const int idx = threadIdx.x + m * kDnThreads;
+    if (idx < kMaxRows * dk) {
+      const int s = idx / dk, i = idx - s * dk;
+      KT[i * kNodeStride + s] = kreg[m];
+      QT[i * kNodeStride + s] = qreg[m];
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kSB; ++m) {
+    const int idx = threadIdx.x + m * kDnThreads;
+    if (idx < dk * kDnCols) S0[idx] = sreg[m];
+  }
+#pragma unroll
+  for (int m = 0; m < kVB; ++m) VB[threadIdx.x + m * kDnThreads] = vreg[m];
   __syncthreads();
   if (s_err != TV_OK) {
     if (threadIdx.x == 0 && h == 0 && cb == 0) status_set(status, s_err);
     return;
   }
-  // stage K^T, Q^T (key head kh), v and S0 column blocks
-  const int c0 = cb * kDnCols;
-  for (int idx = threadIdx.x; idx < kMaxRows * dk; idx += kDnThreads) {
-    const int s = idx / dk, i = idx - s * dk;   // node s, coordinate i (coalesced along i)
-    float kv = 0.f, qv = 0.f;
-    if (s < n) {
-      const size_t off = ((size_t)(row0 + s) * Hk + kh) * dk + i;
-      kv = k[off];
-      qv = q[off];
-    }
-    KT[i * kNodeStride + s] = kv;
-    QT[i * kNodeStride + s] = qv;
-  }
-  const float* S0g = st.S[r] + (size_t)h * dk * dv;
-  for (int idx = threadIdx.x; idx < dk * kDnCols; idx += kDnThreads) {
-    const int i = idx / kDnCols, j = idx - i * kDnCols;
-    S0[idx] = S0g[(size_t)i * dv + c0 + j];
-  }
-  for (int idx = threadIdx.x; idx < kMaxRows * kDnCols; idx += kDnThreads) {
-    const int s = idx / kDnCols, j = idx - s * kDnCols;
-    VB[idx] = s < n ? v[((size_t)(row0 + s) * Hv + h) * dv + c0 + j] : 0.f;
-  }
-  __syncthreads();
-  // K S0, Q S0, K K^T, Q K^T: thread (rows warp + 8m, column lane)
+
+  // K S0, Q S0, K K^T, Q K^T.  A warp takes 4 contiguous rows (one float4 of
+  // K^T and of Q^T per coordinate) and the column lane; with n <= 16 two warps
+  // share a row group, each over half of d_k, and their sums are added.
   {
+    const bool split = n <= 16;
+    const int rg = split ? (warp & 3) : warp;
+    const int half = split ? (warp >> 2) : 0;
+    const int i_lo = split ? half * (dk / 2) : 0, i_hi = split ? i_lo + dk / 2 : dk;
     float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
     float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < dk; ++i) {
-      const float sij = S0[i * kDnCols + lane];
-      const float kis = KT[i * kNodeStride + lane];
+    const bool live = 4 * rg < n;
+    if (live) {
+#pragma unroll 4
+      for (int i = i_lo; i < i_hi; ++i) {
+        const float sij = S0[i * kDnCols + lane];
+        const float kis = KT[i * kNodeStride + lane];
+        const float4 kt4 = *reinterpret_cast<const float4*>(KT + i * kNodeStride + 4 * rg);
+        const float4 qt4 = *reinterpret_cast<const float4*>(QT + i * kNodeStride + 4 * rg);
+        const float kt[4] = {kt4.x, kt4.y, kt4.z, kt4.w}, qt[4] = {qt4.x, qt4.y, qt4.z, qt4.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          ks[m] = fmaf(kt[m], sij, ks[m]);
+          qs[m] = fmaf(qt[m], sij, qs[m]);
+          kk[m] = fmaf(kt[m], kis, kk[m]);
+          qk[m] = fmaf(qt[m], kis, qk[m]);
+        }
+      }
+    }
+    float* P = U;   // partial sums of the second half: [4 products][16 rows][32]
+    if (split && half == 1 && live) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int tt = warp + 8 * m;
-        const float kti = KT[i * kNodeStride + tt], qti = QT[i * kNodeStride + tt];
-        ks[m] = fmaf(kti, sij, ks[m]);
-        qs[m] = fmaf(qti, sij, qs[m]);
-        kk[m] = fmaf(kti, kis, kk[m]);
-        qk[m] = fmaf(qti, kis, qk[m]);
+        const int tt = 4 * rg + m;
+        P[(0 * 16 + tt) * 32 + lane] = ks[m];
+        P[(1 * 16 + tt) * 32 + lane] = qs[m];
+        A[tt * 32 + lane] = kk[m];   // A doubles as the third and fourth partial arrays
+        A[(16 + tt) * 32 + lane] = qk[m];
       }
     }
+    if (split) __syncthreads();
+    if (live && half == 0) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int tt = warp + 8 * m;
-      KS[tt * kDnCols + lane] = ks[m];
-      QS[tt * kDnCols + lane] = qs[m];
-      KK[tt * kMaxRows + lane] = kk[m];
-      QK[tt * kMaxRows + lane] = qk[m];
+      for (int m = 0; m < 4; ++m) {
+        const int tt = 4 * rg + m;
+        if (split) {
+          ks[m] += P[(0 * 16 + tt) * 32 + lane];
+          qs[m] += P[(1 * 16 + tt) * 32 + lane];
+          kk[m] += A[tt * 32 + lane];
+          qk[m] += A[(16 + tt) * 32 + lane];
+        }
+        KS[tt * kDnCols + lane] = ks[m];
+        QS[tt * kDnCols + lane] = qs[m];
+        KK[tt * kMaxRows + lane] = kk[m];
+        C[tt * kMaxRows + lane] = qk[m];
+      }
     }
   }
   __syncthreads();
-  // right-hand side beta_t (v_t - exp(gc_t) S0^T k_t) in place of K S0, and the
-  // ancestor-masked coefficients
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int tt = warp + 8 * m;
-    if (tt < n) {
-      KS[tt * kDnCols + lane] = s_beta[tt] * (VB[tt * kDnCols + lane] - expf(s_gc[tt]) * KS[tt * kDnCols + lane]);
-      const int s = lane;
-      const bool strict_anc = s < tt && ((s_anc[tt] >> s) & 1u);
-      A[tt * kMaxRows + s] = strict_anc ? s_beta[tt] * expf(s_gc[tt] - s_gc[s]) * KK[tt * kMaxRows + s] : 0.f;
-    }
+  // right-hand side beta_t (v_t - exp(gc_t) S0^T k_t) in place of K S0; the
+  // coefficients A (strict ancestors) and C (the path, t included)
+  for (int idx = threadIdx.x; idx < n * kMaxRows; idx += kDnThreads) {
+    const int tt = idx / kMaxRows, s = idx - tt * kMaxRows;
+    KS[tt * kDnCols + s] = s_beta[tt] * (VB[tt * kDnCols + s] - expf(s_gc[tt]) * KS[tt * kDnCols + s]);
+    const bool on_path = s < n && ((s_anc[tt] >> s) & 1u);
+    const float decay = on_path ? expf(s_gc[tt] - s_gc[s]) : 0.f;
+    A[tt * kMaxRows + s] = (on_path && s < tt) ? s_beta[tt] * decay * KK[tt * kMaxRows + s] : 0.f;
+    C[tt * kMaxRows + s] = decay * C[tt * kMaxRows + s];
   }
+  // rows past n of U meet zero coefficients in the outputs: clear them
+  for (int idx = n * kDnCols + threadIdx.x; idx < kMaxRows * kDnCols; idx += kDnThreads) U[idx] = 0.f;
   __syncthreads();
-  // forward substitution, one column per lane: u_t = rhs_t - sum_s A[t][s] u_s
+  // forward substitution u_t = rhs_t - sum_{s < t} A[t][s] u_s, one column per
+  // lane with the column in registers (A is zero off the path)
   if (warp == 0) {
-    for (int tt = 0; tt < n; ++tt) {
-      float acc = KS[tt * kDnCols + lane];
-      unsigned m = s_anc[tt] & ~(1u << tt);
-      while (m != 0u) {
-        const int s = __ffs(m) - 1;
-        m &= m - 1u;
-        acc = fmaf(-A[tt * kMaxRows + s], U[s * kDnCols + lane], acc);
+    float ur[kMaxRows];
+#pragma unroll
+    for (int tt = 0; tt < kMaxRows; ++tt) {
+      if (tt < n) {
+        float a0 = KS[tt * kDnCols + lane], a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int s4 = 0; s4 < tt; s4 += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(A + tt * kMaxRows + s4);
+          a0 = fmaf(-c4.x, ur[s4], a0);
+          if (s4 + 1 < tt) a1 = fmaf(-c4.y, ur[s4 + 1], a1);
+          if (s4 + 2 < tt) a2 = fmaf(-c4.z, ur[s4 + 2], a2);
+          if (s4 + 3 < tt) a3 = fmaf(-c4.w, ur[s4 + 3], a3);
+        }
+        ur[tt] = (a0 + a1) + (a2 + a3);
+        U[tt * kDnCols + lane] = ur[tt];
       }
-      U[tt * kDnCols + lane] = acc;
     }
   }
   __syncthreads();
-  // outputs o_t = exp(gc_t) S0^T q_t + sum over the path of exp(gc_t - gc_s) (q_t . k_s) u_s
+  // outputs o_t = exp(gc_t) S0^T q_t + sum_s C[t][s] u_s
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int tt = warp + 8 * m;
     if (tt < n) {
-      float acc = expf(s_gc[tt]) * QS[tt * kDnCols + lane];
-      unsigned msk = s_anc[tt];
-      while (msk != 0u) {
-        const int s = __ffs(msk) - 1;
-        msk &= msk - 1u;
-        acc = fmaf(expf(s_gc[tt] - s_gc[s]) * QK[tt * kMaxRows + s], U[s * kDnCols + lane], acc);
+      float a0 = expf(s_gc[tt]) * QS[tt * kDnCols + lane], a1 = 0.f;
+      for (int s4 = 0; s4 <= tt; s4 += 4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(C + tt * kMaxRows + s4);
+        a0 = fmaf(c4.x, U[s4 * kDnCols + lane], a0);
+        a1 = fmaf(c4.y, U[(s4 + 1) * kDnCols + lane], a1);
+        a0 = fmaf(c4.z, U[(s4 + 2) * kDnCols + lane], a0);
+        a1 = fmaf(c4.w, U[(s4 + 3) * kDnCols + lane], a1);
       }
       const size_t off = ((size_t)(row0 + tt) * Hv + h) * dv + c0 + lane;
-      o[off] = acc;
+      o[off] = a0 + a1;
       u[off] = U[tt * kDnCols + lane];
     }
   }
   if (cb == 0 && threadIdx.x < n) gc_out[(size_t)(row0 + threadIdx.x) * Hv + h] = s_gc[threadIdx.x];
 }
 
+// Untiled TMA copy global -> shared, completing on an mbarrier (addresses
+// 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // S <- exp(gc_last) S + sum_{d <= a} exp(gc_last - gc_{p_d}) k_{p_d} u_{p_d}^T
 // for the accepted path p_0 = 0, ..., p_a of each request, in every layer.
-// The path is checked first: a in [0, n), p_0 = 0, parent(p_d) = p_{d-1}.
-__global__ void __launch_bounds__(kDnCommitThreads) dn_commit_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk,
-                                                                     int dv, int rows_per_layer, const float* k,
-                                                                     const float* u, const float* gc,
-                                                                     const int32_t* path, const int32_t* accept_len,
-                                                                     int32_t* status) {
+// The state tile (d_k x d_v, contiguous) comes in by one TMA bulk copy while
+// the path is checked (a in [0, n), p_0 = 0, parent(p_d) = p_{d-1}) and the
+// path's keys and scaled pseudo-values are staged; then every thread updates
+// 4 x 4 blocks of the tile and writes them back.
+__global__ void __launch_bounds__(kDnCommitThreads, 2) dn_commit_kernel(ReqTable t, DnStates st, int Hk, int Hv,
+                                                                        int dk, int dv, int rows_per_layer,
+                                                                        const float* k, const float* u,
+                                                                        const float* gc, const int32_t* path,
+                                                                        const int32_t* accept_len, int32_t* status) {
   extern __shared__ __align__(16) float dsm[];
-  float* KP = dsm;                          // [32 path nodes][d_k]
-  float* UP = dsm + kMaxRows * dk;          // [32][d_v], scaled by exp(gc_last - gc_p)
+  float* ST = dsm;                          // the state tile [d_k][d_v]
+  float* KP = dsm + dk * dv;                // [32 path nodes][d_k]
+  float* UP = KP + kMaxRows * dk;           // [32][d_v], scaled by exp(gc_last - gc_p)
+  __shared__ __align__(8) uint64_t s_bar;
   __shared__ int s_p[kMaxRows];
   __shared__ int s_a;
   __shared__ float s_decay;
@@ -228,7 +316,15 @@ __global__ void __launch_bounds__(kDnCommitThreads) dn_commit_kernel(ReqTable t,
   const int h = blockIdx.x, layer = blockIdx.y, r = blockIdx.z;
   const int n = t.n[r], row0 = t.row_off[r];
   const int kh = h / (Hv / Hk);
-  if (threadIdx.x == 0) s_a = accept_len[r];
+  float* S = st.S[r] + ((size_t)layer * Hv + h) * dk * dv;
+  const uint32_t tile_bytes = (uint32_t)(dk * dv * sizeof(float));
+  if (threadIdx.x == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&s_bar, tile_bytes);
+    bulk_g2s(ST, S, tile_bytes, &s_bar);
+    s_a = accept_len[r];
+  }
   __syncthreads();
   const int a = s_a;
   bool bad = a < 0 || a >= n;
@@ -244,44 +340,63 @@ __global__ void __launch_bounds__(kDnCommitThreads) dn_commit_kernel(ReqTable t,
       bad = t.parent[r][p] != pp;
     }
   }
-  if (__syncthreads_or(bad)) {
+  bad = __syncthreads_or(bad);
+  if (!bad) {
+    const size_t lrow = (size_t)layer * rows_per_layer;
+    const float gl = gc[(lrow + row0 + s_p[a]) * Hv + h];
+    if (threadIdx.x == 0) s_decay = expf(gl);
+    for (int idx = threadIdx.x; idx < (a + 1) * dk; idx += kDnCommitThreads) {
+      const int d = idx / dk, i = idx - d * dk;
+      KP[d * dk + i] = k[((lrow + row0 + s_p[d]) * Hk + kh) * dk + i];
+    }
+    for (int idx = threadIdx.x; idx < (a + 1) * dv; idx += kDnCommitThreads) {
+      const int d = idx / dv, j = idx - d * dv;
+      const size_t pr = lrow + row0 + s_p[d];
+      UP[d * dv + j] = expf(gl - gc[pr * Hv + h]) * u[(pr * Hv + h) * dv + j];
+    }
+  }
+  // every thread waits for the tile (bounded); a wait that gives up reports it
+  // and waits once more for the copy in flight before the CTA leaves
+  bool arrived = mbar_wait(&s_bar, 0);
+  if (!arrived) {
+    status_set(status, TV_E_TIMEOUT);
+    arrived = mbar_wait(&s_bar, 0);
+  }
+  if (bad) {
     if (threadIdx.x == 0 && h == 0 && layer == 0) status_set(status, TV_E_PATH);
     return;
   }
-  const size_t lrow = (size_t)layer * rows_per_layer;
-  const float gl = gc[(lrow + row0 + s_p[a]) * Hv + h];
-  if (threadIdx.x == 0) s_decay = expf(gl);
-  for (int idx = threadIdx.x; idx < (a + 1) * dk; idx += kDnCommitThreads) {
-    const int d = idx / dk, i = idx - d * dk;
-    KP[d * dk + i] = k[((lrow + row0 + s_p[d]) * Hk + kh) * dk + i];
-  }
-  for (int idx = threadIdx.x; idx < (a + 1) * dv; idx += kDnCommitThreads) {
-    const int d = idx / dv, j = idx - d * dv;
-    const size_t pr = lrow + row0 + s_p[d];
-    UP[d * dv + j] = expf(gl - gc[pr * Hv + h]) * u[(pr * Hv + h) * dv + j];
-  }
   __syncthreads();
-  float* S = st.S[r] + ((size_t)layer * Hv + h) * dk * dv;
+  if (!arrived) return;
+  // 4 x 4 blocks: per path node one 4-row load of k and one 4-column load of
+  // the scaled u feed 16 fused multiply-adds
   const float decay = s_decay;
-  // thread: 4 consecutive value columns, rows i = tid / (dv / 4) + stride m
-  const int cols4 = dv / 4;
-  const int rows_per_pass = kDnCommitThreads / cols4;
-  const int j4 = (threadIdx.x % cols4) * 4;
-  for (int i = threadIdx.x / cols4; i < dk; i += rows_per_pass) {
-    float4 s = *reinterpret_cast<const float4*>(S + (size_t)i * dv + j4);
-    s.x *= decay;
-    s.y *= decay;
-    s.z *= decay;
-    s.w *= decay;
-    for (int d = 0; d <= a; ++d) {
-      const float kdi = KP[d * dk + i];
-      const float4 ud = *reinterpret_cast<const float4*>(UP + d * dv + j4);
-      s.x = fmaf(kdi, ud.x, s.x);
-      s.y = fmaf(kdi, ud.y, s.y);
-      s.z = fmaf(kdi, ud.z, s.z);
-      s.w = fmaf(kdi, ud.w, s.w);
+  const int cq_n = dv / 4, quads = (dk / 4) * cq_n;
+  for (int pq = threadIdx.x; pq < quads; pq += kDnCommitThreads) {
+    const int i4 = (pq / cq_n) * 4, j4 = (pq % cq_n) * 4;
+    float4 x[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      x[rr] = *reinterpret_cast<const float4*>(ST + (i4 + rr) * dv + j4);
+      x[rr].x *= decay;
+      x[rr].y *= decay;
+      x[rr].z *= decay;
+      x[rr].w *= decay;
     }
-    *reinterpret_cast<float4*>(S + (size_t)i * dv + j4) = s;
+    for (int d = 0; d <= a; ++d) {
+      const float4 kd = *reinterpret_cast<const float4*>(KP + d * dk + i4);
+      const float4 ud = *reinterpret_cast<const float4*>(UP + d * dv + j4);
+      const float kr[4] = {kd.x, kd.y, kd.z, kd.w};
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        x[rr].x = fmaf(kr[rr], ud.x, x[rr].x);
+        x[rr].y = fmaf(kr[rr], ud.y, x[rr].y);
+        x[rr].z = fmaf(kr[rr], ud.z, x[rr].z);
+        x[rr].w = fmaf(kr[rr], ud.w, x[rr].w);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<float4*>(S + (size_t)(i4 + rr) * dv + j4) = x[rr];
   }
 }
 
@@ -291,7 +406,7 @@ bool g_dn_commit_smem[64] = {false};
 }  // namespace
 
 size_t dn_verify_smem(int dk) { return (size_t)dn_verify_layout(dk).total * sizeof(float); }
-size_t dn_commit_smem(int dk, int dv) { return (size_t)kMaxRows * (dk + dv) * sizeof(float); }
+size_t dn_commit_smem(int dk, int dv) { return (size_t)(dk * dv + kMaxRows * (dk + dv)) * sizeof(float); }
 
 int launch_dn_verify(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, const float* q,
                      const float* k, const float* v, const float* beta, const float* g, float* o, float* u, float* gc,

@@ -83,11 +83,9 @@ __device__ __forceinline__ bool block_skip(const int32_t* status) {
 // 0 <= parent[i] < i), token range (skipped when vocab <= 0), duplicate sibling
 // tokens [Algorithm and correctness contract, §Target position and batching].
 // par/tok receive this lane's parent and token.
-__device__ __forceinline__ int validate_tree_warp(const int32_t* parent, const int32_t* token, int n, int vocab,
-                                                  int& par, int& tok) {
+// check_tree_warp takes the lane's parent and token already loaded (0 past n).
+__device__ __forceinline__ int check_tree_warp(int par, int tok, int n, int vocab) {
   const int lane = threadIdx.x & 31;
-  par = lane < n ? parent[lane] : 0;
-  tok = lane < n ? token[lane] : 0;
   const bool bad_order = lane < n && (lane == 0 ? par != -1 : (par < 0 || par >= lane));
   const bool bad_token = lane < n && vocab > 0 && (tok < 0 || tok >= vocab);
   bool dup = false;
@@ -100,6 +98,13 @@ __device__ __forceinline__ int validate_tree_warp(const int32_t* parent, const i
   if (__any_sync(0xffffffffu, bad_token)) return TV_E_TOKEN;
   if (__any_sync(0xffffffffu, dup)) return TV_E_DUP_SIBLING;
   return TV_OK;
+}
+__device__ __forceinline__ int validate_tree_warp(const int32_t* parent, const int32_t* token, int n, int vocab,
+                                                  int& par, int& tok) {
+  const int lane = threadIdx.x & 31;
+  par = lane < n ? parent[lane] : 0;
+  tok = lane < n ? token[lane] : 0;
+  return check_tree_warp(par, tok, n, vocab);
 }
 
 // ---- launchers (host) -------------------------------------------------------
