@@ -389,8 +389,8 @@ TV_API int tv_profile_stop(float *stage_ms, int max_stages, int *n_stages, int *
  *   states      host array [n_req] of device pointers, 16-byte aligned: the
  *               layer's state of each request, fp32 [n_v_heads][d_k][d_v];
  *               read only
- *   q, k        device fp32 [total_rows][n_k_heads][d_k]
- *   v           device fp32 [total_rows][n_v_heads][d_v]
+ *   q, k        device fp32 [total_rows][n_k_heads][d_k], 16-byte aligned
+ *   v           device fp32 [total_rows][n_v_heads][d_v], 16-byte aligned
  *   beta, g     device fp32 [total_rows][n_v_heads]
  *   o, u        device fp32 [total_rows][n_v_heads][d_v]
  *   gc          device fp32 [total_rows][n_v_heads]
@@ -416,13 +416,14 @@ TV_API int tv_dn_verify_tree(const tv_dn_dims *dims, const tv_tree *trees, int n
  *   n_layers    host >= 1: layers committed in one call
  *   states      host array [n_req] of device pointers, 16-byte aligned: fp32
  *               [n_layers][n_v_heads][d_k][d_v], updated in place
- *   k           device fp32 [n_layers][total_rows][n_k_heads][d_k]
- *   u           device fp32 [n_layers][total_rows][n_v_heads][d_v]
+ *   k           device fp32 [n_layers][total_rows][n_k_heads][d_k], 16-byte aligned
+ *   u           device fp32 [n_layers][total_rows][n_v_heads][d_v], 16-byte aligned
  *   gc          device fp32 [n_layers][total_rows][n_v_heads]
  *               (u and gc as tv_dn_verify_tree wrote them, layer by layer)
  *   path, accept_len  device, from an accept walk
  * Host checks: as tv_dn_verify_tree.  Device checks: TV_E_PATH (a_r outside
- * 0..n_r - 1, path[0] != 0, or path[d] not a child of path[d - 1]).
+ * 0..n_r - 1, path[0] != 0, or path[d] not a child of path[d - 1]); with a
+ * bad path in any request no state is written.
  */
 TV_API int tv_dn_commit(const tv_dn_dims *dims, const tv_tree *trees, int n_req, int n_layers, float *const *states,
                         const float *k, const float *u, const float *gc, const int32_t *path,

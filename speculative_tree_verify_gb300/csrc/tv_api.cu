@@ -368,6 +368,7 @@ int tv_dn_verify_tree(const tv_dn_dims* dims, const tv_tree* trees, int n_req, f
   int rc = dn_check(dims);
   if (rc) return rc;
   if (!q || !k || !v || !beta || !g || !o || !u || !gc || !dev_status) return TV_E_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return TV_E_ARG;
   ReqTable t;
   if ((rc = build_table(t, trees, nullptr, n_req, true))) return rc;
   DnStates st;
@@ -382,6 +383,7 @@ int tv_dn_commit(const tv_dn_dims* dims, const tv_tree* trees, int n_req, int n_
   int rc = dn_check(dims);
   if (rc) return rc;
   if (n_layers < 1 || !k || !u || !gc || !path || !accept_len || !dev_status) return TV_E_ARG;
+  if (!aligned16(k) || !aligned16(u)) return TV_E_ARG;
   ReqTable t;
   if ((rc = build_table(t, trees, nullptr, n_req, true))) return rc;
   DnStates st;

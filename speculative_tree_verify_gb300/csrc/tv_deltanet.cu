@@ -21,9 +21,10 @@
 //  - dn_verify_kernel: one CTA per (value head, block of 32 value columns,
 //    request); every product in fp32 from shared memory, the triangular solve
 //    by forward substitution in node order (parents come first).
-//  - dn_commit_kernel: one CTA per (value head, layer, request); the whole
-//    d_k x d_v state comes in by one TMA bulk copy, is updated and written
-//    back in place (HBM-bound: the state is the only large operand).
+//  - dn_commit_kernel: persistent, one CTA per SM over the (request, layer,
+//    value head) tiles, two in flight: each d_k x d_v state tile comes in by
+//    one TMA bulk copy, is updated and written back in place (HBM-bound: the
+//    state is the only large operand).
 #include "tv_common.cuh"
 #include "tv_kernels.cuh"
 
@@ -35,7 +36,7 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int kDnCols = 32;        // value columns per verify CTA
 constexpr int kDnThreads = 256;    // verify CTA
 constexpr int kDnCommitThreads = 512;
-constexpr int kNodeStride = kMaxRows + 4;   // K^T / Q^T row stride: 16-byte rows, staging stores spread over banks
+constexpr int kNodeStride = kMaxRows + 4;   // K^T / Q^T row stride: 16-byte aligned rows
 
 // dynamic shared memory of the verify CTA, in floats
 struct DnVerifyLayout {
@@ -88,34 +89,35 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
     bl = beta[(size_t)(row0 + lane) * Hv + h];
   }
   const int c0 = cb * kDnCols;
-  constexpr int kKQ = kMaxRows * kDnMaxDim / kDnThreads;   // 16
-  constexpr int kSB = kDnMaxDim * kDnCols / kDnThreads;    // 16
-  constexpr int kVB = kMaxRows * kDnCols / kDnThreads;     // 4
-  float kreg[kKQ], qreg[kKQ], sreg[kSB], vreg[kVB];
+  constexpr int kKQ = kMaxRows * kDnMaxDim / 4 / kDnThreads;   // 4 float4 of K and of Q
+  constexpr int kSB = kDnMaxDim * kDnCols / 4 / kDnThreads;    // 4 float4 of S0
+  float4 kreg[kKQ], qreg[kKQ], sreg[kSB], vreg;
   const float* S0g = st.S[r] + (size_t)h * dk * dv;
+  const int k4 = dk / 4;
 #pragma unroll
   for (int m = 0; m < kKQ; ++m) {
     const int idx = threadIdx.x + m * kDnThreads;
-    const int s = idx / dk, i = idx - s * dk;   // node s, coordinate i (coalesced along i)
-    kreg[m] = 0.f;
-    qreg[m] = 0.f;
-    if (idx < kMaxRows * dk && s < n) {
-      const size_t off = ((size_t)(row0 + s) * Hk + kh) * dk + i;
-      kreg[m] = k[off];
-      qreg[m] = q[off];
+    // node s = the lane: the transposing stores below then hit 32 banks
+    const int s = idx % kMaxRows, c = idx / kMaxRows;   // coordinates 4c .. 4c + 3
+    kreg[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+    qreg[m] = kreg[m];
+    if (idx < kMaxRows * k4 && s < n) {
+      const size_t off = ((size_t)(row0 + s) * Hk + kh) * dk + 4 * c;
+      kreg[m] = *reinterpret_cast<const float4*>(k + off);
+      qreg[m] = *reinterpret_cast<const float4*>(q + off);
     }
   }
 #pragma unroll
   for (int m = 0; m < kSB; ++m) {
     const int idx = threadIdx.x + m * kDnThreads;
-    const int i = idx / kDnCols, j = idx - i * kDnCols;
-    sreg[m] = idx < dk * kDnCols ? S0g[(size_t)i * dv + c0 + j] : 0.f;
+    const int i = idx / (kDnCols / 4), c = idx - i * (kDnCols / 4);
+    sreg[m] = idx < dk * kDnCols / 4 ? *reinterpret_cast<const float4*>(S0g + (size_t)i * dv + c0 + 4 * c)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-#pragma unroll
-  for (int m = 0; m < kVB; ++m) {
-    const int idx = threadIdx.x + m * kDnThreads;
-    const int s = idx / kDnCols, j = idx - s * kDnCols;
-    vreg[m] = s < n ? v[((size_t)(row0 + s) * Hv + h) * dv + c0 + j] : 0.f;
+  {
+    const int s = threadIdx.x / (kDnCols / 4), c = threadIdx.x - s * (kDnCols / 4);   // 256 = 32 nodes x 8
+    vreg = s < n ? *reinterpret_cast<const float4*>(v + ((size_t)(row0 + s) * Hv + h) * dv + c0 + 4 * c)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
   if (warp == 0) {   // the tree: parent order; then cumulative gates and root paths
@@ -149,19 +151,23 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
 #pragma unroll
   for (int m = 0; m < kKQ; ++m) {
     const int idx = threadIdx.x + m * kDnThreads;
-    if (idx < kMaxRows * dk) {
-      const int s = idx / dk, i = idx - s * dk;
-      KT[i * kNodeStride + s] = kreg[m];
-      QT[i * kNodeStride + s] = qreg[m];
+    if (idx < kMaxRows * k4) {
+      const int s = idx % kMaxRows, c = idx / kMaxRows;
+      const float kv[4] = {kreg[m].x, kreg[m].y, kreg[m].z, kreg[m].w};
+      const float qv[4] = {qreg[m].x, qreg[m].y, qreg[m].z, qreg[m].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        KT[(4 * c + e) * kNodeStride + s] = kv[e];
+        QT[(4 * c + e) * kNodeStride + s] = qv[e];
+      }
     }
   }
 #pragma unroll
   for (int m = 0; m < kSB; ++m) {
     const int idx = threadIdx.x + m * kDnThreads;
-    if (idx < dk * kDnCols) S0[idx] = sreg[m];
+    if (idx < dk * kDnCols / 4) reinterpret_cast<float4*>(S0)[idx] = sreg[m];
   }
-#pragma unroll
-  for (int m = 0; m < kVB; ++m) VB[threadIdx.x + m * kDnThreads] = vreg[m];
+  reinterpret_cast<float4*>(VB)[threadIdx.x] = vreg;
   __syncthreads();
   if (s_err != TV_OK) {
     if (threadIdx.x == 0 && h == 0 && cb == 0) status_set(status, s_err);
@@ -291,113 +297,180 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
                : "memory");
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// dynamic shared memory of the commit CTA, in floats: two slots of (state
+// tile, the path's k rows, u rows, gates, weights)
+struct DnCommitLayout {
+  int st, kr, ur, gr, wr, slot, total;
+};
+__host__ __device__ inline DnCommitLayout dn_commit_layout(int dk, int dv) {
+  DnCommitLayout L;
+  int o = 0;
+  L.st = o; o += dk * dv;
+  L.kr = o; o += kMaxRows * dk;
+  L.ur = o; o += kMaxRows * dv;
+  L.gr = o; o += kMaxRows;
+  L.wr = o; o += kMaxRows;
+  L.slot = o;
+  L.total = 2 * o;
+  return L;
+}
+
 // S <- exp(gc_last) S + sum_{d <= a} exp(gc_last - gc_{p_d}) k_{p_d} u_{p_d}^T
 // for the accepted path p_0 = 0, ..., p_a of each request, in every layer.
-// The state tile (d_k x d_v, contiguous) comes in by one TMA bulk copy while
-// the path is checked (a in [0, n), p_0 = 0, parent(p_d) = p_{d-1}) and the
-// path's keys and scaled pseudo-values are staged; then every thread updates
-// 4 x 4 blocks of the tile and writes them back.
-__global__ void __launch_bounds__(kDnCommitThreads, 2) dn_commit_kernel(ReqTable t, DnStates st, int Hk, int Hv,
-                                                                        int dk, int dv, int rows_per_layer,
-                                                                        const float* k, const float* u,
-                                                                        const float* gc, const int32_t* path,
-                                                                        const int32_t* accept_len, int32_t* status) {
+// Persistent: one CTA per SM walks the (request, layer, value head) tiles with
+// a stride of the grid, two tiles in flight: the tile's state (d_k x d_v,
+// contiguous) by one TMA bulk copy, the path's k rows, u rows and gates by
+// asynchronous copies, while the previous tile is updated in 4 x 4 register
+// blocks and written back.  Every CTA first checks every request's path
+// (a in [0, n), p_0 = 0, parent(p_d) = p_{d-1}); with a bad path nothing is
+// written anywhere.
+__global__ void __launch_bounds__(kDnCommitThreads, 1) dn_commit_kernel(ReqTable t, DnStates st, int Hk, int Hv,
+                                                                        int dk, int dv, int n_layers,
+                                                                        int rows_per_layer, const float* k,
+                                                                        const float* u, const float* gc,
+                                                                        const int32_t* path, const int32_t* accept_len,
+                                                                        int32_t* status) {
   extern __shared__ __align__(16) float dsm[];
-  float* ST = dsm;                          // the state tile [d_k][d_v]
-  float* KP = dsm + dk * dv;                // [32 path nodes][d_k]
-  float* UP = KP + kMaxRows * dk;           // [32][d_v], scaled by exp(gc_last - gc_p)
-  __shared__ __align__(8) uint64_t s_bar;
-  __shared__ int s_p[kMaxRows];
-  __shared__ int s_a;
-  __shared__ float s_decay;
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ int s_p[kMaxReq][kMaxRows];
+  __shared__ int s_a[kMaxReq];
+  __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
-  const int h = blockIdx.x, layer = blockIdx.y, r = blockIdx.z;
-  const int n = t.n[r], row0 = t.row_off[r];
-  const int kh = h / (Hv / Hk);
-  float* S = st.S[r] + ((size_t)layer * Hv + h) * dk * dv;
-  const uint32_t tile_bytes = (uint32_t)(dk * dv * sizeof(float));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const DnCommitLayout L = dn_commit_layout(dk, dv);
   if (threadIdx.x == 0) {
-    mbar_init(&s_bar, 1);
+    s_bad = 0;
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(&s_bar, tile_bytes);
-    bulk_g2s(ST, S, tile_bytes, &s_bar);
-    s_a = accept_len[r];
   }
   __syncthreads();
-  const int a = s_a;
-  bool bad = a < 0 || a >= n;
-  if (!bad && (int)threadIdx.x <= a) {
-    const int p = path[row0 + threadIdx.x];
-    s_p[threadIdx.x] = p;
-    if (p < 0 || p >= n) {
-      bad = true;
-    } else if (threadIdx.x == 0) {
-      bad = p != 0;
-    } else {
-      const int pp = path[row0 + threadIdx.x - 1];
-      bad = t.parent[r][p] != pp;
+  for (int r = warp; r < t.n_req; r += kDnCommitThreads / 32) {   // one warp per request
+    const int n = t.n[r], row0 = t.row_off[r];
+    const int a = accept_len[r];
+    bool bad = a < 0 || a >= n;
+    if (!bad && lane <= a) {
+      const int p = path[row0 + lane];
+      s_p[r][lane] = p;
+      if (p < 0 || p >= n) bad = true;
+      else if (lane == 0) bad = p != 0;
+      else bad = t.parent[r][p] != path[row0 + lane - 1];
+    }
+    bad = __any_sync(FULL, bad);
+    if (lane == 0) {
+      s_a[r] = a;
+      if (bad) s_bad = 1;
     }
   }
-  bad = __syncthreads_or(bad);
-  if (!bad) {
-    const size_t lrow = (size_t)layer * rows_per_layer;
-    const float gl = gc[(lrow + row0 + s_p[a]) * Hv + h];
-    if (threadIdx.x == 0) s_decay = expf(gl);
-    for (int idx = threadIdx.x; idx < (a + 1) * dk; idx += kDnCommitThreads) {
-      const int d = idx / dk, i = idx - d * dk;
-      KP[d * dk + i] = k[((lrow + row0 + s_p[d]) * Hk + kh) * dk + i];
-    }
-    for (int idx = threadIdx.x; idx < (a + 1) * dv; idx += kDnCommitThreads) {
-      const int d = idx / dv, j = idx - d * dv;
-      const size_t pr = lrow + row0 + s_p[d];
-      UP[d * dv + j] = expf(gl - gc[pr * Hv + h]) * u[(pr * Hv + h) * dv + j];
-    }
-  }
-  // every thread waits for the tile (bounded); a wait that gives up reports it
-  // and waits once more for the copy in flight before the CTA leaves
-  bool arrived = mbar_wait(&s_bar, 0);
-  if (!arrived) {
-    status_set(status, TV_E_TIMEOUT);
-    arrived = mbar_wait(&s_bar, 0);
-  }
-  if (bad) {
-    if (threadIdx.x == 0 && h == 0 && layer == 0) status_set(status, TV_E_PATH);
+  __syncthreads();
+  if (s_bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, TV_E_PATH);
     return;
   }
-  __syncthreads();
-  if (!arrived) return;
-  // 4 x 4 blocks: per path node one 4-row load of k and one 4-column load of
-  // the scaled u feed 16 fused multiply-adds
-  const float decay = s_decay;
-  const int cq_n = dv / 4, quads = (dk / 4) * cq_n;
-  for (int pq = threadIdx.x; pq < quads; pq += kDnCommitThreads) {
-    const int i4 = (pq / cq_n) * 4, j4 = (pq % cq_n) * 4;
-    float4 x[4];
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      x[rr] = *reinterpret_cast<const float4*>(ST + (i4 + rr) * dv + j4);
-      x[rr].x *= decay;
-      x[rr].y *= decay;
-      x[rr].z *= decay;
-      x[rr].w *= decay;
+
+  const int per_req = n_layers * Hv;
+  const int n_tiles = t.n_req * per_req;
+  const uint32_t tile_bytes = (uint32_t)(dk * dv * sizeof(float));
+  auto tile_state = [&](int tile) {
+    const int r = tile / per_req, rem = tile - r * per_req;
+    return st.S[r] + (size_t)rem * dk * dv;   // rem = layer * Hv + h
+  };
+  // start the copies of one tile into one slot (thread 0: the state; all: the rest)
+  auto stage = [&](int tile, int slot) {
+    float* base = dsm + slot * L.slot;
+    const int r = tile / per_req, rem = tile - r * per_req;
+    const int layer = rem / Hv, h = rem - layer * Hv, kh = h / (Hv / Hk);
+    const int a = s_a[r], row0 = t.row_off[r];
+    const size_t lrow = (size_t)layer * rows_per_layer + row0;
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(&s_bar[slot], tile_bytes);
+      bulk_g2s(base + L.st, tile_state(tile), tile_bytes, &s_bar[slot]);
     }
-    for (int d = 0; d <= a; ++d) {
-      const float4 kd = *reinterpret_cast<const float4*>(KP + d * dk + i4);
-      const float4 ud = *reinterpret_cast<const float4*>(UP + d * dv + j4);
-      const float kr[4] = {kd.x, kd.y, kd.z, kd.w};
+    const int k4 = dk / 4, v4 = dv / 4;
+    for (int idx = threadIdx.x; idx < (a + 1) * (k4 + v4 + 1); idx += kDnCommitThreads) {
+      const int d = idx / (k4 + v4 + 1), c = idx - d * (k4 + v4 + 1);
+      const size_t pr = lrow + s_p[r][d];
+      if (c < k4) cp_async16(base + L.kr + d * dk + 4 * c, k + (pr * Hk + kh) * dk + 4 * c);
+      else if (c < k4 + v4) cp_async16(base + L.ur + d * dv + 4 * (c - k4), u + (pr * Hv + h) * dv + 4 * (c - k4));
+      else cp_async4(base + L.gr + d, gc + pr * Hv + h);
+    }
+  };
+  int tile = blockIdx.x;
+  if (tile < n_tiles) stage(tile, 0);
+  cp_async_commit();
+  if (tile + (int)gridDim.x < n_tiles) stage(tile + gridDim.x, 1);
+  cp_async_commit();
+  bool timed_out = false;
+  for (int j = 0; tile < n_tiles; ++j, tile += gridDim.x) {
+    const int slot = j & 1;
+    float* base = dsm + slot * L.slot;
+    const float* ST = base + L.st;
+    const float* KR = base + L.kr;
+    const float* UR = base + L.ur;
+    float* WR = base + L.wr;
+    cp_async_wait_prev();   // this tile's group (the next tile's may still be in flight)
+    if (!mbar_wait(&s_bar[slot], (uint32_t)((j >> 1) & 1))) {
+      // report, then wait (bounded) once more for the copy in flight before leaving
+      status_set(status, TV_E_TIMEOUT);
+      mbar_wait(&s_bar[slot], (uint32_t)((j >> 1) & 1));
+      timed_out = true;
+    }
+    timed_out = __syncthreads_or(timed_out);
+    if (timed_out) {   // the other slot may hold a copy in flight too
+      if (tile + (int)gridDim.x < n_tiles) mbar_wait(&s_bar[slot ^ 1], (uint32_t)(((j + 1) >> 1) & 1));
+      break;
+    }
+    const int r = tile / per_req;
+    const int a = s_a[r];
+    const float gl = base[L.gr + a];
+    if ((int)threadIdx.x <= a) WR[threadIdx.x] = expf(gl - base[L.gr + threadIdx.x]);
+    __syncthreads();
+    const float decay = expf(gl);
+    float* S = tile_state(tile);
+    const int cq_n = dv / 4, quads = (dk / 4) * cq_n;
+    for (int pq = threadIdx.x; pq < quads; pq += kDnCommitThreads) {
+      const int i4 = (pq / cq_n) * 4, j4 = (pq % cq_n) * 4;
+      float4 x[4];
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
-        x[rr].x = fmaf(kr[rr], ud.x, x[rr].x);
-        x[rr].y = fmaf(kr[rr], ud.y, x[rr].y);
-        x[rr].z = fmaf(kr[rr], ud.z, x[rr].z);
-        x[rr].w = fmaf(kr[rr], ud.w, x[rr].w);
+        x[rr] = *reinterpret_cast<const float4*>(ST + (i4 + rr) * dv + j4);
+        x[rr].x *= decay;
+        x[rr].y *= decay;
+        x[rr].z *= decay;
+        x[rr].w *= decay;
       }
-    }
+      for (int d = 0; d <= a; ++d) {
+        const float w = WR[d];
+        const float4 kd = *reinterpret_cast<const float4*>(KR + d * dk + i4);
+        const float4 ud = *reinterpret_cast<const float4*>(UR + d * dv + j4);
+        const float kr[4] = {kd.x * w, kd.y * w, kd.z * w, kd.w * w};
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<float4*>(S + (size_t)(i4 + rr) * dv + j4) = x[rr];
+        for (int rr = 0; rr < 4; ++rr) {
+          x[rr].x = fmaf(kr[rr], ud.x, x[rr].x);
+          x[rr].y = fmaf(kr[rr], ud.y, x[rr].y);
+          x[rr].z = fmaf(kr[rr], ud.z, x[rr].z);
+          x[rr].w = fmaf(kr[rr], ud.w, x[rr].w);
+        }
+      }
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) *reinterpret_cast<float4*>(S + (size_t)(i4 + rr) * dv + j4) = x[rr];
+    }
+    __syncthreads();   // the slot is free again
+    if (tile + 2 * (int)gridDim.x < n_tiles) stage(tile + 2 * gridDim.x, slot);
+    cp_async_commit();
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 bool g_dn_verify_smem[64] = {false};
@@ -406,7 +479,7 @@ bool g_dn_commit_smem[64] = {false};
 }  // namespace
 
 size_t dn_verify_smem(int dk) { return (size_t)dn_verify_layout(dk).total * sizeof(float); }
-size_t dn_commit_smem(int dk, int dv) { return (size_t)(dk * dv + kMaxRows * (dk + dv)) * sizeof(float); }
+size_t dn_commit_smem(int dk, int dv) { return (size_t)dn_commit_layout(dk, dv).total * sizeof(float); }
 
 int launch_dn_verify(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, const float* q,
                      const float* k, const float* v, const float* beta, const float* g, float* o, float* u, float* gc,
@@ -422,8 +495,14 @@ int launch_dn_commit(const ReqTable& t, const DnStates& st, int Hk, int Hv, int 
                      int32_t* status, cudaStream_t s) {
   int rc = ensure_smem_limit(dn_commit_kernel, dn_commit_smem(kDnMaxDim, kDnMaxDim), g_dn_commit_smem);
   if (rc) return rc;
-  return launch_pdl(dn_commit_kernel, dim3(Hv, n_layers, t.n_req), dim3(kDnCommitThreads), dn_commit_smem(dk, dv), s,
-                    t, st, Hk, Hv, dk, dv, t.total_rows, k, u, gc, path, accept_len, status);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                cudaSuccess)
+    return TV_E_CUDA;
+  const int tiles = t.n_req * n_layers * Hv;
+  const int grid = tiles < sms ? tiles : sms;
+  return launch_pdl(dn_commit_kernel, dim3(grid), dim3(kDnCommitThreads), dn_commit_smem(dk, dv), s, t, st, Hk, Hv,
+                    dk, dv, n_layers, t.total_rows, k, u, gc, path, accept_len, status);
 }
 
 }  // namespace tv
