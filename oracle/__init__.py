@@ -22,6 +22,9 @@ What is here, each written from the pages' statement of the method:
   residual verification].
 * ``commit_kv`` -- [Drafters and tree verify, §The round, step 4, and
   §Tree verify through recurrent layers, last paragraph].
+* ``oracle.sampling`` -- the sampled accept variants and the filters.
+* ``oracle.deltanet`` -- Gated DeltaNet tree verify and the path-state commit
+  [Drafters and tree verify, §Tree verify through recurrent layers].
 
 Parity pins: every function above is pinned in ``tests/test_oracle_*.py`` to
 something other than itself (brute-force sequential decoding, an independent

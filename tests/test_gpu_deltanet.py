@@ -200,3 +200,47 @@ def test_dn_rejects_bad_tree_and_bad_path(gpu):
     torch.cuda.synchronize()
     assert int(st.item()) == abi.CODES["TV_E_PATH"]
     assert np.array_equal(S.cpu().numpy(), r.inp.S0)
+
+
+def test_dn_full_size_48_layers_sampled(gpu):
+    """The bench's configuration: 16 key / 32 value heads of 128, a 16-row
+    lattice, the core of 48 layers (one call per layer, each on its own
+    state), then one commit of all 48 layers along the deepest root path.
+    Sampled (layer, head) pairs are checked against the oracle."""
+    Hk, Hv, dk, dv, NL, n = 16, 32, 128, 128, 48, 16
+    dims = abi.TvDnDims(Hk, Hv, dk, dv)
+    tree = synth.tree_lattice(n, 7, 151936, 7)
+    inps = [synth.dn_inputs(n, Hk, Hv, dk, dv, 900 + l) for l in range(NL)]
+    par = torch.from_numpy(tree.parent.astype(np.int32)).cuda()
+    tok = torch.from_numpy(tree.token.astype(np.int32)).cuda()
+    tv = abi.TvTree(par.data_ptr(), tok.data_ptr(), n)
+    S = torch.from_numpy(np.stack([x.S0 for x in inps])).cuda()
+    k_all = torch.from_numpy(np.stack([x.k for x in inps])).cuda()
+    u_all = torch.empty(NL, n, Hv, dv, device="cuda")
+    gc_all = torch.empty(NL, n, Hv, device="cuda")
+    o_all = torch.empty(NL, n, Hv, dv, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lb = Hv * dk * dv * 4
+    for l, x in enumerate(inps):
+        q, v, beta, g = (torch.from_numpy(a).cuda() for a in (x.q, x.v, x.beta, x.g))
+        _ok(abi.tv_dn_verify_tree(dims, [tv], [S.data_ptr() + l * lb], q, k_all[l], v, beta, g, o_all[l], u_all[l],
+                                  gc_all[l], st))
+    depth = np.zeros(n, int)
+    for t in range(1, n):
+        depth[t] = depth[tree.parent[t]] + 1
+    p = _root_path(tree.parent, int(np.argmax(depth)))
+    path = torch.tensor(p + [-1] * (n - len(p)), dtype=torch.int32, device="cuda")
+    alen = torch.tensor([len(p) - 1], dtype=torch.int32, device="cuda")
+    _ok(abi.tv_dn_commit(dims, [tv], NL, [S], k_all, u_all, gc_all, path, alen, st))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    o_g, S_g = o_all.cpu().numpy(), S.cpu().numpy()
+    rng = np.random.default_rng(0)
+    for l, h in zip(rng.choice(NL, 6, replace=False), rng.choice(Hv, 6)):
+        x = inps[l]
+        kh = h // (Hv // Hk)
+        states, outs = DN.dn_tree_states(tree.parent, x.q[:, kh].astype(np.float64), x.k[:, kh].astype(np.float64),
+                                         x.v[:, h].astype(np.float64), x.beta[:, h].astype(np.float64),
+                                         x.g[:, h].astype(np.float64), x.S0[h].astype(np.float64))
+        _close(o_g[l][:, h], outs, f"layer {l} head {h} outputs")
+        _close(S_g[l, h], DN.dn_commit(x.S0[h], states, p), f"layer {l} head {h} committed state")
