@@ -61,6 +61,9 @@ constexpr int kColS0 = 0, kColS1 = kNqMax, kColO = 2 * kNqMax;   // TMEM columns
 constexpr int kAtTmemCols = 512;
 constexpr int kAtom = 128 * 128;                   // bytes of one 128-row x 128-byte swizzled slab
 constexpr float kRescaleLog2 = 8.f;                // an offset moves when a score passes it by 2^8
+// epilogue: the column sums' table [128 keys][kNqMax + 1] floats, then the O^T
+// staging rows [kNqMax][D] floats, both over the free K, V and P^T stages
+constexpr int kOStageOff = ((128 * (kNqMax + 1) * 4) + 1023) & ~1023;
 static_assert(kNqMax % (8 * kSlices) == 0 && 3 * kNqMax <= kAtTmemCols && kCps == 5, "query columns must fit TMEM");
 
 struct AttnMaps {
@@ -81,6 +84,7 @@ struct AtSmem {
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
   static_assert(OFF_K % 1024 == 0, "swizzled slabs start on 1024-byte boundaries");
+  static_assert(kOStageOff + kNqMax * D * 4 <= OFF_BAR - OFF_K, "the epilogue's tables fit the free stages");
 };
 
 // 128B-swizzle smem descriptor with explicit leading / stride byte offsets.
@@ -690,6 +694,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           if (warp + kAtSoftWarps * i < NQ) s_red[0][warp + kAtSoftWarps * i] = x[i];
       }
     }
+    // O^T into shared memory as [query column][dimension] rows (past the sums'
+    // table; the K, V and P^T stages are free), then one bulk copy per row
+    float* ostage = reinterpret_cast<float*>(smem + L::OFF_K + kOStageOff);
     if (ok) {
       tmem_ld_wait();
       if (kl < D) {
@@ -698,15 +705,23 @@ __global__ void __launch_bounds__(kAtThreads, 1)
           if (u < nu) {
             const int c0 = (cs + kSlices * u) * 8;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int qr = s_qrow[c0 + j];
-              if (qr >= 0) part_o[((size_t)qr * kChunkSlots + chunk) * D + kl] = __uint_as_float(o[u][j]);
-            }
+            for (int j = 0; j < 8; ++j) ostage[(c0 + j) * D + kl] = __uint_as_float(o[u][j]);
           }
         }
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     soft_sync();
+    if (ok && lane == 0) {   // each warp's lane 0 writes columns warp, warp + 16, ...
+      for (int c = warp; c < nq; c += kAtSoftWarps) {
+        const int qr = s_qrow[c];
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                         part_o + ((size_t)qr * kChunkSlots + chunk) * D),
+                     "r"(smem_u32(ostage + c * D)), "r"((uint32_t)(D * sizeof(float)))
+                     : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
     if (!ok) {
       if (lane == 0) status_set(status, TV_E_TIMEOUT);
     } else if (qd == 0 && lane < 8) {
@@ -721,6 +736,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       }
     }
   }
+  if (lane == 0 && warp < kAtSoftWarps)   // the bulk stores have read their rows
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpIssue) {
