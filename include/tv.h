@@ -429,6 +429,66 @@ TV_API int tv_dn_commit(const tv_dn_dims *dims, const tv_tree *trees, int n_req,
                         const float *k, const float *u, const float *gc, const int32_t *path,
                         const int32_t *accept_len, int32_t *dev_status, void *stream);
 
+/*
+ * Verify prices and the StairCut cut [Drafters and tree verify, §StairCut: the
+ * node count, calculated each round; §StairCut on Flash-Next, and the shared
+ * price files].  Host-only: no device memory, nothing launched.
+ *
+ * tv_price_table holds the measured verify prices V(rows) by context class and
+ * kind, and the online state that follows the live prices.  The caller owns
+ * it (plain memory, no allocation); tv_price_init empties it, then the caller
+ * fills n_classes, class_ctx (ascending context lengths), prior (milliseconds
+ * of the measured counts, NaN elsewhere) and step_ms (ms a row past the last
+ * measured count; 0: the slope of the last two counts).
+ *
+ * tv_price_lookup: V(rows) for a context and kind.  The context takes the
+ * nearest lower class (the lowest if it is below all); rows between two
+ * measured counts interpolate; rows past the last measured count extrapolate
+ * as above; rows below the first take its price; a price never falls with more
+ * rows (the maximum over counts 1..rows).  An observed count uses its live
+ * price, the others the table's plus the learned offset of (class, kind).
+ *
+ * tv_price_observe: a measured verify time for (context, kind, rows): the
+ * count's live price moves toward it by an exponential average of weight 0.1,
+ * and the offset of (class, kind) moves by the same average of (observed -
+ * table price).
+ *
+ * tv_staircut: the cut of one drafted candidate.  Nodes 1..n-1 are admitted in
+ * the order of score (highest first, lower index on ties), each after its
+ * ancestors not yet admitted; the cut sizes tried are 7, 15, 23 and 31 nodes
+ * and the whole candidate, and the one maximising
+ *     (1 + min(sum of min(q, 1) over kept nodes, kept)) /
+ *     (V(kept + 1 rows) + draft_ms + commit_ms)
+ * is kept (a chain, kind TV_KIND_CHAIN, pays (1 - q of its deepest kept node)
+ * x rollback_ms instead of commit_ms; equal values keep the smaller cut).
+ *   parent, q, score  host arrays [n], parent-before-child, parent[0] = -1;
+ *                     q = the node's path probability
+ *   keep              host int32 [n]: the kept nodes in admission order
+ *                     (every prefix of it is a tree); *n_keep of them
+ *   value             the maximised expected tokens per millisecond
+ * Errors: TV_E_ARG (null, kind, an invalid table), TV_E_ROWS (n or rows
+ * outside 1..32), TV_E_ORDER (parent order).
+ */
+#define TV_KIND_CHAIN 0
+#define TV_KIND_TREE 1
+#define TV_PRICE_MAX_CLASSES 16
+#define TV_PRICE_MAX_ROWS 32
+typedef struct {
+    int32_t n_classes;
+    int32_t class_ctx[TV_PRICE_MAX_CLASSES];
+    double step_ms;
+    double prior[TV_PRICE_MAX_CLASSES][2][TV_PRICE_MAX_ROWS + 1];   /* [class][kind][rows], NaN: not measured */
+    double live[TV_PRICE_MAX_CLASSES][2][TV_PRICE_MAX_ROWS + 1];    /* NaN: never observed */
+    double offset[TV_PRICE_MAX_CLASSES][2];
+} tv_price_table;
+
+TV_API int tv_price_init(tv_price_table *t);
+TV_API int tv_price_lookup(const tv_price_table *t, int32_t context, int32_t kind, int32_t rows, double *ms);
+TV_API int tv_price_observe(tv_price_table *t, int32_t context, int32_t kind, int32_t rows, double ms);
+TV_API int tv_staircut(const int32_t *parent, const float *q, const float *score, int32_t n, int32_t kind,
+                       const tv_price_table *t, int32_t context, double draft_ms, double commit_ms,
+                       double rollback_ms, int32_t *keep, int32_t *n_keep, double *value);
+
 /* A short English name of a status code (static storage). */
 TV_API const char *tv_status_string(int code);
 

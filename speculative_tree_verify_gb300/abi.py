@@ -28,7 +28,8 @@ CODES = {v: k for k, v in STATUS.items()}
 SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept_residual", "tv_commit_kv",
            "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc",
            "tv_sample_workspace_size", "tv_sample_filter", "tv_accept_single_draw", "tv_accept_gumbel",
-           "tv_accept_rejection", "tv_dn_verify_tree", "tv_dn_commit")
+           "tv_accept_rejection", "tv_dn_verify_tree", "tv_dn_commit", "tv_price_init", "tv_price_lookup",
+           "tv_price_observe", "tv_staircut")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -51,6 +52,17 @@ class TvKv(ctypes.Structure):
 
 class TvTree(ctypes.Structure):
     _fields_ = [("parent", ctypes.c_void_p), ("token", ctypes.c_void_p), ("n", ctypes.c_int32)]
+
+
+TV_KIND_CHAIN, TV_KIND_TREE = 0, 1
+PRICE_MAX_CLASSES, PRICE_MAX_ROWS = 16, 32
+_PriceRows = ctypes.c_double * (PRICE_MAX_ROWS + 1)
+
+
+class TvPriceTable(ctypes.Structure):
+    _fields_ = [("n_classes", ctypes.c_int32), ("class_ctx", ctypes.c_int32 * PRICE_MAX_CLASSES),
+                ("step_ms", ctypes.c_double), ("prior", _PriceRows * 2 * PRICE_MAX_CLASSES),
+                ("live", _PriceRows * 2 * PRICE_MAX_CLASSES), ("offset", ctypes.c_double * 2 * PRICE_MAX_CLASSES)]
 
 
 class TvDnDims(ctypes.Structure):
@@ -100,6 +112,13 @@ def load():
                                           P, P, P, P, P, P, P, P, P]
         lib.tv_dn_commit.argtypes = [ctypes.POINTER(TvDnDims), ctypes.POINTER(TvTree), I, I, ctypes.POINTER(P), P, P,
                                      P, P, P, P, P]
+        D = ctypes.c_double
+        lib.tv_price_init.argtypes = [ctypes.POINTER(TvPriceTable)]
+        lib.tv_price_lookup.argtypes = [ctypes.POINTER(TvPriceTable), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.POINTER(D)]
+        lib.tv_price_observe.argtypes = [ctypes.POINTER(TvPriceTable), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, D]
+        lib.tv_staircut.argtypes = [P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(TvPriceTable),
+                                    ctypes.c_int32, D, D, D, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(D)]
         lib.tv_status_string.argtypes = [I]
         lib.tv_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -226,6 +245,37 @@ def tv_dn_commit(dims: TvDnDims, trees: Sequence[TvTree], n_layers: int, states,
                  dev_status, stream=None) -> int:
     return load().tv_dn_commit(ctypes.byref(dims), _arr(TvTree, trees), len(trees), int(n_layers), _ptrs(states),
                                _p(k), _p(u), _p(gc), _p(path), _p(accept_len), _p(dev_status), _stream(stream))
+
+
+def tv_price_init(table: TvPriceTable) -> int:
+    return load().tv_price_init(ctypes.byref(table))
+
+
+def tv_price_lookup(table: TvPriceTable, context: int, kind: int, rows: int):
+    """(rc, ms)"""
+    ms = ctypes.c_double(0.0)
+    rc = load().tv_price_lookup(ctypes.byref(table), int(context), int(kind), int(rows), ctypes.byref(ms))
+    return rc, ms.value
+
+
+def tv_price_observe(table: TvPriceTable, context: int, kind: int, rows: int, ms: float) -> int:
+    return load().tv_price_observe(ctypes.byref(table), int(context), int(kind), int(rows), float(ms))
+
+
+def tv_staircut(parent, q, score, kind: int, table: TvPriceTable, context: int, draft_ms: float, commit_ms: float,
+                rollback_ms: float = 0.0):
+    """Host arrays (numpy int32 / float32).  Returns (rc, kept nodes, value)."""
+    import numpy as np
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    qq = np.ascontiguousarray(q, dtype=np.float32)
+    sc = np.ascontiguousarray(score, dtype=np.float32)
+    n = int(par.shape[0])
+    keep = np.zeros(max(n, 1), dtype=np.int32)
+    nk, val = ctypes.c_int32(0), ctypes.c_double(0.0)
+    rc = load().tv_staircut(par.ctypes.data, qq.ctypes.data, sc.ctypes.data, n, int(kind), ctypes.byref(table),
+                            int(context), float(draft_ms), float(commit_ms), float(rollback_ms), keep.ctypes.data,
+                            ctypes.byref(nk), ctypes.byref(val))
+    return rc, keep[:nk.value].tolist(), val.value
 
 
 def tv_commit_kv(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], path, accept_len, committed_src,

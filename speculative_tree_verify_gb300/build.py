@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtv.so")
 SOURCES = ["tv_api.cu", "tv_gemm.cu", "tv_layer.cu", "tv_attn.cu", "tv_walks.cu", "tv_noalloc.cu", "tv_sample.cu",
-           "tv_deltanet.cu"]
+           "tv_deltanet.cu", "tv_policy.cpp"]
 HEADERS = ["tv_common.cuh", "tv_gemm.cuh", "tv_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
@@ -43,8 +43,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        # host code: no fused multiply-add contraction, the same doubles on every host
+        extra = ["-Xcompiler", "-ffp-contract=off"] if src.endswith(".cpp") else []
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{res.stderr}")
