@@ -539,6 +539,29 @@ def run_ours(args, world, rank, local):
         "commit_frac_of_peak": round(cbytes / dn_c_us / 1e3 / peak, 4)}
     del dstate, du, dgc, dks
 
+    # ---- StairCut on the measured GB300 prices: the cut of a 31-node lattice
+    #      (q = 0.85^depth, scores = q), its host cost through the C ABI ---------
+    from speculative_tree_verify_gb300 import prices as pr
+    if os.path.exists(pr.GB300_PRICES):
+        ptab = pr.table_from_json(pr.GB300_PRICES)
+        lat = synth.tree_lattice(32, 15, D.vocab, 77)
+        depth = np.zeros(32)
+        for i in range(1, 32):
+            depth[i] = depth[lat.parent[i]] + 1
+        qn = (0.85 ** depth).astype(np.float32)
+        cuts = {}
+        for cctx in (1024, 32768):
+            rc, kept, val = abi.tv_staircut(lat.parent, qn, qn, abi.TV_KIND_TREE, ptab, cctx, 0.0, 0.0)
+            dv.check(rc, "tv_staircut")
+            cuts[str(cctx)] = {"nodes": len(kept), "tokens_per_ms": round(val, 3)}
+        reps = 20000
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            abi.tv_staircut(lat.parent, qn, qn, abi.TV_KIND_TREE, ptab, 1024, 0.0, 0.0)
+        out["staircut"] = {"cut_31_node_lattice": cuts,
+                           "host_us_per_cut": round((time.perf_counter() - t0) / reps * 1e6, 2),
+                           "note": "through the Python binding (argument marshalling included)"}
+
     # ---- end to end through the C ABI with host buffers --------------------------
     par_h = torch.from_numpy(req.parent.cpu().numpy()).pin_memory()
     tok_h = torch.from_numpy(req.token.cpu().numpy()).pin_memory()
