@@ -346,7 +346,7 @@ def run_ours(args, world, rank, local):
                       "l2": "inputs larger than L2: 1.68 GB of weights stream from HBM every step",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "eager_ms_per_step": round(eager_ms, 4), "clocks": clocks,
-           "gpu_launches": 11 * args.steps, "code_sha256": _code_sha256()}
+           "gpu_launches": 10 * args.steps, "code_sha256": _code_sha256()}
     if rank != 0 or args.no_extras:
         return out if rank == 0 else None
 

@@ -189,8 +189,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
 
   StageMarks pm(st);
   pm.mark(0);
-  if ((rc = launch_prologue(t, d, b, dev_status, st))) return rc;
-  if ((rc = launch_embed_norm(t, *model, b, dev_status, st))) return rc;
+  if ((rc = launch_prologue_embed(t, *model, b, dev_status, st))) return rc;
   pm.mark(1);
   gp.out = b.part_qkv;
   if ((rc = launch_gemm(GEMM_PARTIAL, model->wqkv, QKV, H, b.h, t.total_rows, pq, gp, sms, st))) return rc;

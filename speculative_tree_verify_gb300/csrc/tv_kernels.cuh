@@ -131,8 +131,10 @@ struct LayerBufs {
   __nv_bfloat16* hf;       // [32][H]
 };
 
-int launch_prologue(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st);
-int launch_embed_norm(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status, cudaStream_t st);
+// the verify's first kernel: per request the tree prologue (validation, depth,
+// position, ancestors), per row the embedding and first RMSNorm
+int launch_prologue_embed(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status,
+                          cudaStream_t st);
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
                         cudaStream_t st);
 int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int sms, int32_t* status,

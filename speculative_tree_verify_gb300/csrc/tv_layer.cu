@@ -14,20 +14,15 @@ constexpr int kRowThreads = 512;   // one block per row for the row-wise kernels
 constexpr int kRowVecs = 4;        // uint4 (8 bf16) vectors per thread: hidden <= 16384
 
 // ---------------------------------------------------------------------------
-// prologue: one warp per request.  Validates the tree and computes per row the
-// depth, position ctx + depth and ancestor set (node i sees its ancestors and
-// itself: "an attention mask of its ancestors and a position equal to its
+// prologue of request r, by one warp.  Validates the tree and computes per row
+// the depth, position ctx + depth and ancestor set (node i sees its ancestors
+// and itself: "an attention mask of its ancestors and a position equal to its
 // depth" [Drafters and tree verify, §Tree verify through recurrent layers]).
 // ---------------------------------------------------------------------------
-__global__ void prologue_kernel(ReqTable t, int vocab, RowMeta* meta, unsigned int* head_counter, int32_t* status) {
+__device__ void prologue_warp(const ReqTable& t, int r, int vocab, RowMeta* meta, int32_t* status) {
   __shared__ int s_depth[32];
   __shared__ uint32_t s_anc[32];
-  const int r = blockIdx.x;
-  const int lane = threadIdx.x;
-  pdl_wait();
-  pdl_trigger();
-  if (status_get(status) != 0) return;
-  if (r == 0 && lane == 0) *head_counter = 0u;
+  const int lane = threadIdx.x & 31;
   const int n = t.n[r];
   int par, tok;
   const int err = validate_tree_warp(t.parent[r], t.token[r], n, vocab, par, tok);
@@ -93,18 +88,35 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return u;
 }
 
-// h = bf16( x / sqrt(mean(x^2) + eps) * g ), x = E[token]; one block per row,
-// each thread holds up to kRowVecs 8-element vectors of the row.
-__global__ void __launch_bounds__(kRowThreads) embed_norm_kernel(const RowMeta* meta, const __nv_bfloat16* embed,
-                                                                 const __nv_bfloat16* g, int H, float eps,
-                                                                 __nv_bfloat16* h, const int32_t* status) {
+// The verify's first kernel.  Row blocks: h = bf16( x / sqrt(mean(x^2) + eps)
+// * g ), x = E[token], each thread holding up to kRowVecs 8-element vectors of
+// the row.  The last n_req blocks: the prologue of each request (warp 0).
+__global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t, int vocab, RowMeta* meta,
+                                                                     unsigned int* head_counter,
+                                                                     const __nv_bfloat16* embed,
+                                                                     const __nv_bfloat16* g, int H, float eps,
+                                                                     __nv_bfloat16* h, int32_t* status) {
   __shared__ float red[33];
   pdl_wait();
   pdl_trigger();
   if (block_skip(status)) return;
+  if ((int)blockIdx.x >= t.total_rows) {   // the last n_req blocks: the prologues
+    if (threadIdx.x < 32) {
+      const int r = blockIdx.x - t.total_rows;
+      if (r == 0 && threadIdx.x == 0) *head_counter = 0u;
+      prologue_warp(t, r, vocab, meta, status);
+    }
+    return;
+  }
+  // row blocks: the row's token straight from its tree (a token out of range,
+  // which the prologue reports, reads row 0 here; the status stops the verify)
   const int row = blockIdx.x;
+  int r = 0;
+  while (r + 1 < t.n_req && t.row_off[r + 1] <= row) ++r;
+  int token = t.token[r][row - t.row_off[r]];
+  token = token < 0 || token >= vocab ? 0 : token;
   const int nvec = H / 8;
-  const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)meta[row].token * H);
+  const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)token * H);
   float xf[kRowVecs][8];
   float ss = 0.f;
 #pragma unroll
@@ -283,15 +295,12 @@ RopeParams rope_params(int head_dim, float theta) {
 
 }  // namespace
 
-int launch_prologue(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int32_t* status, cudaStream_t st) {
-  return launch_pdl(prologue_kernel, dim3(t.n_req), dim3(32), 0, st, t, d.vocab, b.meta, b.head_counter, status);
-}
-
-int launch_embed_norm(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status, cudaStream_t st) {
+int launch_prologue_embed(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status,
+                          cudaStream_t st) {
   if (m.dims.hidden > kRowVecs * kRowThreads * 8) return TV_E_UNSUPPORTED;
-  return launch_pdl(embed_norm_kernel, dim3(t.total_rows), dim3(kRowThreads), 0, st, (const RowMeta*)b.meta,
-                    reinterpret_cast<const __nv_bfloat16*>(m.embed), reinterpret_cast<const __nv_bfloat16*>(m.ln1),
-                    m.dims.hidden, m.dims.rms_eps, b.h, (const int32_t*)status);
+  return launch_pdl(prologue_embed_kernel, dim3(t.total_rows + t.n_req), dim3(kRowThreads), 0, st, t, m.dims.vocab,
+                    b.meta, b.head_counter, reinterpret_cast<const __nv_bfloat16*>(m.embed),
+                    reinterpret_cast<const __nv_bfloat16*>(m.ln1), m.dims.hidden, m.dims.rms_eps, b.h, status);
 }
 
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,

@@ -36,10 +36,11 @@ __global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t*
     if (lane == 0) status_set(status, err);
     return;
   }
+  const int am = lane < n ? argmax[row0 + lane] : 0;   // every row's token at once; the walk shuffles
   int cur = 0, a = 0;
   if (lane == 0) path[row0] = 0;
   for (;;) {
-    const int want = argmax[row0 + cur];
+    const int want = __shfl_sync(FULL, am, cur);
     const unsigned hit = __ballot_sync(FULL, lane > 0 && lane < n && par == cur && tok == want);
     if (hit == 0u) {
       if (lane == 0) out_tokens[row0 + a] = want;   // the model's token at the stopping node
