@@ -20,7 +20,7 @@
 // query vectors are the MMA's N dimension, so a KV head's queries need no
 // padding to 128.  Per 128-key tile t:
 //   S^T = K_t Q^T      tcgen05.mma M128 (keys) N (queries) K16, fp32 in TMEM;
-//                      K by TMA (K-major A), Q staged once (K-major B)
+//                      K by TMA (K-major A), Q once by a 3-D TMA box (K-major B)
 //   softmax            16 warps: four per TMEM lane quarter, each thread one key
 //                      x a quarter of the query columns.  Each query column
 //                      has an offset m (log2 units) that moves only when a
@@ -35,7 +35,8 @@
 // O, the column sums and the offsets all carry the same offset, which cancels
 // in O / sum, so the lazy offset is exact.
 // A 17th warp issues the TMA loads (two K and two V stages) and the MMAs from
-// an event loop.  S^T is double-buffered in TMEM so that S^T of tile t+1
+// an event loop; it issues the first two K tiles before the programmatic-launch
+// wait and the queries and the first two V tiles right after it.  S^T is double-buffered in TMEM so that S^T of tile t+1
 // overlaps the softmax of t, and O^T of tile t overlaps the next tile's
 // softmax up to its P^T store.
 #include <cmath>
@@ -61,14 +62,12 @@ constexpr int kColS0 = 0, kColS1 = kNqMax, kColO = 2 * kNqMax;   // TMEM columns
 constexpr int kAtTmemCols = 512;
 constexpr int kAtom = 128 * 128;                   // bytes of one 128-row x 128-byte swizzled slab
 constexpr float kRescaleLog2 = 8.f;                // an offset moves when a score passes it by 2^8
-// epilogue: the column sums' table [128 keys][kNqMax + 1] floats, then the O^T
-// staging rows [kNqMax][D] floats, both over the free K, V and P^T stages
-constexpr int kOStageOff = ((128 * (kNqMax + 1) * 4) + 1023) & ~1023;
 static_assert(kNqMax % (8 * kSlices) == 0 && 3 * kNqMax <= kAtTmemCols && kCps == 5, "query columns must fit TMEM");
 
 struct AttnMaps {
   CUtensorMap k[kMaxReq];   // per request: [Hkv * capacity][D] bf16, box 64 x 128, 128B swizzle
   CUtensorMap v[kMaxReq];
+  CUtensorMap q[kMaxReq];   // per request: q as [rows][Hq][D], box 64 x G x n (one KV head's query columns)
 };
 
 template <int D>
@@ -84,7 +83,6 @@ struct AtSmem {
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   static constexpr size_t BYTES = 1024 + OFF_BAR + 256;
   static_assert(OFF_K % 1024 == 0, "swizzled slabs start on 1024-byte boundaries");
-  static_assert(kOStageOff + kNqMax * D * 4 <= OFF_BAR - OFF_K, "the epilogue's tables fit the free stages");
 };
 
 // 128B-swizzle smem descriptor with explicit leading / stride byte offsets.
@@ -191,8 +189,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   uint64_t* s_free = s_full + 2;                                          // [2] S^T buffer read (16 warps)
   uint64_t* p_full = s_free + 2;                                          // P^T stored (16 warps)
   uint64_t* o_done = p_full + 1;                                          // O^T MMA of a tile done
-  uint64_t* q_full = o_done + 1;                                          // queries staged (16 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
+  uint64_t* q_full = o_done + 1;                                          // query padding zeroed (16 warps)
+  uint64_t* q_land = q_full + 1;                                          // queries landed (TMA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_land + 1);
   int* s_stat = reinterpret_cast<int*>(tmem_slot + 1);
   __shared__ uint32_t s_anc[32];
   __shared__ int s_qrow[kNqMax];                     // query column c: its row of q and of the partials, (row0 + c / G) Hq + g G + c % G
@@ -246,9 +245,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     mbar_init(p_full, kAtSoftWarps);
     mbar_init(o_done, 1);
     mbar_init(q_full, kAtSoftWarps);
+    mbar_init(q_land, 1);
     fence_mbar_init();
     prefetch_tmap(&maps.k[r]);
     prefetch_tmap(&maps.v[r]);
+    prefetch_tmap(&maps.q[r]);
   }
   if (warp == kWarpIssue) {
     tmem_alloc(tmem_slot, kAtTmemCols);
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     // its predecessor before it completes, so every earlier writer of the
     // cache is done.  The tree slots (written by the previous kernel) and the
     // queries are read after the wait.
-    for (int j = 0; j < 2 && j < T; ++j)   // K only: the V tiles wait until the queries are staged
+    for (int j = 0; j < 2 && j < T; ++j)   // K only: the queries go ahead of the V tiles
       if (pre_ok(j)) {
         issue(false, j);
         pre |= 1u << j;
@@ -287,6 +288,14 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 
   pdl_wait();
   pdl_trigger();
+  if (issuer) {
+    // the KV head's query columns (rows row0 .. row0 + n - 1, heads g G .. g G + G - 1:
+    // column c = row c / G, head c % G), then the first two V tiles
+    mbar_arrive_expect_tx(q_land, (uint32_t)((D / 64) * nq * 128));
+#pragma unroll
+    for (int a = 0; a < D / 64; ++a) tma_load_3d(smem + L::OFF_Q + a * L::QSLAB, &maps.q[r], q_land, a * 64, g * G, row0);
+    for (int j = 0; j < 2 && j < T; ++j) issue(true, j);
+  }
   if (threadIdx.x == 0) *s_stat = status_get(status);
   if (threadIdx.x < 32) s_anc[threadIdx.x] = (int)threadIdx.x < n ? meta[row0 + threadIdx.x].anc : 0u;
   __syncthreads();
@@ -302,14 +311,14 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       for (int j = 0; j < 2 && j < T; ++j)
         if (!((pre >> j) & 1u)) issue(false, j);
       kiss = T < 2 ? T : 2;
-      viss = 0;
+      viss = T < 2 ? T : 2;
       int ns = 0, no = 0;   // S^T / O^T MMAs issued
       bool qready = false, ok = true;
       unsigned long long t_last = globaltimer();
       uint32_t polls = 0;
       while (no < T) {
         bool progress = false;
-        if (!qready) qready = mbar_test(q_full, 0);
+        if (!qready) qready = mbar_test(q_land, 0) && mbar_test(q_full, 0);
         // O^T += V^T P^T of tile no
         if (qready && no < ns && mbar_test(p_full, (uint32_t)no & 1u) &&
             mbar_test(&v_full[no & 1], (uint32_t)(no >> 1) & 1u)) {
@@ -350,9 +359,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         // V of tile viss: its stage held tile viss-2, whose O^T is done (O^T
         // of tile viss cannot have run yet, so the parity names tile viss-2)
-        // (the first two once the queries are staged, so that the query loads
-        // do not queue behind them)
-        if (viss < T && (viss < 2 ? qready : viss - 2 < no && mbar_test(&v_free[viss & 1], (uint32_t)((viss - 2) >> 1) & 1u))) {
+        if (viss < T && viss - 2 < no && mbar_test(&v_free[viss & 1], (uint32_t)((viss - 2) >> 1) & 1u)) {
           issue(true, viss);
           ++viss;
           progress = true;
@@ -373,12 +380,16 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       // waited for by an MMA, except after a timeout)
       for (int j = (ns > 0 ? ns : 0); j < kiss; ++j) mbar_wait(&k_full[j & 1], (uint32_t)(j >> 1) & 1u);
       for (int j = no; j < viss; ++j) mbar_wait(&v_full[j & 1], (uint32_t)(j >> 1) & 1u);
+      if (!qready) mbar_wait(q_land, 0);
       // and every MMA issued is done before TMEM is released
       if (no > 0) mbar_wait(o_done, (uint32_t)(no - 1) & 1u);
       if (ns > 0) mbar_wait(&s_full[(ns - 1) & 1], (uint32_t)((ns - 1) >> 1) & 1u);
     } else if (issuer) {
-      for (int j = 0; j < 2 && j < T; ++j)   // loads issued before the wait land before the CTA leaves
+      for (int j = 0; j < 2 && j < T; ++j) {   // loads already issued land before the CTA leaves
         if ((pre >> j) & 1u) mbar_wait(&k_full[j & 1], 0);
+        mbar_wait(&v_full[j & 1], 0);
+      }
+      mbar_wait(q_land, 0);
     }
   } else if (run) {
     // ---------------- softmax / epilogue (warps 0-15) ----------------
@@ -396,27 +407,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       s_qrow[c] = c < nq ? (row0 + c / G) * Hq + g * G + c % G : -1;
       s_canc[c] = c < nq ? s_anc[c / G] : 0u;
     }
-    soft_sync();
-    {   // all of this thread's 16-byte pieces are loaded before any is stored
-      constexpr int kPer = (kNqMax * (D / 8) + kAtSoftThreads - 1) / kAtSoftThreads;
-      uint4 v[kPer];
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int idx = threadIdx.x + kAtSoftThreads * i;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (idx < NQ * (D / 8)) {
-          const int qr = s_qrow[idx / (D / 8)];
-          if (qr >= 0) v[i] = reinterpret_cast<const uint4*>(q + (size_t)qr * D)[idx % (D / 8)];
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int idx = threadIdx.x + kAtSoftThreads * i;
-        if (idx < NQ * (D / 8)) {
-          const int c = idx / (D / 8), e = idx % (D / 8);
-          *reinterpret_cast<uint4*>(sQ + (e >> 3) * L::QSLAB + swz(c, e & 7)) = v[i];
-        }
-      }
+    // query columns nq .. NQ-1 pad the MMA's N to a multiple of 16: zero (the
+    // columns below nq arrive by TMA)
+    for (int idx = threadIdx.x; idx < (NQ - nq) * (D / 8); idx += kAtSoftThreads) {
+      const int c = nq + idx / (D / 8), e = idx % (D / 8);
+      *reinterpret_cast<uint4*>(sQ + (e >> 3) * L::QSLAB + swz(c, e & 7)) = make_uint4(0u, 0u, 0u, 0u);
     }
     if constexpr (D == 64) {   // O^T is M = 128: dimensions 64..127 read a zero slab
       for (int idx = threadIdx.x; idx < 2 * kAtom / 16; idx += kAtSoftThreads) {
@@ -649,95 +644,76 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
 
     // ---- epilogue: unnormalised O, offsets and sums of this chunk --------------
+    // Column sums over the 128 keys while the last O^T MMA runs.  In each warp
+    // a reduce-scatter over its 32 keys: the 40 sums of a lane are halved
+    // three times (lane bits 4, 3, 2; the half a lane keeps follows its bit),
+    // then the five left are summed over lane bits 1 and 0; so lane L ends with
+    // the warp's sums of entries 20 b4 + 10 b3 + 5 b2 + k, k < 5, of its
+    // [chunk u][column j] list.  The four lane quarters of a slice then meet
+    // in s_red.
+    {
+      const uint32_t b4 = (lane >> 4) & 1u, b3 = (lane >> 3) & 1u, b2 = (lane >> 2) & 1u;
+      float a20[20], a10[10], a5[5];
+#pragma unroll
+      for (int k = 0; k < 20; ++k) {
+        const float lo = l[k / 8][k % 8], hi = l[(20 + k) / 8][(20 + k) % 8];
+        a20[k] = (b4 ? hi : lo) + __shfl_xor_sync(0xffffffffu, b4 ? lo : hi, 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 10; ++k)
+        a10[k] = (b3 ? a20[10 + k] : a20[k]) + __shfl_xor_sync(0xffffffffu, b3 ? a20[k] : a20[10 + k], 8);
+#pragma unroll
+      for (int k = 0; k < 5; ++k) {
+        a5[k] = (b2 ? a10[5 + k] : a10[k]) + __shfl_xor_sync(0xffffffffu, b2 ? a10[k] : a10[5 + k], 4);
+        a5[k] += __shfl_xor_sync(0xffffffffu, a5[k], 2);
+        a5[k] += __shfl_xor_sync(0xffffffffu, a5[k], 1);
+      }
+      if ((lane & 3) == 0) {
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+          const int e = (int)(20 * b4 + 10 * b3 + 5 * b2) + k;   // entry: chunk e / 8, column e % 8
+          if (e / 8 < nu) s_red[qd][(cs + kSlices * (e / 8)) * 8 + e % 8] = a5[k];
+        }
+      }
+    }
+    slice_sync(cs);
+    // one thread per column of the slice: the column's sum over the four quarters
+    const int own = qd * 32 + lane;
+    const int c_own = own < nu * 8 ? (cs + kSlices * (own >> 3)) * 8 + (own & 7) : -1;
+    const float l_own = c_own >= 0 ? (s_red[0][c_own] + s_red[1][c_own]) + (s_red[2][c_own] + s_red[3][c_own]) : 0.f;
+
     if (ok && !mbar_wait(o_done, (uint32_t)(T - 1) & 1u)) ok = false;
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    // column sums over the 128 keys: every MMA and load is done, so the K/V
-    // stages hold a [key][column] table (row stride 161 words: no bank conflicts)
-    float* lsum = reinterpret_cast<float*>(smem + L::OFF_K);
     if (ok) {
-#pragma unroll
-      for (int u = 0; u < kCps; ++u) {
-        if (u < nu) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) lsum[kl * (kNqMax + 1) + (cs + kSlices * u) * 8 + j] = l[u][j];
-        }
-      }
-    }
-    // O^T of this thread's dimension and columns, loaded while the sums are formed
-    uint32_t o[kCps][8];
-    if (ok) {
+      // O^T row kl (dimension kl) of this thread's columns, stored straight from
+      // the registers: for one column the warp writes 32 consecutive floats
+      uint32_t o[kCps][8];
 #pragma unroll
       for (int u = 0; u < kCps; ++u)
         if (u < nu) ld8(tO + (cs + kSlices * u) * 8, o[u]);
-    }
-    soft_sync();
-    if (ok) {   // warp w sums columns w, w + 16, ...: all loads, then the shuffles, interleaved
-      constexpr int kCols = kNqMax / kAtSoftWarps;
-      float x[kCols];
-#pragma unroll
-      for (int i = 0; i < kCols; ++i) {
-        const int c = warp + kAtSoftWarps * i;
-        x[i] = 0.f;
-        if (c < NQ) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) x[i] += lsum[(lane + 32 * k) * (kNqMax + 1) + c];
-        }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < kCols; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], off);
-      if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < kCols; ++i)
-          if (warp + kAtSoftWarps * i < NQ) s_red[0][warp + kAtSoftWarps * i] = x[i];
-      }
-    }
-    // O^T into shared memory as [query column][dimension] rows (past the sums'
-    // table; the K, V and P^T stages are free), then one bulk copy per row
-    float* ostage = reinterpret_cast<float*>(smem + L::OFF_K + kOStageOff);
-    if (ok) {
       tmem_ld_wait();
       if (kl < D) {
 #pragma unroll
         for (int u = 0; u < kCps; ++u) {
           if (u < nu) {
-            const int c0 = (cs + kSlices * u) * 8;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) ostage[(c0 + j) * D + kl] = __uint_as_float(o[u][j]);
+            for (int j = 0; j < 8; ++j) {
+              const int qr = s_qrow[(cs + kSlices * u) * 8 + j];
+              if (qr >= 0) part_o[((size_t)qr * kChunkSlots + chunk) * D + kl] = __uint_as_float(o[u][j]);
+            }
           }
         }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    soft_sync();
-    if (ok && lane == 0) {   // each warp's lane 0 writes columns warp, warp + 16, ...
-      for (int c = warp; c < nq; c += kAtSoftWarps) {
-        const int qr = s_qrow[c];
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                         part_o + ((size_t)qr * kChunkSlots + chunk) * D),
-                     "r"(smem_u32(ostage + c * D)), "r"((uint32_t)(D * sizeof(float)))
-                     : "memory");
+      if (c_own >= 0 && s_qrow[c_own] >= 0) {
+        const size_t base = (size_t)s_qrow[c_own] * kChunkSlots + chunk;
+        part_ml[base * 2] = s_m[ver][c_own];
+        part_ml[base * 2 + 1] = l_own;
       }
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    }
-    if (!ok) {
-      if (lane == 0) status_set(status, TV_E_TIMEOUT);
-    } else if (qd == 0 && lane < 8) {
-      for (int u = 0; u < nu; ++u) {
-        const int c = (cs + kSlices * u) * 8 + lane;
-        const int qr = s_qrow[c];
-        if (qr >= 0) {
-          const size_t base = (size_t)qr * kChunkSlots + chunk;
-          part_ml[base * 2] = s_m[ver][c];
-          part_ml[base * 2 + 1] = s_red[0][c];
-        }
-      }
+    } else if (lane == 0) {
+      status_set(status, TV_E_TIMEOUT);
     }
   }
-  if (lane == 0 && warp < kAtSoftWarps)   // the bulk stores have read their rows
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpIssue) {
@@ -747,41 +723,41 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // out[row][h*D + d] = bf16( sum_c o_c[d] 2^(m_c - M) / sum_c l_c 2^(m_c - M) ),
-// chunks in order.  grid (rows, Hq), block D.
-__global__ void attn_merge_kernel(ReqTable t, const RowMeta* meta, int Hq, int D, int chunk_target,
-                                  const float* part_ml, const float* part_o, __nv_bfloat16* out,
-                                  const int32_t* status) {
-  __shared__ float s_mc[kChunkSlots], s_lc[kChunkSlots], s_w[kChunkSlots];
-  pdl_wait();
-  pdl_trigger();
-  if (block_skip(status)) return;
+// chunks in order.  grid (rows, Hq), block D (>= the chunk slots).  The row's
+// chunk count follows from the kernel parameters, so every partial of the row
+// is requested at once, right after the wait.
+__global__ void __launch_bounds__(128) attn_merge_kernel(ReqTable t, int Hq, int D, int chunk_target,
+                                                         const float* part_ml, const float* part_o,
+                                                         __nv_bfloat16* out, const int32_t* status) {
+  static_assert(kChunkSlots <= 64, "one thread per chunk slot in a block of D >= 64 threads");
+  __shared__ float2 s_ml[kChunkSlots];   // chunk offset (log2 units), chunk sum
+  __shared__ int s_stat;
   const int row = blockIdx.x, hq = blockIdx.y, d = threadIdx.x;
-  const int nch = attn_plan(t.ctx[meta[row].req], chunk_target).n_chunks;
+  int r = 0;
+  while (r + 1 < t.n_req && t.row_off[r + 1] <= row) ++r;
+  const int nch = attn_plan(t.ctx[r], chunk_target).n_chunks;
   const size_t base = ((size_t)row * Hq + hq) * kChunkSlots;
-  // every chunk's offset and sum at once (one load each), then the weights
-  for (int c = d; c < nch; c += blockDim.x) {
-    s_mc[c] = part_ml[(base + c) * 2];
-    s_lc[c] = part_ml[(base + c) * 2 + 1];
-  }
-  __syncthreads();
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, s_mc[c]);
-  for (int c = d; c < nch; c += blockDim.x) s_w[c] = exp2f(s_mc[c] - M);   // offsets are in log2 units
-  __syncthreads();
-  float L = 0.f;
-  for (int c = 0; c < nch; ++c) L = fmaf(s_lc[c], s_w[c], L);
-  // the chunks' outputs, eight loads in flight, summed in chunk order
+  pdl_trigger();   // the O GEMM may start streaming its weights now
+  pdl_wait();
+  if (d == 0) s_stat = status_get(status);
+  if (d < nch) s_ml[d] = reinterpret_cast<const float2*>(part_ml)[base + d];
   const float* po = part_o + base * D + d;
-  float O = 0.f;
-  int c = 0;
-  for (; c + 8 <= nch; c += 8) {
-    float v[8];
+  float v[kChunkSlots];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = po[(size_t)(c + i) * D];
+  for (int c = 0; c < kChunkSlots; ++c) v[c] = c < nch ? po[(size_t)c * D] : 0.f;
+  __syncthreads();
+  if (s_stat != 0) return;
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, s_ml[c].x);
+  float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) O = fmaf(v[i], s_w[c + i], O);
+  for (int c = 0; c < kChunkSlots; ++c) {
+    if (c < nch) {
+      const float w = exp2f(s_ml[c].x - M);
+      L = fmaf(s_ml[c].y, w, L);
+      O = fmaf(v[c], w, O);
+    }
   }
-  for (; c < nch; ++c) O = fmaf(po[(size_t)c * D], s_w[c], O);
   out[(size_t)row * Hq * D + (size_t)hq * D + d] = f2bf(O / L);
 }
 
@@ -798,6 +774,9 @@ int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b,
     if (rc) return rc;
     rc = make_tmap_bf16(&maps.v[r], t.v[r], D, rows, 64, 128);
     if (rc) return rc;
+    rc = make_tmap_bf16_3d(&maps.q[r], b.q, D, dm.n_q_heads, t.total_rows, 64, dm.n_q_heads / dm.n_kv_heads,
+                           t.n[r]);
+    if (rc) return rc;
     nch_max = max(nch_max, attn_plan(t.ctx[r], target).n_chunks);
   }
   const size_t smem = AtSmem<D>::BYTES;
@@ -809,8 +788,7 @@ int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b,
                       (const __nv_bfloat16*)b.q, dm.n_q_heads, dm.n_kv_heads, target, scale_log2, b.attn_ml,
                       b.attn_o, status);
   if (rc) return rc;
-  return launch_pdl(attn_merge_kernel, dim3(t.total_rows, dm.n_q_heads), dim3(D), 0, st, t, (const RowMeta*)b.meta,
-                    dm.n_q_heads, D, target, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn,
+  return launch_pdl(attn_merge_kernel, dim3(t.total_rows, dm.n_q_heads), dim3(D), 0, st, t, dm.n_q_heads, D, target, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn,
                     (const int32_t*)status);
 }
 

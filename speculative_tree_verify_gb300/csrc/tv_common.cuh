@@ -184,6 +184,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -274,6 +283,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 // memory at all (weights, which no kernel writes, may be read).  pdl_wait()
 // returns once the previous grid has completed and its writes are visible;
 // since every kernel waits before it completes, that covers all earlier grids.
+// pdl_trigger() lets the next kernel start.  Kernels trigger right after their
+// wait, except the three whose successor is a GEMM (the verify's first kernel,
+// the attention merge, the O finalize): they trigger on entry, so that the
+// GEMM streams weights while they wait.  A kernel that loads more than
+// weights before its wait (the attention: cached keys below the context) needs
+// its predecessor to trigger after its wait: then, when it starts, every grid
+// before that predecessor has completed.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -396,6 +396,20 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int 
   return r == CUDA_SUCCESS ? TV_OK : TV_E_CUDA;
 }
 
+int make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d0, int d1, int d2, int b0, int b1, int b2) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return TV_E_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (d0 * 2) % 16 != 0) return TV_E_ARG;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)d0 * d1 * 2};
+  cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, (cuuint32_t)b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TV_OK : TV_E_CUDA;
+}
+
 int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows, const GemmPlan& pl,
                 const GemmParams& base, int num_sms, cudaStream_t stream) {
   if (K % BK != 0 || n_rows < 1 || n_rows > kMaxRows) return TV_E_UNSUPPORTED;

@@ -35,6 +35,10 @@ size_t gemm_smem_bytes();
 // 2-D bf16 tensor map over [rows][inner] with a box of box_rows x box_inner
 // and the 128-byte swizzle; rows past `rows` read as zeros.
 int make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int box_inner, int box_rows);
+// 3-D bf16 tensor map over [d2][d1][d0] (d0 contiguous) with a box of
+// b2 x b1 x b0 and the 128-byte swizzle: a box lands as b2 * b1 rows of b0
+// elements, row (z, y) at row index z * b1 + y.
+int make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d0, int d1, int d2, int b0, int b1, int b2);
 int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows, const GemmPlan& pl,
                 const GemmParams& base, int num_sms, cudaStream_t stream);
 

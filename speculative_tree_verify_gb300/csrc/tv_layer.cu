@@ -97,8 +97,8 @@ __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t,
                                                                      const __nv_bfloat16* g, int H, float eps,
                                                                      __nv_bfloat16* h, int32_t* status) {
   __shared__ float red[33];
+  pdl_trigger();   // the QKV GEMM may start streaming its weights now
   pdl_wait();
-  pdl_trigger();
   if (block_skip(status)) return;
   if ((int)blockIdx.x >= t.total_rows) {   // the last n_req blocks: the prologues
     if (threadIdx.x < 32) {
@@ -220,8 +220,8 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(const RowMeta* 
                                                                  const __nv_bfloat16* g, float eps,
                                                                  __nv_bfloat16* hf, const int32_t* status) {
   __shared__ float red[33];
+  pdl_trigger();   // the head GEMM may start streaming its weights now
   pdl_wait();
-  pdl_trigger();
   if (block_skip(status)) return;
   const int row = blockIdx.x;
   const int nvec = H / 8;
