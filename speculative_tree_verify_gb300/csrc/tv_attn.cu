@@ -723,42 +723,70 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 }
 
 // out[row][h*D + d] = bf16( sum_c o_c[d] 2^(m_c - M) / sum_c l_c 2^(m_c - M) ),
-// chunks in order.  grid (rows, Hq), block D (>= the chunk slots).  The row's
-// chunk count follows from the kernel parameters, so every partial of the row
-// is requested at once, right after the wait.
-__global__ void __launch_bounds__(128) attn_merge_kernel(ReqTable t, int Hq, int D, int chunk_target,
-                                                         const float* part_ml, const float* part_o,
-                                                         __nv_bfloat16* out, const int32_t* status) {
-  static_assert(kChunkSlots <= 64, "one thread per chunk slot in a block of D >= 64 threads");
-  __shared__ float2 s_ml[kChunkSlots];   // chunk offset (log2 units), chunk sum
-  __shared__ int s_stat;
-  const int row = blockIdx.x, hq = blockIdx.y, d = threadIdx.x;
+// chunks in order.  One warp per (row, query head), lane i holding dimensions
+// 4i .. 4i + 3 (a chunk's partial is one 16-byte load per lane) and the offset
+// and sum of chunks i and i + 32.  The row's chunk count follows from the
+// kernel parameters, so the partials are requested right after the wait, up
+// to kMergeBatch chunks at a time.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 20;
+static_assert(kChunkSlots <= 64, "a lane holds at most two chunks' offsets");
+
+__global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(ReqTable t, int Hq, int D, int chunk_target,
+                                                                      const float* part_ml, const float* part_o,
+                                                                      __nv_bfloat16* out, const int32_t* status) {
+  pdl_trigger();   // the O GEMM may start streaming its weights now
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * kMergeWarps + warp;
+  const int row = pair / Hq, hq = pair % Hq;
+  if (row >= t.total_rows) {   // warp-uniform; the rest of the block does not synchronise
+    pdl_wait();
+    return;
+  }
   int r = 0;
   while (r + 1 < t.n_req && t.row_off[r + 1] <= row) ++r;
   const int nch = attn_plan(t.ctx[r], chunk_target).n_chunks;
   const size_t base = ((size_t)row * Hq + hq) * kChunkSlots;
-  pdl_trigger();   // the O GEMM may start streaming its weights now
+  const int nv = D / 4;   // 16-byte pieces of one chunk's partial
+  const bool dl = lane < nv;
   pdl_wait();
-  if (d == 0) s_stat = status_get(status);
-  if (d < nch) s_ml[d] = reinterpret_cast<const float2*>(part_ml)[base + d];
-  const float* po = part_o + base * D + d;
-  float v[kChunkSlots];
+  const float2* ml = reinterpret_cast<const float2*>(part_ml) + base;
+  float2 ml0 = make_float2(-INFINITY, 0.f), ml1 = make_float2(-INFINITY, 0.f);
+  if (lane < nch) ml0 = __ldcg(ml + lane);
+  if (lane + 32 < nch) ml1 = __ldcg(ml + lane + 32);
+  const bool skip = status_get(status) != 0;
+  const float4* po = reinterpret_cast<const float4*>(part_o + base * D) + lane;
+  float M = fmaxf(ml0.x, ml1.x);
 #pragma unroll
-  for (int c = 0; c < kChunkSlots; ++c) v[c] = c < nch ? po[(size_t)c * D] : 0.f;
-  __syncthreads();
-  if (s_stat != 0) return;
-  float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, s_ml[c].x);
-  float L = 0.f, O = 0.f;
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < nch; c0 += kMergeBatch) {   // a batch of loads in flight, then its terms in order
+    float4 v[kMergeBatch];
 #pragma unroll
-  for (int c = 0; c < kChunkSlots; ++c) {
-    if (c < nch) {
-      const float w = exp2f(s_ml[c].x - M);
-      L = fmaf(s_ml[c].y, w, L);
-      O = fmaf(v[c], w, O);
+    for (int i = 0; i < kMergeBatch; ++i)
+      v[i] = dl && c0 + i < nch ? __ldcg(po + (size_t)(c0 + i) * nv) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      const int c = c0 + i;
+      if (c < nch) {
+        const float mc = __shfl_sync(0xffffffffu, c < 32 ? ml0.x : ml1.x, c & 31);
+        const float lc = __shfl_sync(0xffffffffu, c < 32 ? ml0.y : ml1.y, c & 31);
+        const float w = exp2f(mc - M);   // offsets are in log2 units
+        L = fmaf(lc, w, L);
+        O.x = fmaf(v[i].x, w, O.x);
+        O.y = fmaf(v[i].y, w, O.y);
+        O.z = fmaf(v[i].z, w, O.z);
+        O.w = fmaf(v[i].w, w, O.w);
+      }
     }
   }
-  out[(size_t)row * Hq * D + (size_t)hq * D + d] = f2bf(O / L);
+  if (skip || !dl) return;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(O.x / L, O.y / L), hi = __floats2bfloat162_rn(O.z / L, O.w / L);
+  uint2 pk;
+  pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out + (size_t)row * Hq * D + (size_t)hq * D + 4 * lane) = pk;
 }
 
 template <int D>
@@ -788,7 +816,9 @@ int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b,
                       (const __nv_bfloat16*)b.q, dm.n_q_heads, dm.n_kv_heads, target, scale_log2, b.attn_ml,
                       b.attn_o, status);
   if (rc) return rc;
-  return launch_pdl(attn_merge_kernel, dim3(t.total_rows, dm.n_q_heads), dim3(D), 0, st, t, dm.n_q_heads, D, target, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn,
+  const int pairs = t.total_rows * dm.n_q_heads;
+  return launch_pdl(attn_merge_kernel, dim3((pairs + kMergeWarps - 1) / kMergeWarps), dim3(kMergeWarps * 32), 0, st, t,
+                    dm.n_q_heads, D, target, (const float*)b.attn_ml, (const float*)b.attn_o, b.attn,
                     (const int32_t*)status);
 }
 
