@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t,
   __shared__ float red[33];
   pdl_trigger();   // the QKV GEMM may start streaming its weights now
   pdl_wait();
-  if (block_skip(status)) return;
+  // no status check: nothing here indexes with data an earlier kernel wrote
+  // (tokens are clamped), and the kernels after it check the status
   if ((int)blockIdx.x >= t.total_rows) {   // the last n_req blocks: the prologues
     if (threadIdx.x < 32) {
       const int r = blockIdx.x - t.total_rows;
@@ -170,7 +171,6 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
                                     int D, RopeParams rp, __nv_bfloat16* q_out, const int32_t* status) {
   pdl_wait();
   pdl_trigger();
-  if (block_skip(status)) return;
   const int row = blockIdx.x, head = blockIdx.y, d = threadIdx.x;
   const int half = D / 2;
   const int M = (Hq + 2 * Hkv) * D;
@@ -184,6 +184,10 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
       p2[s] = ps[f2];
     }
   }
+  // the row's metadata and the status are read with the partials; the status
+  // is checked before the metadata picks a cache address
+  const RowMeta m = meta[row];
+  const bool bad = status_get(status) != 0;
   float x1 = 0.f, x2 = 0.f;
 #pragma unroll
   for (int s = 0; s < kMaxSplits; ++s) {
@@ -192,7 +196,7 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
       x2 += p2[s];
     }
   }
-  const RowMeta m = meta[row];
+  if (bad) return;
   float y1 = x1, y2 = x2;
   if (head < Hq + Hkv) {
     float sn, cs;
@@ -215,17 +219,23 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
 
 // O projection finalize: r = bf16(x + sum_s partial_s) with the splits summed in
 // order, hf = bf16(RMSNorm(r) g_f); one block per row.
-__global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(const RowMeta* meta, const float* part, int splits,
+__global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(ReqTable t, int vocab, const float* part, int splits,
                                                                  int H, const __nv_bfloat16* embed,
                                                                  const __nv_bfloat16* g, float eps,
                                                                  __nv_bfloat16* hf, const int32_t* status) {
   __shared__ float red[33];
   pdl_trigger();   // the head GEMM may start streaming its weights now
   pdl_wait();
-  if (block_skip(status)) return;
+  // the row's token straight from its tree (clamped like the first kernel's),
+  // read with the status; nothing is written after an earlier error
   const int row = blockIdx.x;
+  int rq = 0;
+  while (rq + 1 < t.n_req && t.row_off[rq + 1] <= row) ++rq;
+  int token = t.token[rq][row - t.row_off[rq]];
+  const bool bad = status_get(status) != 0;
+  token = token < 0 || token >= vocab ? 0 : token;
   const int nvec = H / 8;
-  const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)meta[row].token * H);
+  const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)token * H);
   float r[kRowVecs][8];
   float ss = 0.f;
 #pragma unroll
@@ -263,6 +273,7 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(const RowMeta* 
     }
   }
   ss = block_sum(ss, red);
+  if (bad) return;
   const float inv = 1.0f / sqrtf(ss / (float)H + eps);
   const uint4* gv = reinterpret_cast<const uint4*>(g);
   uint4* hv = reinterpret_cast<uint4*>(hf + (size_t)row * H);
@@ -323,7 +334,7 @@ int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b,
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st) {
   if (m.dims.hidden > kRowVecs * kRowThreads * 8 || splits > kMaxSplits) return TV_E_UNSUPPORTED;
-  return launch_pdl(o_finalize_kernel, dim3(t.total_rows), dim3(kRowThreads), 0, st, (const RowMeta*)b.meta,
+  return launch_pdl(o_finalize_kernel, dim3(t.total_rows), dim3(kRowThreads), 0, st, t, m.dims.vocab,
                     (const float*)b.part_o, splits, m.dims.hidden, reinterpret_cast<const __nv_bfloat16*>(m.embed),
                     reinterpret_cast<const __nv_bfloat16*>(m.ln_f), m.dims.rms_eps, b.hf, (const int32_t*)status);
 }

@@ -28,15 +28,18 @@ __global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t*
   const int r = blockIdx.x, lane = threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  if (status_get(status) != 0) return;
   const int n = t.n[r], row0 = t.row_off[r];
+  // every row's token, the status and the tree in one round trip (all reads
+  // in bounds whatever an earlier kernel left); the walk shuffles
+  const int am = lane < n ? argmax[row0 + lane] : 0;
+  const bool prior = status_get(status) != 0;   // one load for the whole warp
   int par, tok;
   const int err = validate_tree_warp(t.parent[r], t.token[r], n, 0, par, tok);
+  if (prior) return;
   if (err != TV_OK) {
     if (lane == 0) status_set(status, err);
     return;
   }
-  const int am = lane < n ? argmax[row0 + lane] : 0;   // every row's token at once; the walk shuffles
   int cur = 0, a = 0;
   if (lane == 0) path[row0] = 0;
   for (;;) {
@@ -590,21 +593,21 @@ __global__ void __launch_bounds__(128) commit_kernel(ReqTable t, int D, const in
                                                      int32_t* committed_src, int32_t* new_ctx, int32_t* status) {
   __shared__ uint4 rows[kMaxRows * 128 * 2 / 16];
   __shared__ int s_src[kMaxRows];
-  __shared__ int s_a;
   pdl_wait();
   pdl_trigger();
-  if (block_skip(status)) return;
   const int g = blockIdx.x, which = blockIdx.y, r = blockIdx.z;
   const int n = t.n[r], row0 = t.row_off[r], ctx = t.ctx[r];
-  if (threadIdx.x == 0) s_a = accept_len[r];
-  __syncthreads();
-  const int a = s_a;
+  // the accepted length, the path entries and the status in one round trip
+  // (every read in bounds whatever an earlier kernel left)
+  const int a = accept_len[r];
+  const int p = (int)threadIdx.x < n ? path[row0 + threadIdx.x] : 0;
+  const int prior = threadIdx.x == 0 ? status_get(status) : 0;
   bool bad = a < 0 || a >= n;
   if (!bad && (int)threadIdx.x <= a) {
-    const int p = path[row0 + threadIdx.x];
     s_src[threadIdx.x] = p;
     if (p < 0 || p >= n || (threadIdx.x == 0 && p != 0)) bad = true;
   }
+  if (__syncthreads_or(prior != 0)) return;   // an earlier error: nothing is written
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) status_set(status, TV_E_PATH);
     return;
