@@ -89,17 +89,41 @@ typedef struct tv_dims {
   float rms_eps;      /* RMSNorm epsilon                                    */
 } tv_dims;
 
-/* The layer + head, all device pointers to bf16, row-major, caller-owned:
+/* The layer + head, all device pointers to bf16, caller-owned:
  *   embed   [vocab][hidden]            token embedding
  *   ln1     [hidden]                   RMSNorm gain before the projections
  *   wqkv    [(Hq + 2 Hkv) D][hidden]   rows: the Q heads, then K heads, then V heads
  *   wo      [hidden][Hq D]             output projection
  *   ln_f    [hidden]                   final RMSNorm gain
- *   lm_head [vocab][hidden]            output head                               */
+ *   lm_head [vocab][hidden]            output head
+ * packed = 0: wqkv, wo and lm_head are row-major as above.  packed = 1: each
+ * of the three is the tile-packed copy tv_pack_weight makes of that matrix
+ * (the same numbers; the GEMMs then read every 16 KB tile from one contiguous
+ * stretch of memory, which streams faster).  Every other pointer is row-major
+ * either way.                                                                  */
 typedef struct tv_model {
   const tv_bf16 *embed, *ln1, *wqkv, *wo, *ln_f, *lm_head;
   tv_dims dims;
+  int32_t packed;
 } tv_model;
+
+/*
+ * The tile-packed layout of a bf16 weight W [rows][cols] (cols a multiple of
+ * 64): the rows are padded with zeros to a multiple of 128, cut into tiles of
+ * 128 rows x 64 columns, and tile (i, j) (rows 128 i .., columns 64 j ..) is
+ * stored row-major at element offset (i * (cols / 64) + j) * 8192.
+ *
+ * tv_packed_weight_bytes: host-only; writes the packed size in bytes
+ * (ceil(rows / 128) * 128 * cols * 2).  TV_E_ARG on rows < 1 or cols not a
+ * positive multiple of 64.
+ * tv_pack_weight: device W (row-major, 16-byte aligned) -> device packed
+ * (16-byte aligned, tv_packed_weight_bytes bytes, caller-owned, not
+ * overlapping W), enqueued on `stream`; meant to run once when the weights are
+ * loaded.  TV_E_ARG as above or on null / unaligned pointers, TV_E_CUDA if
+ * the launch fails.
+ */
+TV_API int tv_packed_weight_bytes(int32_t rows, int32_t cols, size_t *bytes);
+TV_API int tv_pack_weight(const tv_bf16 *w, int32_t rows, int32_t cols, tv_bf16 *packed, void *stream);
 
 /* One request's KV cache, device pointers to bf16, layout [Hkv][capacity][D].
  * Slots [0, ctx_len) hold the cached context.  ctx_len and capacity are host

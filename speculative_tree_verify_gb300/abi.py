@@ -29,7 +29,7 @@ SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept
            "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc",
            "tv_sample_workspace_size", "tv_sample_filter", "tv_accept_single_draw", "tv_accept_gumbel",
            "tv_accept_rejection", "tv_dn_verify_tree", "tv_dn_commit", "tv_price_init", "tv_price_lookup",
-           "tv_price_observe", "tv_staircut")
+           "tv_price_observe", "tv_staircut", "tv_packed_weight_bytes", "tv_pack_weight")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -42,7 +42,7 @@ class TvDims(ctypes.Structure):
 class TvModel(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("ln1", ctypes.c_void_p), ("wqkv", ctypes.c_void_p),
                 ("wo", ctypes.c_void_p), ("ln_f", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
-                ("dims", TvDims)]
+                ("dims", TvDims), ("packed", ctypes.c_int32)]
 
 
 class TvKv(ctypes.Structure):
@@ -96,6 +96,8 @@ def load():
                                                    I, P, P, P, P, P, P]
         lib.tv_commit_kv.argtypes = [ctypes.POINTER(TvKv), ctypes.POINTER(TvDims), ctypes.POINTER(TvTree), I,
                                      P, P, P, P, P, P]
+        lib.tv_packed_weight_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Z)]
+        lib.tv_pack_weight.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
         lib.tv_profile_start.argtypes = [I]
         lib.tv_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I), ctypes.POINTER(I)]
         lib.tv_sample_workspace_size.argtypes = [ctypes.c_int32, I, ctypes.POINTER(Z)]
@@ -156,6 +158,18 @@ def tv_workspace_size(dims: TvDims, max_rows: int, max_ctx: int) -> int:
     if rc != TV_OK:
         raise ValueError(f"tv_workspace_size: {STATUS.get(rc, rc)}")
     return int(out.value)
+
+
+def tv_packed_weight_bytes(rows: int, cols: int) -> int:
+    out = ctypes.c_size_t(0)
+    rc = load().tv_packed_weight_bytes(int(rows), int(cols), ctypes.byref(out))
+    if rc != TV_OK:
+        raise ValueError(f"tv_packed_weight_bytes: {STATUS.get(rc, rc)}")
+    return int(out.value)
+
+
+def tv_pack_weight(w, rows: int, cols: int, packed, stream=None) -> int:
+    return load().tv_pack_weight(_p(w), int(rows), int(cols), _p(packed), _stream(stream))
 
 
 def tv_verify_tree(model: TvModel, kvs: Sequence[TvKv], trees: Sequence[TvTree], logits, argmax, top2_gap,

@@ -151,6 +151,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   if (!model->embed || !model->ln1 || !model->wqkv || !model->wo || !model->ln_f || !model->lm_head)
     return TV_E_ARG;
   if (!aligned16(model->wqkv) || !aligned16(model->wo) || !aligned16(model->lm_head)) return TV_E_ARG;
+  if (model->packed != 0 && model->packed != 1) return TV_E_ARG;
   ReqTable t;
   rc = build_table(t, trees, kv, n_req, true);
   if (rc) return rc;
@@ -186,6 +187,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
   GemmParams gp;
   memset(&gp, 0, sizeof(gp));
   gp.status = dev_status;
+  gp.packed = model->packed ? 1 : 0;
 
   StageMarks pm(st);
   pm.mark(0);
@@ -443,6 +445,17 @@ int tv_profile_stop(float* stage_ms, int max_stages, int* n_stages, int* n_calls
   if (stage_ms)
     for (int s = 0; s < TV_PROFILE_STAGES && s < max_stages; ++s) stage_ms[s] = sums[s];
   return rc;
+}
+
+int tv_packed_weight_bytes(int32_t rows, int32_t cols, size_t* bytes) {
+  if (!bytes || rows < 1 || cols < 64 || cols % 64 != 0) return TV_E_ARG;
+  *bytes = (size_t)((rows + 127) / 128) * 128 * (size_t)cols * 2;
+  return TV_OK;
+}
+
+int tv_pack_weight(const tv_bf16* w, int32_t rows, int32_t cols, tv_bf16* packed, void* stream) {
+  if (!w || !packed || !aligned16(w) || !aligned16(packed) || rows < 1 || cols < 64 || cols % 64 != 0) return TV_E_ARG;
+  return launch_pack_weight(w, rows, cols, packed, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* tv_status_string(int code) {

@@ -111,6 +111,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   int pre = 0;
   int pre_u = blockIdx.x, pre_kb = 0, pre_kb1 = 0;
   uint64_t pol_w = 0, pol_x = 0;
+  // weight tile (m-tile mt, k-block kb): a box of the row-major matrix, or
+  // the tile's own contiguous 16 KB of the packed copy
+  auto load_a = [&](uint8_t* dst, uint64_t* bar, int mt, int kb) {
+    if (p.packed) tma_load_2d(dst, &mapA, bar, 0, (mt * KB + kb) * BM, pol_w);
+    else tma_load_2d(dst, &mapA, bar, kb * BK, mt * BM, pol_w);
+  };
   if (warp == 0 && lane == 0) {
     pol_w = policy_evict_first();
     pol_x = policy_evict_last();
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int u = pre_u, kb = pre_kb, kb1 = pre_kb1;
     while (pre < STAGES && u < p.n_units) {
       mbar_expect_tx(&full[pre], A_BYTES);
-      tma_load_2d(sA + (size_t)pre * A_BYTES, &mapA, &full[pre], kb * BK, (u / p.splits) * BM, pol_w);
+      load_a(sA + (size_t)pre * A_BYTES, &full[pre], u / p.splits, kb);
       ++pre;
       if (++kb >= kb1) {
         u += gridDim.x;
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
-        tma_load_2d(sA + (size_t)stage * A_BYTES, &mapA, &full[stage], kb * BK, (u / p.splits) * BM, pol_w);
+        load_a(sA + (size_t)stage * A_BYTES, &full[stage], u / p.splits, kb);
         tma_load_2d(sB + (size_t)stage * B_BYTES, &mapB, &full[stage], kb * BK, 0, pol_x);
         armed |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -414,7 +420,9 @@ int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows
                 const GemmParams& base, int num_sms, cudaStream_t stream) {
   if (K % BK != 0 || n_rows < 1 || n_rows > kMaxRows) return TV_E_UNSUPPORTED;
   CUtensorMap mA, mB;
-  int rc = make_tmap_bf16(&mA, W, K, M, BK, BM);
+  const int m_tiles = (M + BM - 1) / BM;
+  // packed: [m_tiles * (K / BK) * BM][BK], tile (mt, kb) at row (mt * K / BK + kb) * BM
+  int rc = base.packed ? make_tmap_bf16(&mA, W, BK, m_tiles * (K / BK) * BM, BK, BM) : make_tmap_bf16(&mA, W, K, M, BK, BM);
   if (rc) return rc;
   rc = make_tmap_bf16(&mB, X, K, n_rows, BK, BN);
   if (rc) return rc;
@@ -435,6 +443,31 @@ int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows
     if (ensure_smem_limit(gemm_skinny_kernel<GEMM_PARTIAL>, SMEM_BYTES, attr)) return TV_E_CUDA;
     return launch_pdl(gemm_skinny_kernel<GEMM_PARTIAL>, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, mA, mB, p);
   }
+}
+
+// one thread per 16 bytes of the packed copy: tile t = mt * KB + kb, row r,
+// 16-byte piece c of the tile's 128-byte row
+__global__ void pack_weight_kernel(const uint4* __restrict__ w, int rows, int cols, uint4* __restrict__ packed,
+                                   size_t total) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int c = (int)(i & 7);
+  const size_t rt = i >> 3;          // row of the packed view
+  const int r = (int)(rt % BM);
+  const size_t tile = rt / BM;
+  const int KB = cols / BK;
+  const int kb = (int)(tile % KB);
+  const size_t row = (tile / KB) * BM + r;
+  packed[i] = row < (size_t)rows ? w[(row * cols + (size_t)kb * BK) / 8 + c] : make_uint4(0u, 0u, 0u, 0u);
+}
+
+int launch_pack_weight(const void* W, int rows, int cols, void* packed, cudaStream_t stream) {
+  if (rows < 1 || cols < BK || cols % BK != 0) return TV_E_ARG;
+  const size_t total = (size_t)((rows + BM - 1) / BM) * BM * cols / 8;
+  const unsigned blocks = (unsigned)((total + 255) / 256);
+  pack_weight_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(W), rows, cols,
+                                                 reinterpret_cast<uint4*>(packed), total);
+  return cudaGetLastError() == cudaSuccess ? TV_OK : TV_E_CUDA;
 }
 
 }  // namespace tv

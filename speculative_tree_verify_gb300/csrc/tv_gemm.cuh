@@ -23,6 +23,7 @@ struct GemmParams {
   int32_t* argmax;           // HEAD: [n_rows]
   float* gap;                // HEAD: [n_rows]
   int32_t* status;           // sticky status word
+  int packed;                // weight in the tile-packed layout (tiles of BM x BK, row-major inside)
 };
 
 struct GemmPlan {
@@ -41,5 +42,8 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int 
 int make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d0, int d1, int d2, int b0, int b1, int b2);
 int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows, const GemmPlan& pl,
                 const GemmParams& base, int num_sms, cudaStream_t stream);
+// W [rows][cols] row-major -> the tile-packed layout (128 x 64 tiles, rows
+// padded with zeros to a multiple of 128)
+int launch_pack_weight(const void* W, int rows, int cols, void* packed, cudaStream_t stream);
 
 }  // namespace tv

@@ -29,20 +29,39 @@ def tv_dims(d: Dims) -> abi.TvDims:
                       float(d.rms_eps))
 
 
+PACKED = ("wqkv", "wo", "lm_head")
+
+
 class DeviceModel:
-    def __init__(self, dims: Dims, tensors: dict):
+    """The layer + head on the GPU.  packed=True (the default) also makes the
+    tile-packed copies of wqkv, wo and lm_head (tv_pack_weight) and hands
+    those to the verify; the row-major tensors stay in ``t``."""
+
+    def __init__(self, dims: Dims, tensors: dict, packed: bool = True):
         self.dims = dims
-        self.t = tensors    # name -> bf16 tensor on the GPU
-        self.c = abi.TvModel(*(self.t[k].data_ptr() for k in ("embed", "ln1", "wqkv", "wo", "ln_f", "lm_head")),
-                             tv_dims(dims))
+        self.t = tensors    # name -> bf16 tensor on the GPU, row-major
+        self.p = {}         # name -> packed copy (packed=True)
+        ptr = {k: self.t[k].data_ptr() for k in ("embed", "ln1", "wqkv", "wo", "ln_f", "lm_head")}
+        if packed:
+            for k in PACKED:
+                w = self.t[k]
+                rows, cols = int(w.shape[0]), int(w.shape[1])
+                buf = torch.empty(abi.tv_packed_weight_bytes(rows, cols) // 2, dtype=torch.bfloat16, device=w.device)
+                check(abi.tv_pack_weight(w, rows, cols, buf, stream=torch.cuda.current_stream(w.device)),
+                      "tv_pack_weight")
+                self.p[k] = buf
+                ptr[k] = buf.data_ptr()
+        self.packed = bool(packed)
+        self.c = abi.TvModel(*(ptr[k] for k in ("embed", "ln1", "wqkv", "wo", "ln_f", "lm_head")), tv_dims(dims),
+                             1 if packed else 0)
 
     @classmethod
-    def from_host(cls, m: Model, device="cuda") -> "DeviceModel":
+    def from_host(cls, m: Model, device="cuda", packed: bool = True) -> "DeviceModel":
         return cls(m.dims, {k: _bf16_tensor(getattr(m, k), device)
-                            for k in ("embed", "ln1", "wqkv", "wo", "ln_f", "lm_head")})
+                            for k in ("embed", "ln1", "wqkv", "wo", "ln_f", "lm_head")}, packed)
 
     @classmethod
-    def random(cls, dims: Dims, seed: int, device="cuda", std: float = 0.02) -> "DeviceModel":
+    def random(cls, dims: Dims, seed: int, device="cuda", std: float = 0.02, packed: bool = True) -> "DeviceModel":
         """Random-init weights drawn on the device (torch's generator), gains 1."""
         g = torch.Generator(device=device)
         g.manual_seed(seed)
@@ -54,7 +73,7 @@ class DeviceModel:
         t = {"embed": w(V, H), "wqkv": w(dims.qkv_out, H), "wo": w(H, dims.n_q_heads * dims.head_dim),
              "lm_head": w(V, H), "ln1": torch.ones(H, device=device, dtype=torch.bfloat16),
              "ln_f": torch.ones(H, device=device, dtype=torch.bfloat16)}
-        return cls(dims, t)
+        return cls(dims, t, packed)
 
 
 class DeviceRequest:

@@ -99,9 +99,26 @@ def test_verify_host_checks(lib):
     assert call(kvs=[abi.TvKv(FAKE + 2, FAKE, 64, 96)]) == abi.CODES["TV_E_ARG"]   # misaligned cache
     bad = synth.Dims(hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=96, vocab=1024)
     assert call(model=_model(bad)) == abi.CODES["TV_E_UNSUPPORTED"]
+    packed2 = _model()
+    packed2.packed = 2
+    assert call(model=packed2) == abi.CODES["TV_E_ARG"]                            # packed is 0 or 1
     wide = synth.Dims(hidden=512, n_q_heads=16, n_kv_heads=2, head_dim=64, vocab=1024)   # 8 heads per group
     assert call(model=_model(wide), trees=[_tree(21)], kvs=[_kv(0, 64)],
                 workspace_bytes=abi.tv_workspace_size(tv_dims(wide), 32, 64)) == abi.CODES["TV_E_UNSUPPORTED"]
+
+
+def test_packed_weight_host_checks(lib):
+    # rows padded to a multiple of 128, bf16
+    assert abi.tv_packed_weight_bytes(1, 64) == 128 * 64 * 2
+    assert abi.tv_packed_weight_bytes(300, 192) == 384 * 192 * 2
+    assert abi.tv_packed_weight_bytes(151936, 5120) == 151936 * 5120 * 2
+    for rows, cols in ((0, 64), (128, 0), (128, 96), (128, 32)):
+        with pytest.raises(ValueError, match="ARG"):
+            abi.tv_packed_weight_bytes(rows, cols)
+    assert abi.tv_pack_weight(None, 128, 64, FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_pack_weight(FAKE, 128, 64, None) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_pack_weight(FAKE + 2, 128, 64, FAKE) == abi.CODES["TV_E_ARG"]   # misaligned
+    assert abi.tv_pack_weight(FAKE, 128, 96, FAKE) == abi.CODES["TV_E_ARG"]
 
 
 def test_walk_and_commit_host_checks(lib):

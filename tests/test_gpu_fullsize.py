@@ -22,7 +22,7 @@ from speculative_tree_verify_gb300 import synth
 from speculative_tree_verify_gb300 import device as dv
 from speculative_tree_verify_gb300.device import DeviceModel
 
-from parity import KV_TOL, _ok, check_close_bf16, check_verify, greedy_replay, plant_spine, to_np
+from parity import KV_TOL, _ok, check_close_bf16, check_verify, gpu_verify, greedy_replay, plant_spine, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -57,6 +57,20 @@ def test_hidden5120_greedy_round(full_model):
     k = to_np(reqs[0].k)
     for dd, node in enumerate(path):
         check_close_bf16(orc[0]["k"][node], k[:, ctx + dd, :].reshape(-1), KV_TOL, "committed K", relative=True)
+
+
+def test_hidden5120_packed_weights_equal_row_major(full_model):
+    """The tile-packed head / QKV / O weights the benchmark streams give the
+    same bits as the row-major matrices."""
+    model, dm = full_model
+    assert dm.packed
+    rm = DeviceModel(dm.dims, dm.t, packed=False)
+    host = [(synth.gen_cache(D, 1024, 1100, 21), synth.tree_lattice(16, 7, D.vocab, 22))]
+    _, bp = gpu_verify(dm, host)
+    _, br = gpu_verify(rm, host)
+    for name in ("logits", "argmax", "gap", "attn"):
+        np.testing.assert_array_equal(to_np(getattr(bp, name)).view(np.uint8), to_np(getattr(br, name)).view(np.uint8),
+                                      err_msg=name)
 
 
 @pytest.mark.parametrize("n", [8, 16, 24, 32])

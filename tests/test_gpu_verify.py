@@ -73,6 +73,37 @@ def test_joint_verify_parity(gpu, layout):
 
 
 # ---------------------------------------------------------------------------
+# the tile-packed weights
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("rows,cols", [(1, 64), (300, 192), (128, 5120), (1000, 320)])
+def test_pack_weight_layout(gpu, rows, cols):
+    w = torch.from_numpy(np.random.default_rng(rows + cols).standard_normal((rows, cols)).astype(np.float32))
+    wt = w.to(torch.bfloat16).cuda()
+    mt = (rows + 127) // 128
+    out = torch.full((abi.tv_packed_weight_bytes(rows, cols) // 2,), float("nan"), dtype=torch.bfloat16,
+                     device="cuda")   # every element must be written
+    _ok(abi.tv_pack_weight(wt, rows, cols, out), "tv_pack_weight")
+    torch.cuda.synchronize()
+    # rows padded with zeros to 128 mt, cut into 128 x 64 tiles, tile (i, j) row-major at (i cols/64 + j) 8192
+    wp = np.zeros((mt * 128, cols), np.uint16)
+    wp[:rows] = wt.view(torch.int16).cpu().numpy().view(np.uint16)
+    want = wp.reshape(mt, 128, cols // 64, 64).transpose(0, 2, 1, 3).reshape(-1)
+    np.testing.assert_array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), want)
+
+
+@pytest.mark.parametrize("dims", ["tiny", "mid"])
+def test_packed_weights_give_the_same_verify(gpu, dims):
+    d = {"tiny": synth.TINY, "mid": synth.MID}[dims]
+    model = synth.gen_model(d, 90, random_gains=True)
+    host = [(synth.gen_cache(d, 700, 760, 91), synth.tree_lattice(24, 7, d.vocab, 92))]
+    _, bp = gpu_verify(DeviceModel.from_host(model, packed=True), host)
+    _, br = gpu_verify(DeviceModel.from_host(model, packed=False), host)
+    for name in ("logits", "argmax", "gap", "attn"):
+        a, b = to_np(getattr(bp, name)), to_np(getattr(br, name))
+        np.testing.assert_array_equal(a.view(np.uint8), b.view(np.uint8), err_msg=name)
+
+
+# ---------------------------------------------------------------------------
 # a row's results do not depend on the other rows of the pass
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dims", ["tiny", "mid"])
