@@ -218,11 +218,15 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
 }
 
 // O projection finalize: r = bf16(x + sum_s partial_s) with the splits summed in
-// order, hf = bf16(RMSNorm(r) g_f); one block per row.
-__global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(ReqTable t, int vocab, const float* part, int splits,
-                                                                 int H, const __nv_bfloat16* embed,
-                                                                 const __nv_bfloat16* g, float eps,
-                                                                 __nv_bfloat16* hf, const int32_t* status) {
+// order, hf = bf16(RMSNorm(r) g_f); one block per row, VECS 8-element vectors
+// of the row per thread (one at hidden <= 5120), every split of a vector
+// requested at once (up to eight).
+constexpr int kORowThreads = 640;
+template <int VECS>
+__global__ void __launch_bounds__(kORowThreads) o_finalize_kernel(ReqTable t, int vocab, const float* part, int splits,
+                                                                  int H, const __nv_bfloat16* embed,
+                                                                  const __nv_bfloat16* g, float eps,
+                                                                  __nv_bfloat16* hf, const int32_t* status) {
   __shared__ float red[33];
   pdl_trigger();   // the head GEMM may start streaming its weights now
   pdl_wait();
@@ -236,18 +240,18 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(ReqTable t, int
   token = token < 0 || token >= vocab ? 0 : token;
   const int nvec = H / 8;
   const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)token * H);
-  float r[kRowVecs][8];
+  float r[VECS][8];
   float ss = 0.f;
 #pragma unroll
-  for (int k = 0; k < kRowVecs; ++k) {
-    const int vi = threadIdx.x + k * kRowThreads;
+  for (int k = 0; k < VECS; ++k) {
+    const int vi = threadIdx.x + k * kORowThreads;
     if (vi < nvec) {
-      // partials summed in split order; loads issued four splits at a time
+      // partials summed in split order; loads issued eight splits at a time
       float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int s0 = 0; s0 < splits; s0 += 4) {
-        float4 pv[4][2];
+      for (int s0 = 0; s0 < splits; s0 += 8) {
+        float4 pv[8][2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           if (s0 + j < splits) {
             const float4* ps =
                 reinterpret_cast<const float4*>(part + ((size_t)(s0 + j) * kMaxRows + row) * H) + 2 * vi;
@@ -256,7 +260,7 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(ReqTable t, int
           }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           if (s0 + j < splits) {
             o[0] += pv[j][0].x; o[1] += pv[j][0].y; o[2] += pv[j][0].z; o[3] += pv[j][0].w;
             o[4] += pv[j][1].x; o[5] += pv[j][1].y; o[6] += pv[j][1].z; o[7] += pv[j][1].w;
@@ -278,8 +282,8 @@ __global__ void __launch_bounds__(kRowThreads) o_finalize_kernel(ReqTable t, int
   const uint4* gv = reinterpret_cast<const uint4*>(g);
   uint4* hv = reinterpret_cast<uint4*>(hf + (size_t)row * H);
 #pragma unroll
-  for (int k = 0; k < kRowVecs; ++k) {
-    const int vi = threadIdx.x + k * kRowThreads;
+  for (int k = 0; k < VECS; ++k) {
+    const int vi = threadIdx.x + k * kORowThreads;
     if (vi < nvec) {
       float gf[8], y[8];
       unpack8(gv[vi], gf);
@@ -333,10 +337,16 @@ int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b,
 
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st) {
-  if (m.dims.hidden > kRowVecs * kRowThreads * 8 || splits > kMaxSplits) return TV_E_UNSUPPORTED;
-  return launch_pdl(o_finalize_kernel, dim3(t.total_rows), dim3(kRowThreads), 0, st, t, m.dims.vocab,
-                    (const float*)b.part_o, splits, m.dims.hidden, reinterpret_cast<const __nv_bfloat16*>(m.embed),
-                    reinterpret_cast<const __nv_bfloat16*>(m.ln_f), m.dims.rms_eps, b.hf, (const int32_t*)status);
+  const int nvec = m.dims.hidden / 8;
+  if (nvec > 4 * kORowThreads || splits > kMaxSplits) return TV_E_UNSUPPORTED;
+  auto go = [&](auto kern) {
+    return launch_pdl(kern, dim3(t.total_rows), dim3(kORowThreads), 0, st, t, m.dims.vocab, (const float*)b.part_o,
+                      splits, m.dims.hidden, reinterpret_cast<const __nv_bfloat16*>(m.embed),
+                      reinterpret_cast<const __nv_bfloat16*>(m.ln_f), m.dims.rms_eps, b.hf, (const int32_t*)status);
+  };
+  if (nvec <= kORowThreads) return go(o_finalize_kernel<1>);
+  if (nvec <= 2 * kORowThreads) return go(o_finalize_kernel<2>);
+  return go(o_finalize_kernel<4>);
 }
 
 }  // namespace tv
