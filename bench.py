@@ -4,7 +4,8 @@
 One step = one verify round on one GPU at the hidden-5120 shapes (40/8 heads
 of 128, vocab 151936, bf16 weights ~ N(0, 0.02) drawn on the device):
 tv_verify_tree over a 16-row lattice tree (spine of 8 + 8 next-best branches)
-at 1024 tokens of context, tv_accept_greedy, tv_commit_kv.  The drafts along
+at 1024 tokens of context, tv_accept_greedy_commit (the greedy walk and the KV
+commit in one launch).  The drafts along
 the spine are teacher-forced (the GPU's own greedy tokens, planted before
 timing) so the walk and the commit do real work.  Inputs are synthetic.
 
@@ -346,7 +347,7 @@ def run_ours(args, world, rank, local):
                       "l2": "inputs larger than L2: 1.68 GB of weights stream from HBM every step",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "eager_ms_per_step": round(eager_ms, 4), "clocks": clocks,
-           "gpu_launches": 10 * args.steps, "code_sha256": _code_sha256()}
+           "gpu_launches": 9 * args.steps, "code_sha256": _code_sha256()}
     if rank != 0 or args.no_extras:
         return out if rank == 0 else None
 

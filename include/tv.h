@@ -263,6 +263,24 @@ TV_API int tv_commit_kv(const tv_kv *kv, const tv_dims *dims, const tv_tree *tre
                  int32_t *committed_src, int32_t *new_ctx, int32_t *dev_status, void *stream);
 
 /*
+ * The greedy walk and the KV commit in one launch [Drafters and tree verify,
+ * §The round, steps 3 and 4]: the outputs of tv_accept_greedy followed by
+ * tv_commit_kv on the same arguments -- path, accept_len, out_tokens,
+ * committed_src, new_ctx and the cache rows -- with one kernel instead of two.
+ * The path comes from the walk, so TV_E_PATH cannot arise.
+ *
+ *   kv, dims, trees  as tv_commit_kv (trees: the device parent/token arrays
+ *                    are read, as by tv_accept_greedy)
+ *   argmax           device int32 [total_rows], from tv_verify_tree
+ *   the rest         as those two calls
+ * Host checks: TV_E_ARG, TV_E_ROWS, TV_E_UNSUPPORTED.  Device checks:
+ * TV_E_ORDER, TV_E_DUP_SIBLING.
+ */
+TV_API int tv_accept_greedy_commit(const tv_kv *kv, const tv_dims *dims, const tv_tree *trees, int n_req,
+                                   const int32_t *argmax, int32_t *path, int32_t *accept_len, int32_t *out_tokens,
+                                   int32_t *committed_src, int32_t *new_ctx, int32_t *dev_status, void *stream);
+
+/*
  * Sampled variants [Exactness, §Sampling; Drafters and tree verify,
  * §Sampling; Algorithm and correctness contract, §Single-path sampling].
  * They read the verify's fp32 logits (or the output of tv_sample_filter with

@@ -29,7 +29,8 @@ SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept
            "tv_profile_start", "tv_profile_stop", "tv_status_string", "tv_accept_residual_noalloc",
            "tv_sample_workspace_size", "tv_sample_filter", "tv_accept_single_draw", "tv_accept_gumbel",
            "tv_accept_rejection", "tv_dn_verify_tree", "tv_dn_commit", "tv_price_init", "tv_price_lookup",
-           "tv_price_observe", "tv_staircut", "tv_packed_weight_bytes", "tv_pack_weight")
+           "tv_price_observe", "tv_staircut", "tv_packed_weight_bytes", "tv_pack_weight",
+           "tv_accept_greedy_commit")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -96,6 +97,8 @@ def load():
                                                    I, P, P, P, P, P, P]
         lib.tv_commit_kv.argtypes = [ctypes.POINTER(TvKv), ctypes.POINTER(TvDims), ctypes.POINTER(TvTree), I,
                                      P, P, P, P, P, P]
+        lib.tv_accept_greedy_commit.argtypes = [ctypes.POINTER(TvKv), ctypes.POINTER(TvDims), ctypes.POINTER(TvTree),
+                                                I, P, P, P, P, P, P, P, P]
         lib.tv_packed_weight_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(Z)]
         lib.tv_pack_weight.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P]
         lib.tv_profile_start.argtypes = [I]
@@ -158,6 +161,13 @@ def tv_workspace_size(dims: TvDims, max_rows: int, max_ctx: int) -> int:
     if rc != TV_OK:
         raise ValueError(f"tv_workspace_size: {STATUS.get(rc, rc)}")
     return int(out.value)
+
+
+def tv_accept_greedy_commit(kvs: Sequence[TvKv], dims: TvDims, trees: Sequence[TvTree], argmax, path, accept_len,
+                            out_tokens, committed_src, new_ctx, dev_status, stream=None) -> int:
+    return load().tv_accept_greedy_commit(_arr(TvKv, kvs), ctypes.byref(dims), _arr(TvTree, trees), len(trees),
+                                          _p(argmax), _p(path), _p(accept_len), _p(out_tokens), _p(committed_src),
+                                          _p(new_ctx), _p(dev_status), _stream(stream))
 
 
 def tv_packed_weight_bytes(rows: int, cols: int) -> int:

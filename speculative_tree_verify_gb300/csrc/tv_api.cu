@@ -405,6 +405,19 @@ int tv_commit_kv(const tv_kv* kv, const tv_dims* dims, const tv_tree* trees, int
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+int tv_accept_greedy_commit(const tv_kv* kv, const tv_dims* dims, const tv_tree* trees, int n_req,
+                            const int32_t* argmax, int32_t* path, int32_t* accept_len, int32_t* out_tokens,
+                            int32_t* committed_src, int32_t* new_ctx, int32_t* dev_status, void* stream) {
+  if (!kv || !dims || !argmax || !path || !accept_len || !out_tokens || !committed_src || !new_ctx || !dev_status)
+    return TV_E_ARG;
+  if (dims->n_kv_heads <= 0 || (dims->head_dim != 64 && dims->head_dim != 128)) return TV_E_UNSUPPORTED;
+  ReqTable t;
+  const int rc = build_table(t, trees, kv, n_req, true);
+  if (rc) return rc;
+  return launch_accept_greedy_commit(t, *dims, argmax, path, accept_len, out_tokens, committed_src, new_ctx,
+                                     dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int tv_profile_start(int max_calls) {
   if (max_calls < 1 || max_calls > (1 << 16)) return TV_E_ARG;
   if (g_prof.ev) return TV_E_ARG;   // already running

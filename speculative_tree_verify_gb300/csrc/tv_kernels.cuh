@@ -148,6 +148,9 @@ int launch_accept_residual(const ReqTable& t, const float* logits, int vocab, fl
                            const float* uniforms, int bonus_at_leaf, RowStat* stats, int32_t* path,
                            int32_t* accept_len, int32_t* out_tokens, int32_t* out_count, int32_t* status,
                            cudaStream_t st);
+int launch_accept_greedy_commit(const ReqTable& t, const tv_dims& d, const int32_t* argmax, int32_t* path,
+                                int32_t* accept_len, int32_t* out_tokens, int32_t* committed_src, int32_t* new_ctx,
+                                int32_t* status, cudaStream_t st);
 int launch_commit(const ReqTable& t, const tv_dims& d, const int32_t* path, const int32_t* accept_len,
                   int32_t* committed_src, int32_t* new_ctx, int32_t* status, cudaStream_t st);
 

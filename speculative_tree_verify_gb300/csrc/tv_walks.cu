@@ -62,6 +62,85 @@ __global__ void accept_greedy_kernel(ReqTable t, const int32_t* argmax, int32_t*
 }
 
 // ---------------------------------------------------------------------------
+// greedy walk + commit in one launch.  grid (Hkv, K|V, requests), block 128:
+// every block walks its request with one warp (a few hundred cycles: the
+// tree and every row's token in one round trip), block (0, K) of the request
+// writes the walk's outputs, and every block copies its (KV head, K|V) rows as
+// commit_kernel does.  The path comes from the walk, so it is in range by
+// construction.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) accept_greedy_commit_kernel(ReqTable t, int D, const int32_t* argmax,
+                                                                   int32_t* path, int32_t* accept_len,
+                                                                   int32_t* out_tokens, int32_t* committed_src,
+                                                                   int32_t* new_ctx, int32_t* status) {
+  __shared__ uint4 rows[kMaxRows * 128 * 2 / 16];
+  __shared__ int s_src[kMaxRows], s_tok[kMaxRows];
+  __shared__ int s_a;   // accepted count, -1: nothing to do
+  pdl_wait();
+  pdl_trigger();
+  const int g = blockIdx.x, which = blockIdx.y, r = blockIdx.z;
+  const int n = t.n[r], row0 = t.row_off[r], ctx = t.ctx[r];
+  const bool lead = g == 0 && which == 0;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int am = lane < n ? argmax[row0 + lane] : 0;
+    const bool prior = status_get(status) != 0;
+    int par, tok;
+    const int err = validate_tree_warp(t.parent[r], t.token[r], n, 0, par, tok);
+    if (prior || err != TV_OK) {
+      if (!prior && err != TV_OK && lead && lane == 0) status_set(status, err);
+      if (lane == 0) s_a = -1;
+    } else {
+      int cur = 0, a = 0;
+      if (lane == 0) s_src[0] = 0;
+      for (;;) {
+        const int want = __shfl_sync(FULL, am, cur);
+        const unsigned hit = __ballot_sync(FULL, lane > 0 && lane < n && par == cur && tok == want);
+        if (hit == 0u) {
+          if (lane == 0) s_tok[a] = want;   // the model's token at the stopping node
+          break;
+        }
+        const int c = __ffs(hit) - 1;
+        const int ctok = __shfl_sync(FULL, tok, c);
+        ++a;
+        if (lane == 0) {
+          s_src[a] = c;
+          s_tok[a - 1] = ctok;
+        }
+        cur = c;
+      }
+      if (lane == 0) s_a = a;
+    }
+  }
+  __syncthreads();
+  const int a = s_a;
+  if (a < 0) return;
+  if (lead) {
+    if ((int)threadIdx.x <= a) {
+      path[row0 + threadIdx.x] = s_src[threadIdx.x];
+      out_tokens[row0 + threadIdx.x] = s_tok[threadIdx.x];
+      committed_src[row0 + threadIdx.x] = ctx + s_src[threadIdx.x];
+    }
+    if (threadIdx.x == 0) {
+      accept_len[r] = a;
+      new_ctx[r] = ctx + a + 1;
+    }
+  }
+  __nv_bfloat16* base = (which ? t.v[r] : t.k[r]) + (size_t)g * t.capacity[r] * D;
+  const int vec_per_row = D / 8;
+  const int total = (a + 1) * vec_per_row;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int d = i / vec_per_row, c = i - d * vec_per_row;
+    rows[i] = *reinterpret_cast<const uint4*>(base + (size_t)(ctx + s_src[d]) * D + c * 8);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int d = i / vec_per_row, c = i - d * vec_per_row;
+    *reinterpret_cast<uint4*>(base + (size_t)(ctx + d) * D + c * 8) = rows[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Pass 1 of every sampled walk: per (row, vocab chunk) the chunk max m and,
 // per 128-token segment, sum exp((l - m) / T).  grid (chunks, rows), block
 // 256: warp w reads the chunk's tokens 512w .. 512w + 511 (its segments
@@ -677,6 +756,13 @@ int launch_accept_rejection(const ReqTable& t, const float* logits, int vocab, f
   return launch_pdl(accept_rejection_kernel, dim3(t.n_req), dim3(1024), 0, st, t, logits, vocab, inv_t, proposals,
                     uniforms, (const RowStat*)stats, (const RejStat*)rstats, nvc, path, accept_len, out_tokens,
                     out_count, status);
+}
+
+int launch_accept_greedy_commit(const ReqTable& t, const tv_dims& d, const int32_t* argmax, int32_t* path,
+                                int32_t* accept_len, int32_t* out_tokens, int32_t* committed_src, int32_t* new_ctx,
+                                int32_t* status, cudaStream_t st) {
+  return launch_pdl(accept_greedy_commit_kernel, dim3(d.n_kv_heads, 2, t.n_req), dim3(128), 0, st, t, d.head_dim,
+                    argmax, path, accept_len, out_tokens, committed_src, new_ctx, status);
 }
 
 int launch_commit(const ReqTable& t, const tv_dims& d, const int32_t* path, const int32_t* accept_len,

@@ -161,6 +161,13 @@ def commit(reqs: Sequence[DeviceRequest], b: RoundBuffers, stream=None) -> int:
                             b.accept_len, b.committed_src, b.new_ctx, b.status, stream)
 
 
+def accept_greedy_commit(reqs: Sequence[DeviceRequest], b: RoundBuffers, stream=None) -> int:
+    """The greedy walk and the commit in one launch (tv_accept_greedy_commit)."""
+    return abi.tv_accept_greedy_commit([r.kv() for r in reqs], tv_dims(b.dims), [r.tree() for r in reqs], b.argmax,
+                                       b.path, b.accept_len, b.out_tokens, b.committed_src, b.new_ctx, b.status,
+                                       stream)
+
+
 @dataclass
 class SampleBuffers:
     """Workspace and outputs of the sampled entry points (filters, single-draw,
@@ -208,10 +215,11 @@ def accept_rejection(reqs: Sequence[DeviceRequest], b: RoundBuffers, sb: SampleB
 def run_round(model: DeviceModel, reqs: Sequence[DeviceRequest], b: RoundBuffers, sampled: Optional[float] = None,
               stream=None):
     """One round on one stream: verify, accept (greedy, or residual sampling at
-    temperature ``sampled``), commit.  Raises on a host-side error code."""
+    temperature ``sampled``), commit; the greedy walk and the commit are one
+    launch (tv_accept_greedy_commit).  Raises on a host-side error code."""
     check(verify(model, reqs, b, stream), "tv_verify_tree")
     if sampled is None:
-        check(accept_greedy(reqs, b, stream), "tv_accept_greedy")
+        check(accept_greedy_commit(reqs, b, stream), "tv_accept_greedy_commit")
     else:
         check(accept_residual(reqs, b, sampled, stream=stream), "tv_accept_residual")
-    check(commit(reqs, b, stream), "tv_commit_kv")
+        check(commit(reqs, b, stream), "tv_commit_kv")

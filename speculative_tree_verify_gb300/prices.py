@@ -104,8 +104,7 @@ def measure(contexts: Sequence[int] = (1024, 4096, 8192, 16384, 32768),
 
                 def round_():
                     dv.check(dv.verify(dm, [req], b, stream=torch.cuda.current_stream()), "verify")
-                    dv.check(dv.accept_greedy([req], b, stream=torch.cuda.current_stream()), "accept")
-                    dv.check(dv.commit([req], b, stream=torch.cuda.current_stream()), "commit")
+                    dv.check(dv.accept_greedy_commit([req], b, stream=torch.cuda.current_stream()), "accept+commit")
 
                 s = torch.cuda.Stream()
                 s.wait_stream(torch.cuda.current_stream())

@@ -134,6 +134,12 @@ def test_walk_and_commit_host_checks(lib):
     dims = tv_dims(synth.TINY)
     assert abi.tv_commit_kv([_kv(64, 96)], dims, trees, None, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ARG"]
     assert abi.tv_commit_kv([_kv(64, 96)], dims, [_tree(33)], FAKE, FAKE, FAKE, FAKE, FAKE) == abi.CODES["TV_E_ROWS"]
+    assert abi.tv_accept_greedy_commit([_kv(64, 96)], dims, trees, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       FAKE) == abi.CODES["TV_E_ARG"]
+    assert abi.tv_accept_greedy_commit([_kv(64, 96)], dims, [_tree(33)], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       FAKE) == abi.CODES["TV_E_ROWS"]
+    assert abi.tv_accept_greedy_commit([_kv(90, 96)], dims, trees, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       FAKE) == abi.CODES["TV_E_CAPACITY"]
 
 
 def test_sampled_host_checks(lib):

@@ -185,6 +185,56 @@ def test_greedy_joint_round(gpu):
         off += t.n
 
 
+@pytest.mark.parametrize("dims", ["tiny", "mid"])
+def test_fused_greedy_commit_equals_the_two_calls(gpu, dims):
+    """tv_accept_greedy_commit gives the bits of tv_accept_greedy followed by
+    tv_commit_kv: walk outputs and every cache row."""
+    d = {"tiny": synth.TINY, "mid": synth.MID}[dims]
+    model = synth.gen_model(d, 450, random_gains=True)
+    host = []
+    for i in range(3):
+        c = synth.gen_cache(d, 60 + 11 * i, 140, 451 + i)
+        t = synth.tree_lattice(8 + 2 * i, 7, d.vocab, 452 + i)   # 30 rows in all
+        plant_spine(model, c, t, depth=i + 1)
+        host.append((c, t))
+    dm = DeviceModel.from_host(model)
+    reqs_a, b_a = gpu_verify(dm, host)
+    reqs_b, b_b = gpu_verify(dm, host)
+    _ok(dv.accept_greedy(reqs_a, b_a))
+    _ok(dv.commit(reqs_a, b_a))
+    _ok(dv.accept_greedy_commit(reqs_b, b_b))
+    torch.cuda.synchronize()
+    assert int(b_a.status.item()) == 0 and int(b_b.status.item()) == 0
+    rows = sum(t.n for _, t in host)
+    off = 0
+    for r, (_, t) in enumerate(host):
+        a = int(b_a.accept_len[r])
+        assert int(b_b.accept_len[r]) == a and a >= 1
+        for name in ("path", "out_tokens", "committed_src"):
+            assert to_np(getattr(b_a, name))[off:off + a + 1].tolist() == to_np(getattr(b_b, name))[off:off + a + 1].tolist(), name
+        off += t.n
+    assert to_np(b_a.new_ctx).tolist() == to_np(b_b.new_ctx).tolist()
+    for ra, rb in zip(reqs_a, reqs_b):
+        np.testing.assert_array_equal(to_np(ra.k).view(np.uint16), to_np(rb.k).view(np.uint16))
+        np.testing.assert_array_equal(to_np(ra.v).view(np.uint16), to_np(rb.v).view(np.uint16))
+    assert rows == off
+
+
+def test_fused_greedy_commit_reports_a_bad_tree(gpu):
+    d = synth.TINY
+    model = synth.gen_model(d, 460, random_gains=True)
+    cache = synth.gen_cache(d, 40, 80, 461)
+    tree = synth.tree_lattice(8, 7, d.vocab, 462)
+    dm = DeviceModel.from_host(model)
+    reqs, b = gpu_verify(dm, [(cache, tree)])
+    k0, v0 = reqs[0].k.clone(), reqs[0].v.clone()
+    reqs[0].parent[3] = 5   # parent after child: not in [0, 3)
+    _ok(dv.accept_greedy_commit(reqs, b))
+    torch.cuda.synchronize()
+    assert int(b.status.item()) == abi.CODES["TV_E_ORDER"]
+    assert torch.equal(reqs[0].k, k0) and torch.equal(reqs[0].v, v0)   # nothing committed
+
+
 # ---------------------------------------------------------------------------
 # accept walks on given logits (both sides read the same inputs)
 # ---------------------------------------------------------------------------
