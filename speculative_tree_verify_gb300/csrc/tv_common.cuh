@@ -275,12 +275,51 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ---- thread-block cluster helpers ------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; orders shared-memory writes before
+// it against reads after it, in this CTA and the others
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return (int)v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch.  Every kernel of the library is launched with
 // programmatic stream serialisation: it may start while the previous kernel in
 // the stream finishes.  Before pdl_wait() a kernel only does set-up that
 // touches no global memory written by earlier kernels, and writes no global
-// memory at all (weights, which no kernel writes, may be read).  pdl_wait()
+// memory at all (weights, which no kernel writes, may be read; so may the
+// round's trees in a kernel that starts only after the verify's first kernel
+// has completed).  pdl_wait()
 // returns once the previous grid has completed and its writes are visible;
 // since every kernel waits before it completes, that covers all earlier grids.
 // pdl_trigger() lets the next kernel start.  Kernels trigger right after their

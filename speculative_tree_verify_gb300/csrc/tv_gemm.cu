@@ -41,22 +41,31 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 32;
 constexpr int BK = 64;
-constexpr int STAGES = 8;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 64;
 constexpr int EPI_STRIDE = 33;
-constexpr size_t SMEM_TILES = (size_t)STAGES * (A_BYTES + B_BYTES);
+constexpr int kPartialStages = 8;
 constexpr size_t SMEM_BAR = 1024;
 constexpr size_t SMEM_EPI = 4 * 32 * EPI_STRIDE * sizeof(float);
 constexpr size_t SMEM_T2 = 4 * 32 * sizeof(Top2);
-constexpr size_t SMEM_BYTES = 1024 + SMEM_TILES + SMEM_BAR + SMEM_EPI + SMEM_T2;
+// Ring depth and shared memory by mode.  The head streams 1.5 GB with eight
+// 16 KB weight stages (six and ten were slower); the split-K GEMMs measured
+// the same with eight and eleven; they need no top-2 tables.
+template <int MODE>
+struct GemmCfg {
+  static constexpr int STAGES = MODE == GEMM_HEAD ? 8 : kPartialStages;
+  static constexpr size_t TILES = (size_t)STAGES * (A_BYTES + B_BYTES);
+  static constexpr size_t BYTES = 1024 + TILES + SMEM_BAR + (MODE == GEMM_HEAD ? SMEM_EPI + SMEM_T2 : 0);
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                        GemmParams p) {
+  constexpr int STAGES = GemmCfg<MODE>::STAGES;
+  constexpr size_t SMEM_TILES = GemmCfg<MODE>::TILES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -366,7 +375,7 @@ GemmPlan plan_gemm(int M, int K, bool head) {
   return pl;
 }
 
-size_t gemm_smem_bytes() { return SMEM_BYTES; }
+size_t gemm_smem_bytes() { return GemmCfg<GEMM_HEAD>::BYTES; }
 
 namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -436,12 +445,14 @@ int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows
   const int grid = pl.n_units < num_sms ? pl.n_units : num_sms;
   if (mode == GEMM_HEAD) {
     static bool attr[64] = {false};
-    if (ensure_smem_limit(gemm_skinny_kernel<GEMM_HEAD>, SMEM_BYTES, attr)) return TV_E_CUDA;
-    return launch_pdl(gemm_skinny_kernel<GEMM_HEAD>, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, mA, mB, p);
+    constexpr size_t bytes = GemmCfg<GEMM_HEAD>::BYTES;
+    if (ensure_smem_limit(gemm_skinny_kernel<GEMM_HEAD>, bytes, attr)) return TV_E_CUDA;
+    return launch_pdl(gemm_skinny_kernel<GEMM_HEAD>, dim3(grid), dim3(THREADS), bytes, stream, mA, mB, p);
   } else {
     static bool attr[64] = {false};
-    if (ensure_smem_limit(gemm_skinny_kernel<GEMM_PARTIAL>, SMEM_BYTES, attr)) return TV_E_CUDA;
-    return launch_pdl(gemm_skinny_kernel<GEMM_PARTIAL>, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, mA, mB, p);
+    constexpr size_t bytes = GemmCfg<GEMM_PARTIAL>::BYTES;
+    if (ensure_smem_limit(gemm_skinny_kernel<GEMM_PARTIAL>, bytes, attr)) return TV_E_CUDA;
+    return launch_pdl(gemm_skinny_kernel<GEMM_PARTIAL>, dim3(grid), dim3(THREADS), bytes, stream, mA, mB, p);
   }
 }
 

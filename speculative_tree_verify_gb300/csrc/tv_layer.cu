@@ -218,34 +218,49 @@ __global__ void qkv_finalize_kernel(ReqTable t, const RowMeta* meta, const float
 }
 
 // O projection finalize: r = bf16(x + sum_s partial_s) with the splits summed in
-// order, hf = bf16(RMSNorm(r) g_f); one block per row, VECS 8-element vectors
-// of the row per thread (one at hidden <= 5120), every split of a vector
-// requested at once (up to eight).
-constexpr int kORowThreads = 640;
+// order, hf = bf16(RMSNorm(r) g_f).  A cluster of kOCtas CTAs per row, each a
+// contiguous slice of the row's 8-element vectors (VECS per thread, every split
+// of a vector requested at once, up to eight), so that a row's partials stream
+// into four SMs; the sum of squares is the four CTA sums added in rank order
+// over distributed shared memory.
+constexpr int kOCtas = 4;
+constexpr int kOThreads = 160;
 template <int VECS>
-__global__ void __launch_bounds__(kORowThreads) o_finalize_kernel(ReqTable t, int vocab, const float* part, int splits,
-                                                                  int H, const __nv_bfloat16* embed,
-                                                                  const __nv_bfloat16* g, float eps,
-                                                                  __nv_bfloat16* hf, const int32_t* status) {
+__global__ void __cluster_dims__(kOCtas, 1, 1) __launch_bounds__(kOThreads)
+    o_finalize_kernel(ReqTable t, int vocab, const float* part, int splits, int H, const __nv_bfloat16* embed,
+                      const __nv_bfloat16* g, float eps, __nv_bfloat16* hf, const int32_t* status) {
   __shared__ float red[33];
-  pdl_trigger();   // the head GEMM may start streaming its weights now
-  pdl_wait();
-  // the row's token straight from its tree (clamped like the first kernel's),
-  // read with the status; nothing is written after an earlier error
-  const int row = blockIdx.x;
+  __shared__ float s_ss;   // this CTA's sum of squares
+  pdl_trigger();           // the head GEMM may start streaming its weights now
+  const int row = blockIdx.x / kOCtas;
+  const uint32_t rank = cluster_ctarank();
+  const int nvec = H / 8;
+  const int slice = (nvec + kOCtas - 1) / kOCtas;
+  const int v0 = (int)rank * slice, v1 = min(nvec, v0 + slice);
+  // Before the wait: the row's token straight from its tree (clamped like the
+  // first kernel's) and its embedding row, the residual.  Neither is written
+  // inside the round, and the tree is final: when this kernel starts, the
+  // attention kernel has passed its wait, so the verify's first kernel, which
+  // reads the tree after its own wait, has completed.
   int rq = 0;
   while (rq + 1 < t.n_req && t.row_off[rq + 1] <= row) ++rq;
   int token = t.token[rq][row - t.row_off[rq]];
-  const bool bad = status_get(status) != 0;
   token = token < 0 || token >= vocab ? 0 : token;
-  const int nvec = H / 8;
   const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)token * H);
+  uint4 xv[VECS];
+#pragma unroll
+  for (int k = 0; k < VECS; ++k) {
+    const int vi = v0 + threadIdx.x + k * kOThreads;
+    xv[k] = vi < v1 ? x[vi] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  pdl_wait();
+  const bool bad = status_get(status) != 0;   // nothing is written after an earlier error
   float r[VECS][8];
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < VECS; ++k) {
-    const int vi = threadIdx.x + k * kORowThreads;
-    if (vi < nvec) {
+    const int vi = v0 + threadIdx.x + k * kOThreads;
+    if (vi < v1) {
       // partials summed in split order; loads issued eight splits at a time
       float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int s0 = 0; s0 < splits; s0 += 8) {
@@ -268,7 +283,7 @@ __global__ void __launch_bounds__(kORowThreads) o_finalize_kernel(ReqTable t, in
         }
       }
       float xf[8];
-      unpack8(x[vi], xf);
+      unpack8(xv[k], xf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         r[k][e] = bf2f(f2bf(xf[e] + o[e]));
@@ -277,14 +292,20 @@ __global__ void __launch_bounds__(kORowThreads) o_finalize_kernel(ReqTable t, in
     }
   }
   ss = block_sum(ss, red);
+  if (threadIdx.x == 0) s_ss = ss;
+  cluster_sync_all();
+  float tot = 0.f;
+#pragma unroll
+  for (int c = 0; c < kOCtas; ++c) tot += ld_dsmem_f32(dsmem_addr(&s_ss, (uint32_t)c));
+  cluster_sync_all();   // every CTA has read the others' sums before any leaves
   if (bad) return;
-  const float inv = 1.0f / sqrtf(ss / (float)H + eps);
+  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
   const uint4* gv = reinterpret_cast<const uint4*>(g);
   uint4* hv = reinterpret_cast<uint4*>(hf + (size_t)row * H);
 #pragma unroll
   for (int k = 0; k < VECS; ++k) {
-    const int vi = threadIdx.x + k * kORowThreads;
-    if (vi < nvec) {
+    const int vi = v0 + threadIdx.x + k * kOThreads;
+    if (vi < v1) {
       float gf[8], y[8];
       unpack8(gv[vi], gf);
 #pragma unroll
@@ -338,14 +359,15 @@ int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b,
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st) {
   const int nvec = m.dims.hidden / 8;
-  if (nvec > 4 * kORowThreads || splits > kMaxSplits) return TV_E_UNSUPPORTED;
+  const int slice = (nvec + kOCtas - 1) / kOCtas;
+  if (slice > 4 * kOThreads || splits > kMaxSplits) return TV_E_UNSUPPORTED;
   auto go = [&](auto kern) {
-    return launch_pdl(kern, dim3(t.total_rows), dim3(kORowThreads), 0, st, t, m.dims.vocab, (const float*)b.part_o,
-                      splits, m.dims.hidden, reinterpret_cast<const __nv_bfloat16*>(m.embed),
+    return launch_pdl(kern, dim3(t.total_rows * kOCtas), dim3(kOThreads), 0, st, t, m.dims.vocab,
+                      (const float*)b.part_o, splits, m.dims.hidden, reinterpret_cast<const __nv_bfloat16*>(m.embed),
                       reinterpret_cast<const __nv_bfloat16*>(m.ln_f), m.dims.rms_eps, b.hf, (const int32_t*)status);
   };
-  if (nvec <= kORowThreads) return go(o_finalize_kernel<1>);
-  if (nvec <= 2 * kORowThreads) return go(o_finalize_kernel<2>);
+  if (slice <= kOThreads) return go(o_finalize_kernel<1>);
+  if (slice <= 2 * kOThreads) return go(o_finalize_kernel<2>);
   return go(o_finalize_kernel<4>);
 }
 

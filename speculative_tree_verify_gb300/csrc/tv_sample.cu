@@ -29,43 +29,6 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 
-// ---- thread-block cluster helpers ------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// every thread of every CTA of the cluster; orders shared-memory writes before
-// it against reads after it, in this CTA and the others
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t a) {
-  unsigned long long v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_dsmem_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_dsmem_u16(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared::cluster.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-  return (int)v;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-
 // ---- filter --------------------------------------------------------------------------
 constexpr int kFCluster = 8;            // CTAs per row
 constexpr int kFThreads = 512;
