@@ -756,16 +756,23 @@ __global__ void __launch_bounds__(kMergeWarps * 32) attn_merge_kernel(ReqTable t
   if (lane + 32 < nch) ml1 = __ldcg(ml + lane + 32);
   const bool skip = status_get(status) != 0;
   const float4* po = reinterpret_cast<const float4*>(part_o + base * D) + lane;
+  // the first batch of partials is requested with the offsets, before the
+  // shuffles that need them
+  float4 v[kMergeBatch];
+#pragma unroll
+  for (int i = 0; i < kMergeBatch; ++i)
+    v[i] = dl && i < nch ? __ldcg(po + (size_t)i * nv) : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = fmaxf(ml0.x, ml1.x);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int c0 = 0; c0 < nch; c0 += kMergeBatch) {   // a batch of loads in flight, then its terms in order
-    float4 v[kMergeBatch];
+    if (c0 > 0) {
 #pragma unroll
-    for (int i = 0; i < kMergeBatch; ++i)
-      v[i] = dl && c0 + i < nch ? __ldcg(po + (size_t)(c0 + i) * nv) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < kMergeBatch; ++i)
+        v[i] = dl && c0 + i < nch ? __ldcg(po + (size_t)(c0 + i) * nv) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
     for (int i = 0; i < kMergeBatch; ++i) {
       const int c = c0 + i;

@@ -98,6 +98,15 @@ __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t,
                                                                      __nv_bfloat16* h, int32_t* status) {
   __shared__ float red[33];
   pdl_trigger();   // the QKV GEMM may start streaming its weights now
+  // the norm's gain (a weight: no kernel writes it) before the wait
+  const int nvec = H / 8;
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+  uint4 gvv[kRowVecs];
+#pragma unroll
+  for (int k = 0; k < kRowVecs; ++k) {
+    const int vi = threadIdx.x + k * kRowThreads;
+    gvv[k] = (int)blockIdx.x < t.total_rows && vi < nvec ? gv[vi] : make_uint4(0u, 0u, 0u, 0u);
+  }
   pdl_wait();
   // no status check: nothing here indexes with data an earlier kernel wrote
   // (tokens are clamped), and the kernels after it check the status
@@ -116,7 +125,6 @@ __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t,
   while (r + 1 < t.n_req && t.row_off[r + 1] <= row) ++r;
   int token = t.token[r][row - t.row_off[r]];
   token = token < 0 || token >= vocab ? 0 : token;
-  const int nvec = H / 8;
   const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)token * H);
   float xf[kRowVecs][8];
   float ss = 0.f;
@@ -131,14 +139,13 @@ __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t,
   }
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-  const uint4* gv = reinterpret_cast<const uint4*>(g);
   uint4* hv = reinterpret_cast<uint4*>(h + (size_t)row * H);
 #pragma unroll
   for (int k = 0; k < kRowVecs; ++k) {
     const int vi = threadIdx.x + k * kRowThreads;
     if (vi < nvec) {
       float gf[8], y[8];
-      unpack8(gv[vi], gf);
+      unpack8(gvv[k], gf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] = xf[k][e] * inv * gf[e];
       hv[vi] = pack8(y);
@@ -247,11 +254,13 @@ __global__ void __cluster_dims__(kOCtas, 1, 1) __launch_bounds__(kOThreads)
   int token = t.token[rq][row - t.row_off[rq]];
   token = token < 0 || token >= vocab ? 0 : token;
   const uint4* x = reinterpret_cast<const uint4*>(embed + (size_t)token * H);
-  uint4 xv[VECS];
+  const uint4* gv = reinterpret_cast<const uint4*>(g);
+  uint4 xv[VECS], gvv[VECS];   // and the final norm's gain (a weight)
 #pragma unroll
   for (int k = 0; k < VECS; ++k) {
     const int vi = v0 + threadIdx.x + k * kOThreads;
     xv[k] = vi < v1 ? x[vi] : make_uint4(0u, 0u, 0u, 0u);
+    gvv[k] = vi < v1 ? gv[vi] : make_uint4(0u, 0u, 0u, 0u);
   }
   pdl_wait();
   const bool bad = status_get(status) != 0;   // nothing is written after an earlier error
@@ -300,14 +309,13 @@ __global__ void __cluster_dims__(kOCtas, 1, 1) __launch_bounds__(kOThreads)
   cluster_sync_all();   // every CTA has read the others' sums before any leaves
   if (bad) return;
   const float inv = 1.0f / sqrtf(tot / (float)H + eps);
-  const uint4* gv = reinterpret_cast<const uint4*>(g);
   uint4* hv = reinterpret_cast<uint4*>(hf + (size_t)row * H);
 #pragma unroll
   for (int k = 0; k < VECS; ++k) {
     const int vi = v0 + threadIdx.x + k * kOThreads;
     if (vi < v1) {
       float gf[8], y[8];
-      unpack8(gv[vi], gf);
+      unpack8(gvv[k], gf);
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] = r[k][e] * inv * gf[e];
       hv[vi] = pack8(y);
