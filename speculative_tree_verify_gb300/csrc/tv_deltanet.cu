@@ -34,13 +34,14 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int kDnCols = 32;        // value columns per verify CTA
-constexpr int kDnThreads = 256;    // verify CTA
+constexpr int kDnThreads = 512;    // verify CTA
+constexpr int kDnWarps = kDnThreads / 32;
 constexpr int kDnCommitThreads = 512;
 constexpr int kNodeStride = kMaxRows + 4;   // K^T / Q^T row stride: 16-byte aligned rows
 
 // dynamic shared memory of the verify CTA, in floats
 struct DnVerifyLayout {
-  int kt, qt, s0, vb, ks, qs, u, kk, c, a, total;
+  int kt, qt, s0, vb, ks, qs, u, kk, c, a, part, total;
 };
 __host__ __device__ inline DnVerifyLayout dn_verify_layout(int dk) {
   DnVerifyLayout L;
@@ -54,7 +55,8 @@ __host__ __device__ inline DnVerifyLayout dn_verify_layout(int dk) {
   L.u = o; o += kMaxRows * kDnCols;      // pseudo-values (first: partial products)
   L.kk = o; o += kMaxRows * kMaxRows;    // k_t . k_s
   L.c = o; o += kMaxRows * kMaxRows;     // q_t . k_s, then exp(gc_t - gc_s) (q_t . k_s) on t's path
-  L.a = o; o += kMaxRows * kMaxRows;     // beta_t exp(gc_t - gc_s) (k_t . k_s), s a strict ancestor (first: partials)
+  L.a = o; o += kMaxRows * kMaxRows;     // beta_t exp(gc_t - gc_s) (k_t . k_s), s a strict ancestor
+  L.part = o; o += 7 * 4 * 8 * 32;       // partial products of the d_k parts past the first
   L.total = o;
   return L;
 }
@@ -66,10 +68,12 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
   extern __shared__ __align__(16) float dsm[];
   __shared__ float s_gc[kMaxRows], s_beta[kMaxRows];
   __shared__ unsigned s_anc[kMaxRows];   // bit s: s is on t's root path (t included)
-  __shared__ int s_err;
+  __shared__ int s_err, s_stat;
   pdl_wait();
   pdl_trigger();
-  if (block_skip(status)) return;
+  // every load below is in bounds whatever an earlier kernel left; the status
+  // (an earlier error) is read with them and checked before anything is written
+  if (threadIdx.x == 0) s_stat = status_get(status);
   const int h = blockIdx.x, cb = blockIdx.y, r = blockIdx.z;
   const int n = t.n[r], row0 = t.row_off[r];
   const int kh = h / (Hv / Hk);
@@ -89,9 +93,9 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
     bl = beta[(size_t)(row0 + lane) * Hv + h];
   }
   const int c0 = cb * kDnCols;
-  constexpr int kKQ = kMaxRows * kDnMaxDim / 4 / kDnThreads;   // 4 float4 of K and of Q
-  constexpr int kSB = kDnMaxDim * kDnCols / 4 / kDnThreads;    // 4 float4 of S0
-  float4 kreg[kKQ], qreg[kKQ], sreg[kSB], vreg;
+  constexpr int kKQ = kMaxRows * kDnMaxDim / 4 / kDnThreads;   // float4 of K and of Q a thread
+  constexpr int kSB = kDnMaxDim * kDnCols / 4 / kDnThreads;    // float4 of S0 a thread
+  float4 kreg[kKQ], qreg[kKQ], sreg[kSB], vreg = make_float4(0.f, 0.f, 0.f, 0.f);
   const float* S0g = st.S[r] + (size_t)h * dk * dv;
   const int k4 = dk / 4;
 #pragma unroll
@@ -114,10 +118,9 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
     sreg[m] = idx < dk * kDnCols / 4 ? *reinterpret_cast<const float4*>(S0g + (size_t)i * dv + c0 + 4 * c)
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  {
-    const int s = threadIdx.x / (kDnCols / 4), c = threadIdx.x - s * (kDnCols / 4);   // 256 = 32 nodes x 8
-    vreg = s < n ? *reinterpret_cast<const float4*>(v + ((size_t)(row0 + s) * Hv + h) * dv + c0 + 4 * c)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (threadIdx.x < kMaxRows * kDnCols / 4) {   // 256 = 32 nodes x 8 float4
+    const int s = threadIdx.x / (kDnCols / 4), c = threadIdx.x - s * (kDnCols / 4);
+    if (s < n) vreg = *reinterpret_cast<const float4*>(v + ((size_t)(row0 + s) * Hv + h) * dv + c0 + 4 * c);
   }
 
   if (warp == 0) {   // the tree: parent order; then cumulative gates and root paths
@@ -167,24 +170,27 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
     const int idx = threadIdx.x + m * kDnThreads;
     if (idx < dk * kDnCols / 4) reinterpret_cast<float4*>(S0)[idx] = sreg[m];
   }
-  reinterpret_cast<float4*>(VB)[threadIdx.x] = vreg;
+  if (threadIdx.x < kMaxRows * kDnCols / 4) reinterpret_cast<float4*>(VB)[threadIdx.x] = vreg;
   __syncthreads();
+  if (s_stat != 0) return;
   if (s_err != TV_OK) {
     if (threadIdx.x == 0 && h == 0 && cb == 0) status_set(status, s_err);
     return;
   }
 
   // K S0, Q S0, K K^T, Q K^T.  A warp takes 4 contiguous rows (one float4 of
-  // K^T and of Q^T per coordinate) and the column lane; with n <= 16 two warps
-  // share a row group, each over half of d_k, and their sums are added.
+  // K^T and of Q^T per coordinate) and the column lane; the row groups share
+  // the 16 warps by cutting d_k into `split` parts, whose sums the first
+  // part's warps add in part order.
   {
-    const bool split = n <= 16;
-    const int rg = split ? (warp & 3) : warp;
-    const int half = split ? (warp >> 2) : 0;
-    const int i_lo = split ? half * (dk / 2) : 0, i_hi = split ? i_lo + dk / 2 : dk;
+    float* PART = dsm + L.part;
+    const int ng = (n + 3) / 4;                                // row groups of 4
+    const int split = ng <= 2 ? 8 : (ng <= 4 ? 4 : 2);         // ng * split <= 16
+    const int rg = warp % ng, part = warp / ng;
+    const bool live = part < split;
+    const int span = dk / split, i_lo = part * span, i_hi = i_lo + span;
     float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
     float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-    const bool live = 4 * rg < n;
     if (live) {
 #pragma unroll 4
       for (int i = i_lo; i < i_hi; ++i) {
@@ -202,27 +208,30 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
         }
       }
     }
-    float* P = U;   // partial sums of the second half: [4 products][16 rows][32]
-    if (split && half == 1 && live) {
+    // PART[((part - 1) 4 + product) (4 ng 32) + row 32 + lane]
+    const int pstride = 4 * ng * 32;
+    if (live && part > 0) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int tt = 4 * rg + m;
-        P[(0 * 16 + tt) * 32 + lane] = ks[m];
-        P[(1 * 16 + tt) * 32 + lane] = qs[m];
-        A[tt * 32 + lane] = kk[m];   // A doubles as the third and fourth partial arrays
-        A[(16 + tt) * 32 + lane] = qk[m];
+        float* base = PART + (size_t)(part - 1) * 4 * pstride + tt * 32 + lane;
+        base[0 * pstride] = ks[m];
+        base[1 * pstride] = qs[m];
+        base[2 * pstride] = kk[m];
+        base[3 * pstride] = qk[m];
       }
     }
-    if (split) __syncthreads();
-    if (live && half == 0) {
+    __syncthreads();
+    if (live && part == 0) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int tt = 4 * rg + m;
-        if (split) {
-          ks[m] += P[(0 * 16 + tt) * 32 + lane];
-          qs[m] += P[(1 * 16 + tt) * 32 + lane];
-          kk[m] += A[tt * 32 + lane];
-          qk[m] += A[(16 + tt) * 32 + lane];
+        for (int pp = 1; pp < split; ++pp) {
+          const float* base = PART + (size_t)(pp - 1) * 4 * pstride + tt * 32 + lane;
+          ks[m] += base[0 * pstride];
+          qs[m] += base[1 * pstride];
+          kk[m] += base[2 * pstride];
+          qk[m] += base[3 * pstride];
         }
         KS[tt * kDnCols + lane] = ks[m];
         QS[tt * kDnCols + lane] = qs[m];
@@ -269,8 +278,8 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
   __syncthreads();
   // outputs o_t = exp(gc_t) S0^T q_t + sum_s C[t][s] u_s
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int tt = warp + 8 * m;
+  for (int m = 0; m < kMaxRows / kDnWarps; ++m) {
+    const int tt = warp + kDnWarps * m;
     if (tt < n) {
       float a0 = expf(s_gc[tt]) * QS[tt * kDnCols + lane], a1 = 0.f;
       for (int s4 = 0; s4 <= tt; s4 += 4) {
