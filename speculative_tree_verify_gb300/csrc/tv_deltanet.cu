@@ -192,20 +192,33 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
     float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
     float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
     if (live) {
+      // rows in pairs through the paired fp32 FMA (each half a correctly
+      // rounded fmaf, so the sums are those of scalar fmaf)
+      float2 ks2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, qs2[2] = {ks2[0], ks2[1]};
+      float2 kk2[2] = {ks2[0], ks2[1]}, qk2[2] = {ks2[0], ks2[1]};
 #pragma unroll 4
       for (int i = i_lo; i < i_hi; ++i) {
         const float sij = S0[i * kDnCols + lane];
         const float kis = KT[i * kNodeStride + lane];
         const float4 kt4 = *reinterpret_cast<const float4*>(KT + i * kNodeStride + 4 * rg);
         const float4 qt4 = *reinterpret_cast<const float4*>(QT + i * kNodeStride + 4 * rg);
-        const float kt[4] = {kt4.x, kt4.y, kt4.z, kt4.w}, qt[4] = {qt4.x, qt4.y, qt4.z, qt4.w};
+        const float2 kt2[2] = {make_float2(kt4.x, kt4.y), make_float2(kt4.z, kt4.w)};
+        const float2 qt2[2] = {make_float2(qt4.x, qt4.y), make_float2(qt4.z, qt4.w)};
+        const float2 s2 = make_float2(sij, sij), k2 = make_float2(kis, kis);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          ks[m] = fmaf(kt[m], sij, ks[m]);
-          qs[m] = fmaf(qt[m], sij, qs[m]);
-          kk[m] = fmaf(kt[m], kis, kk[m]);
-          qk[m] = fmaf(qt[m], kis, qk[m]);
+        for (int m = 0; m < 2; ++m) {
+          ks2[m] = __ffma2_rn(kt2[m], s2, ks2[m]);
+          qs2[m] = __ffma2_rn(qt2[m], s2, qs2[m]);
+          kk2[m] = __ffma2_rn(kt2[m], k2, kk2[m]);
+          qk2[m] = __ffma2_rn(qt2[m], k2, qk2[m]);
         }
+      }
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        ks[2 * m] = ks2[m].x; ks[2 * m + 1] = ks2[m].y;
+        qs[2 * m] = qs2[m].x; qs[2 * m + 1] = qs2[m].y;
+        kk[2 * m] = kk2[m].x; kk[2 * m + 1] = kk2[m].y;
+        qk[2 * m] = qk2[m].x; qk[2 * m + 1] = qk2[m].y;
       }
     }
     // PART[((part - 1) 4 + product) (4 ng 32) + row 32 + lane]
