@@ -310,30 +310,59 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   __syncthreads();
 
-  if (MODE == GEMM_HEAD && warp == 2) {
-    Top2 b = t2s[lane];
-    for (int e = 1; e < 4; ++e) top2_merge(b, t2s[e * 32 + lane]);
-    p.top2_part[(size_t)blockIdx.x * 32 + lane] = b;
-    __threadfence();
-    unsigned prev = 0;
-    if (lane == 0) prev = atomicAdd(p.done_counter, 1u);
-    prev = __shfl_sync(0xffffffffu, prev, 0);
-    if (prev == gridDim.x - 1) {
+  if (MODE == GEMM_HEAD) {
+    // this CTA's best per activation row goes out; the CTA that finishes last
+    // merges every CTA's with its four epilogue warps (CTAs ew, ew + 4, ...,
+    // sixteen 16-byte loads in flight a lane), then warp 2 merges the four.
+    // The merge keeps the largest value and the lowest index among equal
+    // ones, so its order does not change the result.
+    __shared__ int s_last;
+    if (warp == 2) {
+      Top2 b = t2s[lane];
+      for (int e = 1; e < 4; ++e) top2_merge(b, t2s[e * 32 + lane]);
+      p.top2_part[(size_t)blockIdx.x * 32 + lane] = b;
       __threadfence();
+      unsigned prev = 0;
+      if (lane == 0) prev = atomicAdd(p.done_counter, 1u);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (lane == 0) s_last = prev == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last && warp >= 2) {
+      __threadfence();
+      const unsigned ew = (unsigned)(warp - 2);
       Top2 g;
       g.m1 = -INFINITY;
       g.i1 = INT_MAX;
       g.m2 = -INFINITY;
       g.pad = 0;
-      for (unsigned c = 0; c < gridDim.x; ++c) {
-        const Top2* src = p.top2_part + (size_t)c * 32 + lane;
-        Top2 t;
-        t.m1 = __ldcg(&src->m1);
-        t.i1 = __ldcg(&src->i1);
-        t.m2 = __ldcg(&src->m2);
-        t.pad = 0;
-        top2_merge(g, t);
+      constexpr int kBatch = 16;
+      for (unsigned c0 = ew; c0 < gridDim.x; c0 += 4 * kBatch) {
+        int4 raw[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const unsigned c = c0 + 4u * (unsigned)i;
+          raw[i] = c < gridDim.x ? __ldcg(reinterpret_cast<const int4*>(p.top2_part + (size_t)c * 32 + lane))
+                                 : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          if (c0 + 4u * (unsigned)i < gridDim.x) {
+            Top2 t;
+            t.m1 = __int_as_float(raw[i].x);
+            t.i1 = raw[i].y;
+            t.m2 = __int_as_float(raw[i].z);
+            t.pad = 0;
+            top2_merge(g, t);
+          }
+        }
       }
+      t2s[ew * 32 + lane] = g;
+    }
+    __syncthreads();
+    if (s_last && warp == 2) {
+      Top2 g = t2s[lane];
+      for (int e = 1; e < 4; ++e) top2_merge(g, t2s[e * 32 + lane]);
       if (lane < p.n_rows) {
         p.argmax[lane] = g.i1;
         p.gap[lane] = g.m1 - g.m2;
