@@ -70,6 +70,13 @@ def _dist():
     return world, rank, local
 
 
+def _max_over_ranks(vals, device):
+    """Each value's maximum over the ranks (the slowest replica's time)."""
+    t = torch.tensor(list(vals), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def _code_sha256() -> str:
     h = hashlib.sha256()
     for sub in ("include", os.path.join("speculative_tree_verify_gb300", "csrc")):
@@ -332,9 +339,7 @@ def run_ours(args, world, rank, local):
     g = _graph(round_)
     graph_ms = _time_graph(g, args.steps)
     if world > 1:
-        t = torch.tensor([graph_ms, eager_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        graph_ms, eager_ms = float(t[0]), float(t[1])
+        graph_ms, eager_ms = _max_over_ranks([graph_ms, eager_ms], dev)
         torch.distributed.barrier()
 
     out = {"metric": METRIC, "value": round(graph_ms, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
