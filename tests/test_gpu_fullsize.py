@@ -73,6 +73,29 @@ def test_hidden5120_packed_weights_equal_row_major(full_model):
                                       err_msg=name)
 
 
+def test_hidden5120_fused_walk_commit_equals_the_two_calls(full_model):
+    """The benchmark's round commits with tv_accept_greedy_commit: the same
+    walk outputs and cache rows as tv_accept_greedy then tv_commit_kv."""
+    model, dm = full_model
+    cache = synth.gen_cache(D, 1024, 1100, 31)
+    tree = synth.tree_lattice(16, 7, D.vocab, 32)
+    plant_spine(model, cache, tree, depth=4)
+    reqs_a, b_a = gpu_verify(dm, [(cache, tree)])
+    reqs_b, b_b = gpu_verify(dm, [(cache, tree)])
+    _ok(dv.accept_greedy(reqs_a, b_a))
+    _ok(dv.commit(reqs_a, b_a))
+    _ok(dv.accept_greedy_commit(reqs_b, b_b))
+    torch.cuda.synchronize()
+    assert int(b_a.status.item()) == 0 and int(b_b.status.item()) == 0
+    a = int(b_a.accept_len[0])
+    assert a >= 1 and int(b_b.accept_len[0]) == a
+    for name in ("path", "out_tokens", "committed_src"):
+        assert to_np(getattr(b_a, name))[: a + 1].tolist() == to_np(getattr(b_b, name))[: a + 1].tolist(), name
+    assert int(b_a.new_ctx[0]) == int(b_b.new_ctx[0]) == 1024 + a + 1
+    np.testing.assert_array_equal(to_np(reqs_a[0].k).view(np.uint16), to_np(reqs_b[0].k).view(np.uint16))
+    np.testing.assert_array_equal(to_np(reqs_a[0].v).view(np.uint16), to_np(reqs_b[0].v).view(np.uint16))
+
+
 @pytest.mark.parametrize("n", [8, 16, 24, 32])
 def test_hidden5120_row_sweep(full_model, n):
     model, dm = full_model
