@@ -349,9 +349,9 @@ int launch_prologue_embed(const ReqTable& t, const tv_model& m, const LayerBufs&
 
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
                         cudaStream_t st) {
-  static RopeParams cached;
-  static int cached_dim = -1;
-  static float cached_theta = 0.f;
+  thread_local RopeParams cached;   // per host thread: calls from several threads do not race
+  thread_local int cached_dim = -1;
+  thread_local float cached_theta = 0.f;
   if (cached_dim != d.head_dim || cached_theta != d.rope_theta) {
     cached = rope_params(d.head_dim, d.rope_theta);
     cached_dim = d.head_dim;
