@@ -59,15 +59,15 @@ int check_dims(const tv_dims& d) {
 }
 
 int num_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];   // 0 = not read yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  if (cache[dev] == 0) {
-    int v = 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    cache[dev] = v;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return v;
 }
 
 // ---- optional stage timing (tv_profile_*) ----------------------------------

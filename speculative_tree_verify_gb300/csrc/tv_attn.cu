@@ -815,7 +815,7 @@ int launch_attention_d(const ReqTable& t, const tv_dims& dm, const LayerBufs& b,
     nch_max = max(nch_max, attn_plan(t.ctx[r], target).n_chunks);
   }
   const size_t smem = AtSmem<D>::BYTES;
-  static bool attr[64] = {false};
+  static std::atomic<bool> attr[64];
   if (ensure_smem_limit(attn_tc_kernel<D>, smem, attr)) return TV_E_CUDA;
   dim3 grid(nch_max, dm.n_kv_heads, t.n_req);
   const float scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));   // log2(e) / sqrt(D)

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/tv.h"
@@ -353,13 +354,14 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // Host: raise a kernel's dynamic shared memory limit once per device.
 template <typename... Exp>
-inline int ensure_smem_limit(void (*kernel)(Exp...), size_t bytes, bool (&done)[64]) {
+inline int ensure_smem_limit(void (*kernel)(Exp...), size_t bytes, std::atomic<bool> (&done)[64]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TV_E_CUDA;
-  if (!done[dev]) {
+  // two host threads may both set the attribute: the call is idempotent
+  if (!done[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
       return TV_E_CUDA;
-    done[dev] = true;
+    done[dev].store(true, std::memory_order_release);
   }
   return TV_OK;
 }

@@ -495,8 +495,8 @@ __global__ void __launch_bounds__(kDnCommitThreads, 1) dn_commit_kernel(ReqTable
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-bool g_dn_verify_smem[64] = {false};
-bool g_dn_commit_smem[64] = {false};
+std::atomic<bool> g_dn_verify_smem[64];
+std::atomic<bool> g_dn_commit_smem[64];
 
 }  // namespace
 

@@ -473,12 +473,12 @@ int launch_gemm(int mode, const void* W, int M, int K, const void* X, int n_rows
   p.n_units = pl.n_units;
   const int grid = pl.n_units < num_sms ? pl.n_units : num_sms;
   if (mode == GEMM_HEAD) {
-    static bool attr[64] = {false};
+    static std::atomic<bool> attr[64];
     constexpr size_t bytes = GemmCfg<GEMM_HEAD>::BYTES;
     if (ensure_smem_limit(gemm_skinny_kernel<GEMM_HEAD>, bytes, attr)) return TV_E_CUDA;
     return launch_pdl(gemm_skinny_kernel<GEMM_HEAD>, dim3(grid), dim3(THREADS), bytes, stream, mA, mB, p);
   } else {
-    static bool attr[64] = {false};
+    static std::atomic<bool> attr[64];
     constexpr size_t bytes = GemmCfg<GEMM_PARTIAL>::BYTES;
     if (ensure_smem_limit(gemm_skinny_kernel<GEMM_PARTIAL>, bytes, attr)) return TV_E_CUDA;
     return launch_pdl(gemm_skinny_kernel<GEMM_PARTIAL>, dim3(grid), dim3(THREADS), bytes, stream, mA, mB, p);

@@ -537,7 +537,7 @@ __global__ void gumbel_pick_kernel(const GumbelPart* part, int nvc, int32_t* row
   if (lane == 0) row_tokens[row] = bi == INT_MAX ? 0 : bi;
 }
 
-bool g_filter_smem_set[64] = {false};
+std::atomic<bool> g_filter_smem_set[64];
 
 // tokens per CTA of a row's cluster (a multiple of 8, so the index array that
 // follows the slice stays 16-byte aligned)
