@@ -10,7 +10,10 @@ the spine are teacher-forced (the GPU's own greedy tokens, planted before
 timing) so the walk and the commit do real work.  Inputs are synthetic.
 
 Printed: one JSON line (rank 0).  value = ms per round from CUDA-graph replay
-(the served configuration keeps verify in graphs); the eager number, the row
+(the served configuration keeps verify in graphs), the mean over the timed
+steps; step_ms_spread gives the median and 10th/90th percentiles of single
+replays; clocks are sampled over the eager and the graph timed regions.  The
+eager number, the row
 sweep 8/16/24/32, a sampled round (residual walk), the sampled variants (filter,
 single-draw, Gumbel and rejection walks alone and in rounds), the Gated DeltaNet
 recurrent core of 48 layers and their path-state commit, per-stage times, the
@@ -230,6 +233,21 @@ def _time_graph(g, steps):
     return e0.elapsed_time(e1) / steps
 
 
+def _step_spread(g, steps):
+    """Per-replay times of a graph (an event between consecutive replays):
+    median and 10th/90th percentiles, for the spread behind the mean."""
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        g.replay()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    d = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    pick = lambda f: round(d[min(steps - 1, int(f * steps))], 4)
+    return {"median": pick(0.5), "p10": pick(0.1), "p90": pick(0.9), "samples": steps}
+
+
 def verify_bytes(D, n, ctx):
     """Algorithmic bytes one verify must move: every weight once, the cached
     K/V once, the fp32 logits once; embeddings and tree K/V rows are < 0.5 MB."""
@@ -333,11 +351,13 @@ def run_ours(args, world, rank, local):
     e1.record()
     torch.cuda.synchronize()
     eager_ms = e0.elapsed_time(e1) / args.steps
-    clocks = clk.stop()
 
-    # ---- the same round from a CUDA graph ---------------------------------------
+    # ---- the same round from a CUDA graph (the reported value); the clock
+    #      samples cover both timed regions ------------------------------------------
     g = _graph(round_)
     graph_ms = _time_graph(g, args.steps)
+    clocks = clk.stop()
+    spread = _step_spread(g, min(args.steps, 500))
     if world > 1:
         graph_ms, eager_ms = _max_over_ranks([graph_ms, eager_ms], dev)
         torch.distributed.barrier()
@@ -351,7 +371,7 @@ def run_ours(args, world, rank, local):
                       "vocab": D.vocab, "rows": rows, "ctx": ctx, "accept_len": accept_len,
                       "l2": "inputs larger than L2: 1.68 GB of weights stream from HBM every step",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-           "eager_ms_per_step": round(eager_ms, 4), "clocks": clocks,
+           "eager_ms_per_step": round(eager_ms, 4), "step_ms_spread": spread, "clocks": clocks,
            "gpu_launches": 9 * args.steps, "code_sha256": _code_sha256()}
     if rank != 0 or args.no_extras:
         return out if rank == 0 else None
