@@ -297,6 +297,35 @@ def oracle_sampled_step(oracle, model, cache, tree, r_rows, vocab_ids):
     return t1 - t0, t2 - t1
 
 
+def one_thread_round_ms(oracle, model, cache, tree, seconds):
+    """The oracle on ONE host thread: a bounded sample of the round (the layer
+    over a prefix of the tree's rows, the head over a vocabulary slice),
+    scaled to ms per full round; the median of three samples.  Returns
+    (ms, what the sample was)."""
+    n, V = tree.n, model.dims.vocab
+    prev = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        rng = np.random.default_rng(1)
+        ids = np.sort(rng.choice(V, size=min(V, 512), replace=False)).astype(np.int32)
+        r0 = min(n, 2)
+        tl, th = oracle_sampled_step(oracle, model, cache, tree, r0, ids)
+        per_row = tl / r0
+        per_rv = th / (r0 * len(ids))
+        budget = seconds / 6.0                 # three samples of a third each, half layer, half head
+        r_rows = int(max(1, min(n, (budget / 2) / max(per_row, 1e-9))))
+        s_voc = int(max(256, min(V, (budget / 2) / max(per_rv * r_rows, 1e-12))))
+        vids = np.sort(rng.choice(V, size=s_voc, replace=False)).astype(np.int32)
+        est = []
+        for _ in range(3):
+            a, h = oracle_sampled_step(oracle, model, cache, tree, r_rows, vids)
+            est.append(1e3 * (a * n / r_rows + h * (n / r_rows) * (V / s_voc)))
+    finally:
+        oracle.set_num_threads(prev)
+    return statistics.median(est), (f"1 thread: the layer over the first {r_rows} of {n} rows and the head over "
+                                    f"{s_voc} of {V} vocabulary rows, scaled to a full round; median of 3")
+
+
 def cpu_baseline(oracle, model, cache, tree, seconds):
     t0 = time.perf_counter()
     oracle_full_round(oracle, model, cache, tree)
@@ -308,9 +337,11 @@ def cpu_baseline(oracle, model, cache, tree, seconds):
         oracle_full_round(oracle, model, cache, tree)
         ts.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.median(ts)
+    ms1, sample1 = one_thread_round_ms(oracle, model, cache, tree, seconds / 2)
     return {"value": ms, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{len(ts)} full rounds (verify of all {tree.n} rows over the full vocabulary, greedy walk, "
-                      f"commit), median"}
+                      f"commit), median",
+            "value_1_thread": round(ms1, 3), "sample_1_thread": sample1}
 
 
 # ---------------------------------------------------------------------------

@@ -84,12 +84,18 @@ def _load():
         lib.orc_round_bf16.argtypes = [ctypes.c_double]
         lib.orc_round_bf16.restype = ctypes.c_uint16
         lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the following calls (for timing; results do not depend on it)."""
+    _load().orc_set_num_threads(int(n))
 
 
 def _ptr(a: Optional[np.ndarray]):

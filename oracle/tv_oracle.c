@@ -64,6 +64,16 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads for the following calls (timing only: every sum keeps its order, so
+ * the results do not depend on it). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* ---- bf16 <-> fp64 ---------------------------------------------------- */
 
 static double bf(uint16_t b) {

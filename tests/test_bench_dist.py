@@ -56,3 +56,20 @@ def test_reference_arm_under_torchrun_prints_one_line():
     out = json.loads(lines[0])
     assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
     assert out["cpu_baseline"]["kind"] == "oracle" and out["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_all_threads_and_one_thread():
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    from speculative_tree_verify_gb300 import synth
+
+    D = synth.TINY
+    model = synth.gen_model(D, 5)
+    cache = synth.gen_cache(D, 64, 128, 6)
+    tree = synth.tree_lattice(8, 4, D.vocab, 7)
+    threads = oracle.num_threads()
+    out = bench.cpu_baseline(oracle, model, cache, tree, 0.5)
+    assert out["kind"] == "oracle" and out["cores"] == threads and out["value"] > 0
+    assert out["value_1_thread"] > 0 and out["sample_1_thread"].startswith("1 thread")
+    assert oracle.num_threads() == threads   # the thread count is put back
