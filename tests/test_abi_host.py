@@ -198,3 +198,52 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(abi, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(abi.LibraryMissing):
         abi.load()
+
+
+def _param_kinds_from_header():
+    """Every prototype's parameters, each as ptr / i32 / f32 / f64 / u64."""
+    text = re.sub(r"/\*.*?\*/", " ", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"TV_API\s+[\w\s\*]*?\b(tv_\w+)\s*\(([^)]*)\)\s*;", text):
+        kinds = []
+        for p in (x.strip() for x in params.split(",")):
+            if not p or p == "void":
+                continue
+            if "*" in p:
+                kinds.append("ptr")
+            elif re.match(r"(const\s+)?(int|int32_t)\b", p):
+                kinds.append("i32")
+            elif re.match(r"(const\s+)?float\b", p):
+                kinds.append("f32")
+            elif re.match(r"(const\s+)?double\b", p):
+                kinds.append("f64")
+            elif re.match(r"(const\s+)?(size_t|uint64_t)\b", p):
+                kinds.append("u64")
+            else:
+                raise AssertionError(f"{name}: unclassified parameter {p!r}")
+        out[name] = kinds
+    return out
+
+
+def _ctypes_kind(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    if t in (ctypes.c_int, ctypes.c_int32):
+        return "i32"
+    if t is ctypes.c_float:
+        return "f32"
+    if t is ctypes.c_double:
+        return "f64"
+    if t in (ctypes.c_size_t, ctypes.c_uint64):
+        return "u64"
+    raise AssertionError(f"unclassified ctypes type {t}")
+
+
+def test_binding_signatures_match_the_header(lib):
+    """The binding's ctypes argument lists agree with include/tv.h parameter
+    by parameter, so a prototype change cannot leave a stale binding."""
+    header = _param_kinds_from_header()
+    assert sorted(header) == _declared()
+    for name, kinds in header.items():
+        got = [_ctypes_kind(t) for t in getattr(lib, name).argtypes]
+        assert got == kinds, (name, got, kinds)
