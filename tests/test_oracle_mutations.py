@@ -1,0 +1,108 @@
+"""The forward pins catch plausible mistakes in the C oracle.
+
+Each case plants one mistake in a copy of ``oracle/tv_oracle.c`` (a textual
+edit that must match exactly once), builds the copy, points the oracle module
+at it and runs two pins on a small layer with random norm gains:
+
+* chain pin -- a chain's rows equal an independent torch-fp64 layer
+  (rms_norm, linear, complex-exponential RoPE, scaled_dot_product_attention)
+  bit for bit in every bf16 store;
+* tree pin -- every row of a branched tree equals plain sequential decoding of
+  the row's own root path, bit for bit.
+
+The unedited copy passes both; every edited copy must fail at least one.  All
+of it runs on the CPU.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_tree_verify_gb300 import synth
+from test_oracle_forward import _check_tree_against_decode, torch_layer_over_sequence
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "tv_oracle.c")
+
+# (name, exact text in the oracle, the planted mistake)
+MUTATIONS = [
+    ("rope_sign", "x[d] = x1 * c - x2 * s;", "x[d] = x1 * c + x2 * s;"),
+    ("position_is_index", "(long)ctx + depth[i],", "(long)ctx + i,"),
+    ("depth_from_previous_row", "depth[parent[i]] + 1", "depth[i - 1] + 1"),
+    ("no_attention_scale", "s[j] = dot * scale;", "s[j] = dot;"),
+    ("no_residual", "rb(x[c] + dot_w(m->wo", "rb(dot_w(m->wo"),
+    ("dropped_norm_gain", "y[k] = rb(x[k] * inv * bf(g[k]));", "y[k] = rb(x[k] * inv);"),
+    ("no_self_key", "for (int a = i; a >= 0; a = parent[a]) path[len++] = a;",
+     "for (int a = parent[i]; a >= 0; a = parent[a]) path[len++] = a;"),
+    ("gqa_head_map", "const int g = hq / group;", "const int g = hq % Hkv;"),
+    ("no_norm_eps", "sqrt(ss / (double)H + eps)", "sqrt(ss / (double)H)"),
+    ("qkv_store_scaled", "for (int d = 0; d < D; ++d) dst[d] = orc_round_bf16(t[d]);",
+     "for (int d = 0; d < D; ++d) dst[d] = orc_round_bf16((float)t[d] * 1.0009765625f);"),
+]
+
+
+def _build_copy(tmp_path, name, old=None, new=None):
+    text = open(SRC).read()
+    if old is not None:
+        assert text.count(old) == 1, f"{name}: the text to edit must occur exactly once"
+        text = text.replace(old, new)
+    src = tmp_path / f"{name}.c"
+    lib = tmp_path / f"lib{name}.so"
+    src.write_text(text)
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+    try:
+        subprocess.run(base + ["-fopenmp", str(src), "-o", str(lib), "-lm"], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + [str(src), "-o", str(lib), "-lm"], check=True)
+    return str(lib)
+
+
+def _use(monkeypatch, lib_path):
+    monkeypatch.setattr(oracle, "build", lambda force=False: lib_path)
+    monkeypatch.setattr(oracle, "_LIB_PATH", lib_path)
+    monkeypatch.setattr(oracle, "_lib", None)
+
+
+def _chain_pin():
+    d = synth.TINY
+    model = synth.gen_model(d, 0, random_gains=True)
+    cache = synth.gen_cache(d, 64, 75, 50)
+    tree = synth.tree_chain(8, d.vocab, 60)
+    got = oracle.verify_tree(model, cache, tree)
+    ref = torch_layer_over_sequence(model, cache, [int(t) for t in tree.token])
+    for key in ("k", "v", "attn", "hf"):
+        assert np.count_nonzero(got[key] != ref[key]) == 0, key
+    np.testing.assert_allclose(got["logits"], ref["logits"], rtol=3e-7, atol=1e-8)
+
+
+def _tree_pin():
+    d = synth.TINY
+    model = synth.gen_model(d, 101, random_gains=True)
+    cache = synth.gen_cache(d, 64, 128, 201)
+    tree = synth.tree_spine_random(12, 4, d.vocab, 301)
+    assert any(int(tree.parent[i]) != i - 1 for i in range(1, tree.n))   # branched
+    _check_tree_against_decode(model, cache, tree)
+
+
+def _failed_pins():
+    failed = []
+    for name, pin in (("chain", _chain_pin), ("tree", _tree_pin)):
+        try:
+            with np.errstate(all="ignore"):
+                pin()
+        except AssertionError:
+            failed.append(name)
+    return failed
+
+
+def test_unedited_copy_passes_the_pins(tmp_path, monkeypatch):
+    _use(monkeypatch, _build_copy(tmp_path, "unedited"))
+    assert _failed_pins() == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_fails_a_pin(tmp_path, monkeypatch, name, old, new):
+    _use(monkeypatch, _build_copy(tmp_path, name, old, new))
+    assert _failed_pins(), f"planted mistake {name} passed every forward pin"
