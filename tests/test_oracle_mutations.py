@@ -13,7 +13,6 @@ at it and runs two pins on a small layer with random norm gains:
 The unedited copy passes both; every edited copy must fail at least one.  All
 of it runs on the CPU.
 """
-import ctypes
 import os
 import subprocess
 
@@ -106,3 +105,62 @@ def test_unedited_copy_passes_the_pins(tmp_path, monkeypatch):
 def test_planted_mistake_fails_a_pin(tmp_path, monkeypatch, name, old, new):
     _use(monkeypatch, _build_copy(tmp_path, name, old, new))
     assert _failed_pins(), f"planted mistake {name} passed every forward pin"
+
+
+# --------------------------------------------------------------------------
+# the Gated DeltaNet oracle (oracle/deltanet.py) against its pins
+# --------------------------------------------------------------------------
+import inspect  # noqa: E402
+import types  # noqa: E402
+
+import test_oracle_deltanet as DNT  # noqa: E402
+from oracle import deltanet as DN_REAL  # noqa: E402
+
+DN_MUTATIONS = [
+    ("dropped_decay", "S_new = np.exp(g) * (S - beta * np.outer(k, k @ S))", "S_new = (S - beta * np.outer(k, k @ S))"),
+    ("flipped_erase_sign", "(S - beta * np.outer(k, k @ S))", "(S + beta * np.outer(k, k @ S))"),
+    ("unscaled_write", "+ beta * np.outer(k, v)", "+ np.outer(k, v)"),
+    ("previous_row_not_parent", "else states[parent[t]]", "else states[t - 1]"),
+    ("wrong_head_map", "return h // (n_v_heads // n_k_heads)", "return h % n_k_heads"),
+    ("output_before_update", "return S_new, S_new.T @ q", "return S_new, S.T @ q"),
+    ("commit_keeps_the_root", "states[path[-1]]", "states[path[0]]"),
+]
+
+
+def _deltanet_copy(old=None, new=None):
+    text = inspect.getsource(DN_REAL)
+    if old is not None:
+        assert text.count(old) == 1, f"the text to edit must occur exactly once: {old!r}"
+        text = text.replace(old, new)
+    mod = types.ModuleType("deltanet_copy")
+    exec(compile(text, "deltanet_copy", "exec"), mod.__dict__)
+    return mod
+
+
+def _deltanet_pins_failed():
+    failed = []
+    for name, fn in inspect.getmembers(DNT, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        params = getattr(fn, "pytestmark", [])
+        cases = [dict(zip([a.strip() for a in m.args[0].split(",")], vals if isinstance(vals, tuple) else (vals,)))
+                 for m in params if m.name == "parametrize" for vals in m.args[1]] or [{}]
+        for kw in cases:
+            try:
+                with np.errstate(all="ignore"):
+                    fn(**kw)
+            except AssertionError:
+                failed.append(name)
+                break
+    return failed
+
+
+def test_unedited_deltanet_copy_passes_the_pins(monkeypatch):
+    monkeypatch.setattr(DNT, "DN", _deltanet_copy())
+    assert _deltanet_pins_failed() == []
+
+
+@pytest.mark.parametrize("name,old,new", DN_MUTATIONS, ids=[m[0] for m in DN_MUTATIONS])
+def test_planted_deltanet_mistake_fails_a_pin(monkeypatch, name, old, new):
+    monkeypatch.setattr(DNT, "DN", _deltanet_copy(old, new))
+    assert _deltanet_pins_failed(), f"planted mistake {name} passed every DeltaNet pin"
