@@ -127,32 +127,46 @@ DN_MUTATIONS = [
 ]
 
 
-def _deltanet_copy(old=None, new=None):
-    text = inspect.getsource(DN_REAL)
+def _module_copy(real, old=None, new=None):
+    """A fresh module built from ``real``'s source with one textual edit."""
+    text = inspect.getsource(real)
     if old is not None:
         assert text.count(old) == 1, f"the text to edit must occur exactly once: {old!r}"
         text = text.replace(old, new)
-    mod = types.ModuleType("deltanet_copy")
-    exec(compile(text, "deltanet_copy", "exec"), mod.__dict__)
+    mod = types.ModuleType(real.__name__ + "_copy")
+    mod.__file__ = real.__file__          # the copy finds the same C sources and library
+    exec(compile(text, mod.__name__, "exec"), mod.__dict__)
     return mod
 
 
-def _deltanet_pins_failed():
+def _deltanet_copy(old=None, new=None):
+    return _module_copy(DN_REAL, old, new)
+
+
+def _pins_failed(test_module, skip_slow=False):
+    """Runs every test function of ``test_module`` (each parametrisation) and
+    returns the names of those that fail an assertion."""
     failed = []
-    for name, fn in inspect.getmembers(DNT, inspect.isfunction):
+    for name, fn in inspect.getmembers(test_module, inspect.isfunction):
         if not name.startswith("test_"):
             continue
-        params = getattr(fn, "pytestmark", [])
+        marks = getattr(fn, "pytestmark", [])
+        if skip_slow and any(m.name == "slow" for m in marks):
+            continue
         cases = [dict(zip([a.strip() for a in m.args[0].split(",")], vals if isinstance(vals, tuple) else (vals,)))
-                 for m in params if m.name == "parametrize" for vals in m.args[1]] or [{}]
+                 for m in marks if m.name == "parametrize" for vals in m.args[1]] or [{}]
         for kw in cases:
             try:
                 with np.errstate(all="ignore"):
                     fn(**kw)
-            except AssertionError:
+            except Exception:             # a failed assertion, or a pin that cannot run
                 failed.append(name)
                 break
     return failed
+
+
+def _deltanet_pins_failed():
+    return _pins_failed(DNT)
 
 
 def test_unedited_deltanet_copy_passes_the_pins(monkeypatch):
@@ -164,3 +178,38 @@ def test_unedited_deltanet_copy_passes_the_pins(monkeypatch):
 def test_planted_deltanet_mistake_fails_a_pin(monkeypatch, name, old, new):
     monkeypatch.setattr(DNT, "DN", _deltanet_copy(old, new))
     assert _deltanet_pins_failed(), f"planted mistake {name} passed every DeltaNet pin"
+
+
+# --------------------------------------------------------------------------
+# the walk and commit oracles (oracle/__init__.py) against their pins
+# --------------------------------------------------------------------------
+import test_oracle_walks as WT  # noqa: E402
+
+# mistakes that would loop forever (a walk that never leaves the root's
+# children) are left out: the harness runs pins, not a watchdog
+WALK_MUTATIONS = [
+    ("greedy_no_bonus", "out = [int(token[c]) for c in path[1:]] + [t]", "out = [int(token[c]) for c in path[1:]]"),
+    ("greedy_first_child", "nxt = next((c for c in kids[cur] if int(token[c]) == t), None)",
+     "nxt = next((c for c in kids[cur]), None)"),
+    ("residual_no_renormalise", "r = r / r.sum()", "r = r"),
+    ("residual_no_removal", "r[x] = 0.0                      # remove x and renormalise", "r[x] = r[x]"),
+    ("residual_tests_against_p", "ok = u < r[x]", "ok = u < p[x]"),
+    ("residual_draw_from_p", "y = inverse_cdf(r, u)", "y = inverse_cdf(p, u)"),
+    ("inverse_cdf_off_by_one", 'y = int(np.searchsorted(c, float(u) * c[-1], side="right"))',
+     'y = int(np.searchsorted(c, float(u) * c[-1], side="right")) - 1'),
+    ("softmax_ignores_temperature", "z = np.asarray(logits_row, np.float64) / float(temperature)",
+     "z = np.asarray(logits_row, np.float64)"),
+    ("leaf_bonus_ignored", "if kids[cur] or bonus_at_leaf:", "if kids[cur]:"),
+    ("commit_ignores_path", "src = [ctx + int(p) for p in path]", "src = [ctx + d for d in range(len(path))]"),
+]
+
+
+def test_unedited_walk_copy_passes_the_pins(monkeypatch):
+    monkeypatch.setattr(WT, "oracle", _module_copy(oracle))
+    assert _pins_failed(WT, skip_slow=True) == []
+
+
+@pytest.mark.parametrize("name,old,new", WALK_MUTATIONS, ids=[m[0] for m in WALK_MUTATIONS])
+def test_planted_walk_mistake_fails_a_pin(monkeypatch, name, old, new):
+    monkeypatch.setattr(WT, "oracle", _module_copy(oracle, old, new))
+    assert _pins_failed(WT, skip_slow=True), f"planted mistake {name} passed every walk pin"
