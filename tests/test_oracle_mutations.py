@@ -135,6 +135,7 @@ def _module_copy(real, old=None, new=None):
         text = text.replace(old, new)
     mod = types.ModuleType(real.__name__ + "_copy")
     mod.__file__ = real.__file__          # the copy finds the same C sources and library
+    mod.__package__ = real.__package__    # and resolves relative imports in the same package
     exec(compile(text, mod.__name__, "exec"), mod.__dict__)
     return mod
 
@@ -143,13 +144,16 @@ def _deltanet_copy(old=None, new=None):
     return _module_copy(DN_REAL, old, new)
 
 
-def _pins_failed(test_module, skip_slow=False):
+def _pins_failed(test_module, skip_slow=False, first_only=False, last=()):
     """Runs every test function of ``test_module`` (each parametrisation) and
-    returns the names of those that fail an assertion."""
+    returns the names of those that fail.  ``last`` names pins to run after
+    the others; ``first_only`` stops at the first failure."""
     failed = []
-    for name, fn in inspect.getmembers(test_module, inspect.isfunction):
-        if not name.startswith("test_"):
-            continue
+    fns = [(n, f) for n, f in inspect.getmembers(test_module, inspect.isfunction) if n.startswith("test_")]
+    fns.sort(key=lambda nf: nf[0] in last)
+    for name, fn in fns:
+        if first_only and failed:
+            break
         marks = getattr(fn, "pytestmark", [])
         if skip_slow and any(m.name == "slow" for m in marks):
             continue
@@ -213,3 +217,74 @@ def test_unedited_walk_copy_passes_the_pins(monkeypatch):
 def test_planted_walk_mistake_fails_a_pin(monkeypatch, name, old, new):
     monkeypatch.setattr(WT, "oracle", _module_copy(oracle, old, new))
     assert _pins_failed(WT, skip_slow=True), f"planted mistake {name} passed every walk pin"
+
+
+# --------------------------------------------------------------------------
+# the sampled-variant oracles (oracle/sampling.py) against their pins
+# --------------------------------------------------------------------------
+import test_oracle_sampling as ST  # noqa: E402
+from oracle import sampling as SAMPLING_REAL  # noqa: E402
+
+SAMPLING_SLOW = ("test_single_draw_exact_grid_law", "test_rejection_chain_output_follows_the_target",
+                 "test_single_draw_and_residual_walk_share_one_law")
+SAMPLING_MUTATIONS = [
+    ("filter_ignores_temperature", "x = np.asarray(logits_row, np.float64) / float(temperature)",
+     "x = np.asarray(logits_row, np.float64)"),
+    ("top_k_off_by_one", "[::-1][top_k - 1]", "[::-1][top_k]"),
+    ("top_p_drops_the_cut_token", "keep &= p >= p[order[cut]]", "keep &= p > p[order[cut]]"),
+    ("min_p_not_relative_to_max", "keep &= x >= xm + np.log(min_p)", "keep &= x >= np.log(min_p)"),
+    ("philox_wrong_key_bump", "k0 = (k0 + np.uint64(_W0)) & mask", "k0 = (k0 + np.uint64(_W1)) & mask"),
+    ("philox_swapped_products", "c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0",
+     "c0, c1, c2, c3 = hi0 ^ c1 ^ k0, lo0, hi1 ^ c3 ^ k1, lo1"),
+    ("gumbel_noise_sign", "return x - np.log(-np.log(u))", "return x + np.log(-np.log(u))"),
+    ("gumbel_position_off_by_one", "gumbel_draw(rows_x[cur], seed, ctx + depth[cur] + 1)",
+     "gumbel_draw(rows_x[cur], seed, ctx + depth[cur])"),
+    ("gumbel_uniform_not_centred", "return (w.astype(np.float64) + 0.5) / 4294967296.0",
+     "return (w.astype(np.float64) + 1.0) / 4294967296.0"),
+    ("rejection_ratio_inverted", "ratio = p[x] / q[x]", "ratio = q[x] / p[x]"),
+    ("rejection_draws_from_p", "r = np.maximum(p - q, 0.0)", "r = p"),
+]
+# Which uniform a row consumes is a convention the laws cannot see (any
+# independent uniform gives the same law): the GPU parity tests pin it.
+
+
+def test_unedited_sampling_copy_passes_the_pins(monkeypatch):
+    monkeypatch.setattr(ST, "S", _module_copy(SAMPLING_REAL))
+    assert _pins_failed(ST) == []
+
+
+@pytest.mark.parametrize("name,old,new", SAMPLING_MUTATIONS, ids=[m[0] for m in SAMPLING_MUTATIONS])
+def test_planted_sampling_mistake_fails_a_pin(monkeypatch, name, old, new):
+    monkeypatch.setattr(ST, "S", _module_copy(SAMPLING_REAL, old, new))
+    assert _pins_failed(ST, first_only=True, last=SAMPLING_SLOW), f"planted mistake {name} passed every pin"
+
+
+# --------------------------------------------------------------------------
+# the price and StairCut oracles (oracle/policy.py) against their pins
+# --------------------------------------------------------------------------
+import test_oracle_policy as PT  # noqa: E402
+from oracle import policy as POLICY_REAL  # noqa: E402
+
+POLICY_MUTATIONS = [
+    ("ema_weight", "EMA = 0.1", "EMA = 0.2"),
+    ("cut_counts_taken_as_rows", "CUT_NODES = (7, 15, 23, 31)", "CUT_NODES = (8, 16, 24, 32)"),
+    ("price_may_fall", "return max(self.current(c, kind, r) for r in range(1, rows + 1))",
+     "return self.current(c, kind, rows)"),
+    ("nearest_upper_class", "lower = [c for c in keys if c <= context]", "lower = [c for c in keys if c >= context][:1]"),
+    ("rows_without_the_root", "cost = prices.price(context, kind, cnt + 1) + draft_ms",
+     "cost = prices.price(context, kind, cnt) + draft_ms"),
+    ("children_before_ancestors", "for a in reversed(chain):", "for a in chain:"),
+    ("rollback_not_weighted", "cost += (1.0 - q_last) * rollback_ms", "cost += rollback_ms"),
+    ("offset_never_learned", "self.offset[(c, kind)] = off + EMA * ((ms - prior) - off)", "self.offset[(c, kind)] = off"),
+]
+
+
+def test_unedited_policy_copy_passes_the_pins(monkeypatch):
+    monkeypatch.setattr(PT, "P", _module_copy(POLICY_REAL))
+    assert _pins_failed(PT) == []
+
+
+@pytest.mark.parametrize("name,old,new", POLICY_MUTATIONS, ids=[m[0] for m in POLICY_MUTATIONS])
+def test_planted_policy_mistake_fails_a_pin(monkeypatch, name, old, new):
+    monkeypatch.setattr(PT, "P", _module_copy(POLICY_REAL, old, new))
+    assert _pins_failed(PT), f"planted mistake {name} passed every price/StairCut pin"
