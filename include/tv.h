@@ -232,8 +232,11 @@ TV_API int tv_accept_residual(const tv_tree *trees, int n_req, const float *logi
  * per-row softmax statistics live instead in a 272 KB array inside the
  * library's device image (one per GPU, held until the process exits), so:
  *   - vocab may be at most 262144 (TV_E_UNSUPPORTED above that);
- *   - the first call on a device looks up that array's address
- *     (cudaGetSymbolAddress) -- make it before any stream capture;
+ *   - every call looks up that array's address in the context current on
+ *     the calling thread (cudaGetSymbolAddress, a host-side lookup; nothing
+ *     is cached, so another context or a reset device never sees a stale
+ *     address); the first call in a context also loads the library's device
+ *     image there -- make it before any stream capture;
  *   - all calls on a device share the array: calls whose kernels overlap on the
  *     GPU race; order them on one stream.
  * Nothing is allocated.  Arguments and errors as tv_accept_residual.

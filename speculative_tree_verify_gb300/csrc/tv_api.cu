@@ -94,6 +94,8 @@ struct StageMarks {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 // Fills the request table from host structs.  kv may be null (walks).
 int build_table(ReqTable& t, const tv_tree* trees, const tv_kv* kv, int n_req, bool need_parent) {
   if (!trees || n_req < 1 || n_req > kMaxReq) return n_req < 1 || n_req > kMaxReq ? TV_E_ROWS : TV_E_ARG;
@@ -125,7 +127,6 @@ int build_table(ReqTable& t, const tv_tree* trees, const tv_kv* kv, int n_req, b
   return TV_OK;
 }
 
-}  // namespace
 }  // namespace tv
 
 using namespace tv;

@@ -107,6 +107,13 @@ __device__ __forceinline__ int validate_tree_warp(const int32_t* parent, const i
   return check_tree_warp(par, tok, n, vocab);
 }
 
+// ---- host argument checks (tv_api.cu) ------------------------------------------
+// Fills the request table from the caller's host structs and checks them:
+// TV_E_ROWS for a tree size outside 1..32 or more than 32 rows in all,
+// TV_E_ARG for missing parent/token pointers (when need_parent) or bad caches,
+// TV_E_CAPACITY when a cache cannot hold its tree.  kv may be null (walks).
+int build_table(ReqTable& t, const tv_tree* trees, const tv_kv* kv, int n_req, bool need_parent);
+
 // ---- launchers (host) -------------------------------------------------------
 // RoPE frequencies theta^(-2d/D), computed in double on the host and split
 // into hi + lo floats, and 2*pi split into two floats for the reduction.

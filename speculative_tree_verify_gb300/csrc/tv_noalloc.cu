@@ -20,12 +20,15 @@
 // device share it, so two calls whose kernels overlap on the GPU (different
 // streams without ordering between them) race on it.
 //
-// The host needs the array's device address to pass it to the kernels; the
-// first call on each device looks it up with cudaGetSymbolAddress (with that
-// device current) and caches it.  Make that first call before any stream
-// capture.  No call allocates memory.
+// The host needs the array's device address to pass it to the kernels.  Each
+// call looks it up with cudaGetSymbolAddress in the context current on the
+// calling thread: a host-side table lookup that allocates nothing.  Nothing is
+// cached, so a call made after cudaDeviceReset, or with another context
+// current (a host framework's own driver-API context), gets that context's
+// copy of the array and never a stale address.  The first call in a context
+// also loads the library's device image there: make that call before any
+// stream capture.  No call allocates memory.
 #include <cmath>
-#include <cstring>
 
 #include "tv_common.cuh"
 #include "tv_kernels.cuh"
@@ -40,19 +43,11 @@ static_assert(sizeof(g_residual_stats) == 272 * 1024, "the size the header docum
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-RowStat* g_stats_addr[kMaxDevices] = {nullptr};
-
-// Device address of g_residual_stats on the current device (looked up once).
+// Device address of g_residual_stats in the current context.
 int stats_address(RowStat** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TV_E_CUDA;
-  if (!g_stats_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_residual_stats) != cudaSuccess || !p) return TV_E_CUDA;
-    g_stats_addr[dev] = static_cast<RowStat*>(p);
-  }
-  *out = g_stats_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_residual_stats) != cudaSuccess || !p) return TV_E_CUDA;
+  *out = static_cast<RowStat*>(p);
   return TV_OK;
 }
 
@@ -69,27 +64,11 @@ extern "C" int tv_accept_residual_noalloc(const tv_tree* trees, int n_req, const
   if (!logits || !uniforms || !path || !accept_len || !out_tokens || !out_count || !dev_status || vocab < 2)
     return TV_E_ARG;
   if (vocab > kNoAllocMaxVocab) return TV_E_UNSUPPORTED;
-  if (!trees || n_req < 1 || n_req > kMaxReq) return n_req < 1 || n_req > kMaxReq ? TV_E_ROWS : TV_E_ARG;
   ReqTable t;
-  memset(&t, 0, sizeof(t));
-  t.n_req = n_req;
-  int total = 0;
-  for (int r = 0; r < n_req; ++r) {
-    const int n = trees[r].n;
-    if (n < 1 || n > kMaxRows) return TV_E_ROWS;
-    if (!trees[r].parent || !trees[r].token) return TV_E_ARG;
-    t.row_off[r] = total;
-    t.n[r] = n;
-    t.parent[r] = trees[r].parent;
-    t.token[r] = trees[r].token;
-    total += n;
-    if (total > kMaxRows) return TV_E_ROWS;
-  }
-  t.row_off[n_req] = total;
-  t.total_rows = total;
-  RowStat* stats = nullptr;
-  const int rc = stats_address(&stats);
+  int rc = build_table(t, trees, nullptr, n_req, true);
   if (rc != TV_OK) return rc;
+  RowStat* stats = nullptr;
+  if ((rc = stats_address(&stats)) != TV_OK) return rc;
   return launch_accept_residual(t, logits, vocab, temperature, uniforms, bonus_at_leaf ? 1 : 0, stats, path,
                                 accept_len, out_tokens, out_count, dev_status, reinterpret_cast<cudaStream_t>(stream));
 }

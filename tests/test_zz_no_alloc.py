@@ -60,8 +60,13 @@ def test_noalloc_walk_matches_workspace_walk(gpu, V):
         rc = abi.tv_accept_residual(tt, ref.logits, V, 1.0, ref.uniforms, True, ref.path, ref.accept_len,
                                     ref.out_tokens, ref.out_count, ref.status, ref.ws, ref.ws.numel())
         assert rc == abi.TV_OK
+        # the second call runs on a stream of its own: the entry point takes the
+        # caller's stream and needs nothing else from it
+        side = torch.cuda.Stream() if call == 1 else None
+        if side is not None:
+            side.wait_stream(torch.cuda.current_stream())
         rc = abi.tv_accept_residual_noalloc(tt, new.logits, V, 1.0, new.uniforms, True, new.path, new.accept_len,
-                                            new.out_tokens, new.out_count, new.status)
+                                            new.out_tokens, new.out_count, new.status, stream=side)
         assert rc == abi.TV_OK
         torch.cuda.synchronize()
         assert int(ref.status.item()) == 0 and int(new.status.item()) == 0
