@@ -81,6 +81,7 @@ def _load():
         lib.orc_verify_tree.argtypes = [ctypes.POINTER(_Model), P, P, I, I, P, P, I, P, P, P, P, P, P]
         lib.orc_decode_sequence.argtypes = [ctypes.POINTER(_Model), P, P, I, I, P, I, P, P, P, P, P]
         lib.orc_head_rows.argtypes = [ctypes.POINTER(_Model), P, I, P, I, P]
+        lib.orc_matvec_rows.argtypes = [P, I, I, P, I, P]
         lib.orc_round_bf16.argtypes = [ctypes.c_double]
         lib.orc_round_bf16.restype = ctypes.c_uint16
         lib.orc_num_threads.restype = ctypes.c_int
@@ -109,6 +110,18 @@ def _c_model(model):
     cm = _Model(d.hidden, d.n_q_heads, d.n_kv_heads, d.head_dim, d.vocab, float(d.rope_theta),
                 float(d.rms_eps), *[a.ctypes.data for a in arrs])
     return cm, arrs   # keep the arrays alive with the struct
+
+
+def matvec_rows(w_bits: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """y[i] = W x[i] for W given as bf16 bits [M][K] and x fp64 [n][K]; every
+    output one sequential fp64 dot product (``tv_oracle.c``)."""
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    xx = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float64)
+    M, K = w.shape
+    assert xx.shape[1] == K
+    y = np.empty((xx.shape[0], M), dtype=np.float64)
+    _load().orc_matvec_rows(w.ctypes.data, M, K, xx.ctypes.data, xx.shape[0], y.ctypes.data)
+    return y
 
 
 def round_bf16(x: float) -> int:

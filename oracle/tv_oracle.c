@@ -350,3 +350,15 @@ int orc_head_rows(const orc_model *m, const uint16_t *hf_bits, int n, const int3
   free(hf);
   return 0;
 }
+
+/* y[i][o] = sum_k W[o][k] * x[i][k] (k ascending, fp64) for n input rows; W is
+ * [M][K] bf16 bits.  The plain projection the layer-stack oracle builds on:
+ * every output is one sequential dot product, so the result does not depend
+ * on n, on the thread count or on which other rows are projected with it. */
+int orc_matvec_rows(const uint16_t *W, int M, int K, const double *x, int n, double *y) {
+#pragma omp parallel for schedule(static)
+  for (int o = 0; o < M; ++o)
+    for (int i = 0; i < n; ++i)
+      y[(size_t)i * M + o] = dot_w(W + (size_t)o * K, x + (size_t)i * K, K);
+  return 0;
+}

@@ -270,3 +270,107 @@ class Workload:
 def joint_contexts(n_req: int, seed: int, lo: int = 1024, hi: int = 8192) -> list:
     rng = np.random.Generator(np.random.PCG64(seed))
     return [int(c) for c in rng.integers(lo, hi + 1, size=n_req)]
+
+
+# ---------------------------------------------------------------------------
+# the decoder-layer stack: Gated DeltaNet and attention layers, each followed by
+# a SwiGLU MLP (the composition is a reading: the pages name the layer kinds,
+# not the layers)
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class StackDims:
+    base: Dims            # hidden, attention heads, vocab, RoPE base, RMSNorm eps
+    n_layers: int
+    attn_every: int       # layer l is an attention layer iff l % attn_every == attn_every - 1
+    n_k_heads: int        # Gated DeltaNet key heads
+    n_v_heads: int        # Gated DeltaNet value heads
+    d_k: int
+    d_v: int
+    intermediate: int     # MLP width
+
+    def is_attn(self, layer: int) -> bool:
+        return layer % self.attn_every == self.attn_every - 1
+
+    @property
+    def attn_layers(self) -> list:
+        return [l for l in range(self.n_layers) if self.is_attn(l)]
+
+    @property
+    def dn_layers(self) -> list:
+        return [l for l in range(self.n_layers) if not self.is_attn(l)]
+
+    @property
+    def dn_in_out(self) -> int:
+        """Rows of the DeltaNet input projection: q, k (key heads), v, z (value
+        heads), then the write-strength and decay logits (one per value head)."""
+        return 2 * self.n_k_heads * self.d_k + 2 * self.n_v_heads * self.d_v + 2 * self.n_v_heads
+
+
+# small stack for the tests: 3 DeltaNet layers then an attention layer
+STACK_TINY = StackDims(base=TINY, n_layers=4, attn_every=4, n_k_heads=2, n_v_heads=4, d_k=64, d_v=64,
+                       intermediate=512)
+# the hidden-5120 stack of the benchmark: 64 layers, every 4th an attention
+# layer (48 DeltaNet layers), 16 key / 32 value heads of 128, MLP width 17408
+STACK_FULL = StackDims(base=FULL, n_layers=64, attn_every=4, n_k_heads=16, n_v_heads=32, d_k=128, d_v=128,
+                       intermediate=17408)
+
+
+@dataclass
+class StackLayer:
+    attn: bool
+    ln_mix: np.ndarray             # [H] gain of the norm before the mixer
+    ln_mlp: np.ndarray             # [H] gain of the norm before the MLP
+    w_gu: np.ndarray               # [2 I][H]: gate rows, then up rows
+    w_down: np.ndarray             # [H][I]
+    wqkv: np.ndarray = None        # attention: [(Hq + 2 Hkv) D][H]
+    wo: np.ndarray = None          # attention: [H][Hq D]
+    w_in: np.ndarray = None        # DeltaNet: [dn_in_out][H]
+    w_out: np.ndarray = None       # DeltaNet: [H][Hv d_v]
+    dn_norm: np.ndarray = None     # DeltaNet: [d_v] gain of the per-head output norm
+
+
+@dataclass
+class StackModel:
+    dims: StackDims
+    embed: np.ndarray              # [V][H]
+    ln_f: np.ndarray               # [H]
+    lm_head: np.ndarray            # [V][H]
+    layers: list
+
+
+def gen_stack(dims: StackDims, seed: int, std: float = 0.02, random_gains: bool = False) -> StackModel:
+    """Random-init stack (bf16 bits), gains 1.0 unless ``random_gains``."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    b = dims.base
+    H, V = b.hidden, b.vocab
+
+    def gain(n):
+        x = 1.0 + 0.25 * rng.standard_normal(n, dtype=np.float32) if random_gains else np.ones(n, np.float32)
+        return f32_to_bf16_bits(x)
+
+    embed = _normal_bf16(rng, (V, H), std)
+    layers = []
+    for l in range(dims.n_layers):
+        if dims.is_attn(l):
+            lay = StackLayer(True, gain(H), gain(H), None, None,
+                             wqkv=_normal_bf16(rng, (b.qkv_out, H), std),
+                             wo=_normal_bf16(rng, (H, b.n_q_heads * b.head_dim), std))
+        else:
+            lay = StackLayer(False, gain(H), gain(H), None, None,
+                             w_in=_normal_bf16(rng, (dims.dn_in_out, H), std),
+                             w_out=_normal_bf16(rng, (H, dims.n_v_heads * dims.d_v), std),
+                             dn_norm=gain(dims.d_v))
+        lay.w_gu = _normal_bf16(rng, (2 * dims.intermediate, H), std)
+        lay.w_down = _normal_bf16(rng, (H, dims.intermediate), std)
+        layers.append(lay)
+    ln_f = gain(H)
+    lm_head = _normal_bf16(rng, (V, H), std)
+    return StackModel(dims, embed, ln_f, lm_head, layers)
+
+
+def gen_dn_states(dims: StackDims, seed: int) -> list:
+    """The recurrent state before the round of every DeltaNet layer, fp32
+    [H_v][d_k][d_v] ~ N(0, 0.3^2)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return [np.ascontiguousarray(rng.standard_normal((dims.n_v_heads, dims.d_k, dims.d_v)) * 0.3, dtype=np.float32)
+            for _ in dims.dn_layers]

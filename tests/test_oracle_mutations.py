@@ -288,3 +288,43 @@ def test_unedited_policy_copy_passes_the_pins(monkeypatch):
 def test_planted_policy_mistake_fails_a_pin(monkeypatch, name, old, new):
     monkeypatch.setattr(PT, "P", _module_copy(POLICY_REAL, old, new))
     assert _pins_failed(PT), f"planted mistake {name} passed every price/StairCut pin"
+
+
+# --------------------------------------------------------------------------
+# the layer-stack oracle (oracle/stack.py) against its pins
+# --------------------------------------------------------------------------
+import test_oracle_stack as SKT  # noqa: E402
+from oracle import stack as STACK_REAL  # noqa: E402
+
+STACK_MUTATIONS = [
+    ("mlp_no_residual", "return rb(x + matvec_rows(lay.w_down, a[None])[0])",
+     "return rb(matvec_rows(lay.w_down, a[None])[0])"),
+    ("swiglu_gate_on_up", "a = rb(_silu(gu[:I]) * gu[I:])", "a = rb(gu[:I] * _silu(gu[I:]))"),
+    ("dn_state_of_previous_row", "S0 if parent[i] < 0 else Sn[parent[i]]", "S0 if parent[i] < 0 else Sn[i - 1]"),
+    ("dn_q_not_scaled", "q = q / np.sqrt(np.sum(q * q, axis=1, keepdims=True) + 1e-6) / np.sqrt(dk)",
+     "q = q / np.sqrt(np.sum(q * q, axis=1, keepdims=True) + 1e-6)"),
+    ("dn_key_head_map", "kh = h // G", "kh = h % sd.n_k_heads"),
+    ("dn_write_strength_not_sigmoid", "beta = 1.0 / (1.0 + np.exp(-b))", "beta = 1.0 / (1.0 + np.exp(b))"),
+    ("dn_decay_sign", "g = -np.logaddexp(0.0, a)", "g = np.logaddexp(0.0, a) - 2.0 * np.logaddexp(0.0, a) + 0.01"),
+    ("dn_output_gate_dropped", "* bf16_to_f64(lay.dn_norm)[None, :] * _silu(z))",
+     "* bf16_to_f64(lay.dn_norm)[None, :])"),
+    ("attn_position_is_index", "fr = [attn_front(lay, d, h[i], ctx + int(depth[i])) for i in range(n)]",
+     "fr = [attn_front(lay, d, h[i], ctx + i) for i in range(n)]"),
+    ("attn_key_of_wrong_node", "K = np.concatenate([Kc, np.stack([fr[a][1] for a in p])])",
+     "K = np.concatenate([Kc, np.stack([fr[max(a - 1, 0)][1] for a in p])])"),
+    ("commit_keeps_the_root_state", "states = [st[path[-1]].copy() for st in res[\"states\"]]",
+     "states = [st[path[0]].copy() for st in res[\"states\"]]"),
+    ("mlp_norm_gain_of_the_mixer", "h2 = _rms_bf16(x, lay.ln_mlp, sd.base.rms_eps)",
+     "h2 = _rms_bf16(x, lay.ln_mix, sd.base.rms_eps)"),
+]
+
+
+def test_unedited_stack_copy_passes_the_pins(monkeypatch):
+    monkeypatch.setattr(SKT, "ST", _module_copy(STACK_REAL))
+    assert _pins_failed(SKT) == []
+
+
+@pytest.mark.parametrize("name,old,new", STACK_MUTATIONS, ids=[m[0] for m in STACK_MUTATIONS])
+def test_planted_stack_mistake_fails_a_pin(monkeypatch, name, old, new):
+    monkeypatch.setattr(SKT, "ST", _module_copy(STACK_REAL, old, new))
+    assert _pins_failed(SKT, first_only=True), f"planted mistake {name} passed every stack pin"
