@@ -475,6 +475,110 @@ TV_API int tv_dn_commit(const tv_dn_dims *dims, const tv_tree *trees, int n_req,
                         const int32_t *accept_len, int32_t *dev_status, void *stream);
 
 /*
+ * Tree verify through a stack of decoder layers [Drafters and tree verify, §The
+ * round, step 2: "one forward pass of the target model runs over the whole
+ * tree"; §Tree verify through recurrent layers: the model's Gated DeltaNet
+ * layers].  The pages name the layer kinds, not the layers; the stack taken is
+ * a pre-norm residual stack, each layer a mixer and a SwiGLU MLP:
+ *
+ *     x = E[token]
+ *     per layer:  x = bf16( x + Mixer( bf16(RMSNorm(x) ln_mix) ) )
+ *                 x = bf16( x + bf16( silu(h W_gate^T) * (h W_up^T) ) W_down^T ),
+ *                     h = bf16(RMSNorm(x) ln_mlp)
+ *     logits = fp32( bf16(RMSNorm(x) ln_f) W_lm^T ), argmax and top-2 gap
+ *
+ * Mixer of an attention layer (TV_LAYER_ATTN): the layer of tv_verify_tree
+ * (QKV, RoPE at ctx + depth, tree-masked GQA attention over the layer's cache,
+ * O projection); the tree rows' K/V go to its cache at slots ctx + i.
+ * Mixer of a Gated DeltaNet layer (TV_LAYER_DN): [q, k, v, z, b, a] = h W_in^T
+ * (rows: q, k of n_k_heads x d_k, v, z of n_v_heads x d_v, then b, a of
+ * n_v_heads); per key head q and k divided by sqrt(|.|^2 + 1e-6), q also by
+ * sqrt(d_k); beta = sigmoid(b), g = -softplus(a); the gated delta rule over the
+ * tree as tv_dn_verify_tree (from the layer's state before the round); per
+ * value head y = bf16( o / sqrt(mean(o^2) + rms_eps) dn_norm silu(z) ); the
+ * mixer output is y W_out^T.
+ *
+ *   tv_layer     one layer, all device pointers, bf16, weights [out][in] row
+ *                major (or tile-packed by tv_pack_weight when model->packed):
+ *                  ln_mix, ln_mlp [hidden]
+ *                  w_mix_in   attention: W_qkv [(Hq + 2 Hkv) D][hidden];
+ *                             DeltaNet: W_in [2 Hk dk + 2 Hv dv + 2 Hv][hidden]
+ *                  w_mix_out  attention: W_o [hidden][Hq D]; DeltaNet: W_out [hidden][Hv dv]
+ *                  dn_norm    DeltaNet: [d_v]; attention: unused
+ *                  w_gate_up  [2 intermediate][hidden] (gate rows, then up rows)
+ *                  w_down     [hidden][intermediate]
+ *   tv_stack     dims (hidden, attention heads, vocab, RoPE, eps), dn (the
+ *                DeltaNet heads: d_k, d_v in {32, 64, 96, 128}), intermediate
+ *                (a multiple of 64), n_layers and the host array of layers,
+ *                embed / ln_f / lm_head as in tv_model, packed as in tv_model.
+ *   kv           host array [n_attn_layers * n_req]: the cache of attention
+ *                layer j (in layer order) for request r at kv[j * n_req + r];
+ *                every layer of a request has the same ctx_len
+ *   dn_states    host array [n_req] of device pointers, 16-byte aligned: fp32
+ *                [n_dn_layers][n_v_heads][d_k][d_v], the states before the
+ *                round (read only here; tv_commit_stack updates them)
+ *   logits, argmax, top2_gap  as tv_verify_tree
+ *   x_taps       device bf16 [2 n_layers + 1][total_rows][hidden], or NULL: the
+ *                residual stream of every row after each residual sublayer --
+ *                tap 2l is the stream entering layer l (tap 0 the embedding),
+ *                tap 2l + 1 the stream after layer l's mixer, tap 2 n_layers
+ *                the stream after the last layer (before the final norm).  The
+ *                pages' block drafter reads such taps of the target ("the
+ *                residual stream entering layers 5, 19, 33, 47 and 61")
+ *                [Drafters and tree verify, §The block drafter].  Copies on
+ *                the stream when given; nothing when NULL.
+ *   workspace    device, >= tv_stack_workspace_size(model); also holds what
+ *                tv_commit_stack needs (the DeltaNet layers' keys, pseudo-values
+ *                and cumulative gates), so pass the same one to the commit
+ * Host checks: TV_E_ARG, TV_E_ROWS, TV_E_CAPACITY, TV_E_WORKSPACE,
+ * TV_E_UNSUPPORTED.  Device checks: the tree rules, as tv_verify_tree.
+ */
+#define TV_LAYER_ATTN 0
+#define TV_LAYER_DN 1
+typedef struct tv_layer {
+    int32_t kind;
+    const tv_bf16 *ln_mix;
+    const tv_bf16 *w_mix_in;
+    const tv_bf16 *w_mix_out;
+    const tv_bf16 *dn_norm;
+    const tv_bf16 *ln_mlp;
+    const tv_bf16 *w_gate_up;
+    const tv_bf16 *w_down;
+} tv_layer;
+
+typedef struct tv_stack {
+    tv_dims dims;
+    tv_dn_dims dn;
+    int32_t intermediate;
+    int32_t n_layers;
+    const tv_layer *layers;
+    const tv_bf16 *embed, *ln_f, *lm_head;
+    int32_t packed;
+} tv_stack;
+
+TV_API int tv_stack_workspace_size(const tv_stack *model, size_t *bytes);
+TV_API int tv_verify_stack(const tv_stack *model, const tv_kv *kv, float *const *dn_states, const tv_tree *trees,
+                           int n_req, float *logits, int32_t *argmax, float *top2_gap, tv_bf16 *x_taps,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * Commit of a stack verify [Drafters and tree verify, §The round, step 4: keep
+ * the KV rows and the recurrent state of the accepted path]: in every
+ * attention layer the KV commit of tv_commit_kv, in every Gated DeltaNet layer
+ * the path-state commit of tv_dn_commit (the state after the path's last
+ * node), from what tv_verify_stack left in the workspace.
+ *   kv, dn_states, trees  as tv_verify_stack (the same call's)
+ *   path, accept_len      device, from an accept walk on that call's argmax
+ *   committed_src, new_ctx  as tv_commit_kv
+ * Host checks: TV_E_ARG, TV_E_ROWS, TV_E_WORKSPACE, TV_E_UNSUPPORTED.  Device
+ * checks: TV_E_PATH (nothing is written with a bad path).
+ */
+TV_API int tv_commit_stack(const tv_stack *model, const tv_kv *kv, float *const *dn_states, const tv_tree *trees,
+                           int n_req, const int32_t *path, const int32_t *accept_len, int32_t *committed_src,
+                           int32_t *new_ctx, const void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           void *stream);
+
+/*
  * Verify prices and the StairCut cut [Drafters and tree verify, §StairCut: the
  * node count, calculated each round; §StairCut on Flash-Next, and the shared
  * price files].  Host-only: no device memory, nothing launched.

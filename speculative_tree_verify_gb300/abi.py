@@ -30,7 +30,7 @@ SYMBOLS = ("tv_workspace_size", "tv_verify_tree", "tv_accept_greedy", "tv_accept
            "tv_sample_workspace_size", "tv_sample_filter", "tv_accept_single_draw", "tv_accept_gumbel",
            "tv_accept_rejection", "tv_dn_verify_tree", "tv_dn_commit", "tv_price_init", "tv_price_lookup",
            "tv_price_observe", "tv_staircut", "tv_packed_weight_bytes", "tv_pack_weight",
-           "tv_accept_greedy_commit")
+           "tv_accept_greedy_commit", "tv_stack_workspace_size", "tv_verify_stack", "tv_commit_stack")
 PROFILE_STAGES = ("prologue+embed", "qkv_gemm", "qkv_finalize", "attention", "o_gemm", "o_finalize", "lm_head")
 
 
@@ -69,6 +69,21 @@ class TvPriceTable(ctypes.Structure):
 class TvDnDims(ctypes.Structure):
     _fields_ = [("n_k_heads", ctypes.c_int32), ("n_v_heads", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32)]
+
+
+TV_LAYER_ATTN, TV_LAYER_DN = 0, 1
+
+
+class TvLayer(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("ln_mix", ctypes.c_void_p), ("w_mix_in", ctypes.c_void_p),
+                ("w_mix_out", ctypes.c_void_p), ("dn_norm", ctypes.c_void_p), ("ln_mlp", ctypes.c_void_p),
+                ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+class TvStack(ctypes.Structure):
+    _fields_ = [("dims", TvDims), ("dn", TvDnDims), ("intermediate", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("layers", ctypes.POINTER(TvLayer)), ("embed", ctypes.c_void_p), ("ln_f", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p), ("packed", ctypes.c_int32)]
 
 
 _lib = None
@@ -117,6 +132,11 @@ def load():
                                           P, P, P, P, P, P, P, P, P]
         lib.tv_dn_commit.argtypes = [ctypes.POINTER(TvDnDims), ctypes.POINTER(TvTree), I, I, ctypes.POINTER(P), P, P,
                                      P, P, P, P, P]
+        lib.tv_stack_workspace_size.argtypes = [ctypes.POINTER(TvStack), ctypes.POINTER(Z)]
+        lib.tv_verify_stack.argtypes = [ctypes.POINTER(TvStack), ctypes.POINTER(TvKv), ctypes.POINTER(P),
+                                        ctypes.POINTER(TvTree), I, P, P, P, P, P, Z, P, P]
+        lib.tv_commit_stack.argtypes = [ctypes.POINTER(TvStack), ctypes.POINTER(TvKv), ctypes.POINTER(P),
+                                        ctypes.POINTER(TvTree), I, P, P, P, P, P, Z, P, P]
         D = ctypes.c_double
         lib.tv_price_init.argtypes = [ctypes.POINTER(TvPriceTable)]
         lib.tv_price_lookup.argtypes = [ctypes.POINTER(TvPriceTable), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -269,6 +289,30 @@ def tv_dn_commit(dims: TvDnDims, trees: Sequence[TvTree], n_layers: int, states,
                  dev_status, stream=None) -> int:
     return load().tv_dn_commit(ctypes.byref(dims), _arr(TvTree, trees), len(trees), int(n_layers), _ptrs(states),
                                _p(k), _p(u), _p(gc), _p(path), _p(accept_len), _p(dev_status), _stream(stream))
+
+
+def tv_stack_workspace_size(stack: TvStack):
+    """(rc, bytes) of workspace tv_verify_stack / tv_commit_stack need."""
+    z = ctypes.c_size_t(0)
+    rc = load().tv_stack_workspace_size(ctypes.byref(stack), ctypes.byref(z))
+    return rc, int(z.value)
+
+
+def tv_verify_stack(stack: TvStack, kvs: Sequence[TvKv], dn_states, trees: Sequence[TvTree], logits, argmax,
+                    top2_gap, x_taps, workspace, workspace_bytes: int, dev_status, stream=None) -> int:
+    """kvs: [n_attn_layers * n_req] (layer-major); dn_states: one device buffer
+    per request; x_taps: bf16 [2 n_layers + 1][rows][hidden] or None."""
+    return load().tv_verify_stack(ctypes.byref(stack), _arr(TvKv, kvs) if kvs else None,
+                                  _ptrs(dn_states) if dn_states else None, _arr(TvTree, trees), len(trees),
+                                  _p(logits), _p(argmax), _p(top2_gap), _p(x_taps), _p(workspace),
+                                  int(workspace_bytes), _p(dev_status), _stream(stream))
+
+
+def tv_commit_stack(stack: TvStack, kvs: Sequence[TvKv], dn_states, trees: Sequence[TvTree], path, accept_len,
+                    committed_src, new_ctx, workspace, workspace_bytes: int, dev_status, stream=None) -> int:
+    return load().tv_commit_stack(ctypes.byref(stack), _arr(TvKv, kvs) if kvs else None, _ptrs(dn_states) if dn_states else None,
+                                  _arr(TvTree, trees), len(trees), _p(path), _p(accept_len), _p(committed_src),
+                                  _p(new_ctx), _p(workspace), int(workspace_bytes), _p(dev_status), _stream(stream))
 
 
 def tv_price_init(table: TvPriceTable) -> int:

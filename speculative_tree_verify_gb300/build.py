@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtv.so")
 SOURCES = ["tv_api.cu", "tv_gemm.cu", "tv_layer.cu", "tv_attn.cu", "tv_walks.cu", "tv_noalloc.cu", "tv_sample.cu",
-           "tv_deltanet.cu", "tv_policy.cpp"]
+           "tv_deltanet.cu", "tv_stack.cu", "tv_policy.cpp"]
 HEADERS = ["tv_common.cuh", "tv_gemm.cuh", "tv_kernels.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

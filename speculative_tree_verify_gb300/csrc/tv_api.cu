@@ -192,7 +192,7 @@ int tv_verify_tree(const tv_model* model, const tv_kv* kv, const tv_tree* trees,
 
   StageMarks pm(st);
   pm.mark(0);
-  if ((rc = launch_prologue_embed(t, *model, b, dev_status, st))) return rc;
+  if ((rc = launch_prologue_embed(t, d, model->embed, model->ln1, b, nullptr, dev_status, st))) return rc;
   pm.mark(1);
   gp.out = b.part_qkv;
   if ((rc = launch_gemm(GEMM_PARTIAL, model->wqkv, QKV, H, b.h, t.total_rows, pq, gp, sms, st))) return rc;
@@ -492,6 +492,272 @@ const char* tv_status_string(int code) {
     case TV_E_PROPOSAL: return "proposal row not finite, negative, off unit mass or zero at its draft";
     default: return "unknown status";
   }
+}
+
+}  // extern "C"
+
+// ---- the decoder-layer stack -----------------------------------------------------
+namespace tv {
+namespace {
+
+struct StackLayout {
+  size_t rstats, meta, counter, h, x, q, part, attn_ml, attn_o, attn, top2, dq, dv, dz, dbeta, dg, dout, act, dk_all,
+      du_all, dgc_all, total;
+  int n_attn, n_dn;
+};
+
+int stack_counts(const tv_stack& m, int& n_attn, int& n_dn) {
+  n_attn = n_dn = 0;
+  if (!m.layers || m.n_layers < 1) return TV_E_ARG;
+  for (int l = 0; l < m.n_layers; ++l) {
+    if (m.layers[l].kind == TV_LAYER_ATTN) ++n_attn;
+    else if (m.layers[l].kind == TV_LAYER_DN) ++n_dn;
+    else return TV_E_ARG;
+  }
+  return TV_OK;
+}
+
+size_t part_bytes(int M, int K) { return (size_t)plan_gemm(M, K, false).splits * kMaxRows * M * 4; }
+
+StackLayout stack_layout(const tv_stack& m) {
+  StackLayout L;
+  stack_counts(m, L.n_attn, L.n_dn);
+  const tv_dims& d = m.dims;
+  const tv_dn_dims& dn = m.dn;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const int H = d.hidden, QD = d.n_q_heads * d.head_dim, QKV = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const int KD = dn.n_k_heads * dn.d_k, VD = dn.n_v_heads * dn.d_v, I = m.intermediate;
+  const int DIN = 2 * KD + 2 * VD + 2 * dn.n_v_heads;
+  size_t pb = 0;
+  auto mx = [&](size_t b) { pb = b > pb ? b : pb; };
+  if (L.n_attn) {
+    mx(part_bytes(QKV, H));
+    mx(part_bytes(H, QD));
+  }
+  if (L.n_dn) {
+    mx(part_bytes(DIN, H));
+    mx(part_bytes(H, VD));
+  }
+  mx(part_bytes(2 * I, H));
+  mx(part_bytes(H, I));
+  L.rstats = take((size_t)kMaxRows * n_vchunks(d.vocab) * sizeof(RowStat));
+  L.meta = take(kMaxRows * sizeof(RowMeta));
+  L.counter = take(256);
+  L.h = take((size_t)kMaxRows * H * 2);
+  L.x = take((size_t)kMaxRows * H * 2);
+  L.q = take((size_t)kMaxRows * QD * 2);
+  L.part = take(pb);
+  L.attn_ml = take((size_t)kMaxRows * d.n_q_heads * kChunkSlots * 2 * 4);
+  L.attn_o = take((size_t)kMaxRows * d.n_q_heads * kChunkSlots * d.head_dim * 4);
+  L.attn = take((size_t)kMaxRows * QD * 2);
+  L.top2 = take((size_t)kMaxHeadGrid * 32 * sizeof(Top2));
+  L.dq = take((size_t)kMaxRows * KD * 4);
+  L.dv = take((size_t)kMaxRows * VD * 4);
+  L.dz = take((size_t)kMaxRows * VD * 4);
+  L.dbeta = take((size_t)kMaxRows * dn.n_v_heads * 4);
+  L.dg = take((size_t)kMaxRows * dn.n_v_heads * 4);
+  L.dout = take((size_t)kMaxRows * VD * 4);
+  L.act = take((size_t)kMaxRows * (I > VD ? I : VD) * 2);
+  L.dk_all = take((size_t)L.n_dn * kMaxRows * KD * 4);
+  L.du_all = take((size_t)L.n_dn * kMaxRows * VD * 4);
+  L.dgc_all = take((size_t)L.n_dn * kMaxRows * dn.n_v_heads * 4);
+  L.total = off;
+  return L;
+}
+
+int stack_check(const tv_stack* m) {
+  if (!m) return TV_E_ARG;
+  int rc = check_dims(m->dims);
+  if (rc) return rc;
+  int na = 0, nd = 0;
+  if ((rc = stack_counts(*m, na, nd))) return rc;
+  if (nd > 0 && (rc = dn_check(&m->dn))) return rc;
+  if (m->intermediate < 64 || m->intermediate % 64 != 0) return TV_E_UNSUPPORTED;
+  if (m->dims.hidden > 16384 || m->intermediate > 65536) return TV_E_UNSUPPORTED;
+  if (!m->embed || !m->ln_f || !m->lm_head || !aligned16(m->lm_head)) return TV_E_ARG;
+  if (m->packed != 0 && m->packed != 1) return TV_E_ARG;
+  for (int l = 0; l < m->n_layers; ++l) {
+    const tv_layer& y = m->layers[l];
+    if (!y.ln_mix || !y.ln_mlp || !y.w_mix_in || !y.w_mix_out || !y.w_gate_up || !y.w_down) return TV_E_ARG;
+    if (y.kind == TV_LAYER_DN && !y.dn_norm) return TV_E_ARG;
+    if (!aligned16(y.w_mix_in) || !aligned16(y.w_mix_out) || !aligned16(y.w_gate_up) || !aligned16(y.w_down))
+      return TV_E_ARG;
+  }
+  return TV_OK;
+}
+
+// The request table of attention layer j: the trees and that layer's caches.
+int stack_table(ReqTable& t, const tv_tree* trees, const tv_kv* kv, int n_req, int j) {
+  return build_table(t, trees, kv + (size_t)j * n_req, n_req, true);
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" {
+
+int tv_stack_workspace_size(const tv_stack* model, size_t* bytes) {
+  if (!bytes) return TV_E_ARG;
+  const int rc = stack_check(model);
+  if (rc) return rc;
+  *bytes = stack_layout(*model).total;
+  return TV_OK;
+}
+
+int tv_verify_stack(const tv_stack* model, const tv_kv* kv, float* const* dn_states, const tv_tree* trees, int n_req,
+                    float* logits, int32_t* argmax, float* top2_gap, tv_bf16* x_taps, void* workspace,
+                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int rc = stack_check(model);
+  if (rc) return rc;
+  if (!trees || !logits || !argmax || !top2_gap || !dev_status) return TV_E_ARG;
+  if (x_taps && !aligned16(x_taps)) return TV_E_ARG;
+  const StackLayout L = stack_layout(*model);
+  if ((L.n_attn > 0 && !kv) || (L.n_dn > 0 && !dn_states)) return TV_E_ARG;
+  const tv_dims& d = model->dims;
+  const tv_dn_dims& dn = model->dn;
+  ReqTable t;
+  if (L.n_attn > 0) {
+    if ((rc = stack_table(t, trees, kv, n_req, 0))) return rc;
+    for (int j = 1; j < L.n_attn; ++j) {
+      ReqTable tj;
+      if ((rc = stack_table(tj, trees, kv, n_req, j))) return rc;
+      for (int r = 0; r < n_req; ++r)
+        if (tj.ctx[r] != t.ctx[r]) return TV_E_ARG;
+    }
+    const int G = d.n_q_heads / d.n_kv_heads;
+    for (int r = 0; r < n_req; ++r)
+      if (G * t.n[r] > kMaxQueriesPerKvHead) return TV_E_UNSUPPORTED;
+  } else if ((rc = build_table(t, trees, nullptr, n_req, true))) {
+    return rc;
+  }
+  DnStates st;
+  if (L.n_dn > 0 && (rc = ::dn_states(st, dn_states, n_req))) return rc;
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return TV_E_WORKSPACE;
+  const int sms = num_sms();
+  if (sms <= 0) return TV_E_CUDA;
+  if (sms > kMaxHeadGrid) return TV_E_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto bf = [&](size_t o) { return reinterpret_cast<__nv_bfloat16*>(ws + o); };
+  auto f32 = [&](size_t o) { return reinterpret_cast<float*>(ws + o); };
+  LayerBufs b;
+  b.meta = reinterpret_cast<RowMeta*>(ws + L.meta);
+  b.head_counter = reinterpret_cast<unsigned int*>(ws + L.counter);
+  b.h = bf(L.h);
+  b.q = bf(L.q);
+  b.part_qkv = f32(L.part);
+  b.attn_ml = f32(L.attn_ml);
+  b.attn_o = f32(L.attn_o);
+  b.attn = bf(L.attn);
+  b.part_o = f32(L.part);
+  b.hf = bf(L.h);
+  __nv_bfloat16* x = bf(L.x);
+  __nv_bfloat16* act = bf(L.act);
+  float* part = f32(L.part);
+  const int rows = t.total_rows;
+  const int H = d.hidden, QD = d.n_q_heads * d.head_dim, QKV = (d.n_q_heads + 2 * d.n_kv_heads) * d.head_dim;
+  const int KD = dn.n_k_heads * dn.d_k, VD = dn.n_v_heads * dn.d_v, I = model->intermediate;
+  const int DIN = 2 * KD + 2 * VD + 2 * dn.n_v_heads;
+  GemmParams gp;
+  memset(&gp, 0, sizeof(gp));
+  gp.status = dev_status;
+  gp.packed = model->packed ? 1 : 0;
+  gp.out = part;
+  auto gemm = [&](const void* W, int M, int K, const void* X, GemmPlan& pl) {
+    pl = plan_gemm(M, K, false);
+    return launch_gemm(GEMM_PARTIAL, W, M, K, X, rows, pl, gp, sms, s);
+  };
+  GemmPlan pl;
+  int n_tap = 0;
+  auto tap = [&]() {   // the residual stream into the next tap slot
+    if (!x_taps) return TV_OK;
+    const size_t bytes = (size_t)rows * H * sizeof(tv_bf16);
+    return cudaMemcpyAsync(reinterpret_cast<uint8_t*>(x_taps) + (size_t)(n_tap++) * bytes, x, bytes,
+                           cudaMemcpyDeviceToDevice, s) == cudaSuccess ? TV_OK : TV_E_CUDA;
+  };
+  if ((rc = launch_prologue_embed(t, d, model->embed, model->layers[0].ln_mix, b, x, dev_status, s))) return rc;
+  if ((rc = tap())) return rc;
+  int ja = 0, jd = 0;
+  for (int l = 0; l < model->n_layers; ++l) {
+    const tv_layer& y = model->layers[l];
+    if (y.kind == TV_LAYER_ATTN) {
+      ReqTable tl;
+      if ((rc = stack_table(tl, trees, kv, n_req, ja))) return rc;
+      if ((rc = gemm(y.w_mix_in, QKV, H, b.h, pl))) return rc;
+      if ((rc = launch_qkv_finalize(tl, d, b, pl.splits, dev_status, s))) return rc;
+      if ((rc = launch_attention(tl, d, b, sms, dev_status, s))) return rc;
+      if ((rc = gemm(y.w_mix_out, H, QD, b.attn, pl))) return rc;
+      ++ja;
+    } else {
+      float* kl = f32(L.dk_all) + (size_t)jd * rows * KD;
+      float* ul = f32(L.du_all) + (size_t)jd * rows * VD;
+      float* gcl = f32(L.dgc_all) + (size_t)jd * rows * dn.n_v_heads;
+      DnStates sl;
+      for (int r = 0; r < n_req; ++r) sl.S[r] = st.S[r] + (size_t)jd * dn.n_v_heads * dn.d_k * dn.d_v;
+      if ((rc = gemm(y.w_mix_in, DIN, H, b.h, pl))) return rc;
+      if ((rc = launch_dn_in(part, pl.splits, rows, dn.n_k_heads, dn.n_v_heads, dn.d_k, dn.d_v, f32(L.dq), kl,
+                             f32(L.dv), f32(L.dz), f32(L.dbeta), f32(L.dg), dev_status, s)))
+        return rc;
+      if ((rc = launch_dn_verify(t, sl, dn.n_k_heads, dn.n_v_heads, dn.d_k, dn.d_v, f32(L.dq), kl, f32(L.dv),
+                                 f32(L.dbeta), f32(L.dg), f32(L.dout), ul, gcl, dev_status, s)))
+        return rc;
+      if ((rc = launch_dn_out(f32(L.dout), f32(L.dz), y.dn_norm, rows, dn.n_v_heads, dn.d_v, d.rms_eps, act,
+                              dev_status, s)))
+        return rc;
+      if ((rc = gemm(y.w_mix_out, H, VD, act, pl))) return rc;
+      ++jd;
+    }
+    if ((rc = launch_resid(part, pl.splits, H, rows, x, y.ln_mlp, d.rms_eps, b.h, dev_status, s))) return rc;
+    if ((rc = tap())) return rc;
+    if ((rc = gemm(y.w_gate_up, 2 * I, H, b.h, pl))) return rc;
+    if ((rc = launch_act(part, pl.splits, I, rows, act, dev_status, s))) return rc;
+    if ((rc = gemm(y.w_down, H, I, act, pl))) return rc;
+    const void* next = l + 1 < model->n_layers ? (const void*)model->layers[l + 1].ln_mix : (const void*)model->ln_f;
+    if ((rc = launch_resid(part, pl.splits, H, rows, x, next, d.rms_eps, b.h, dev_status, s))) return rc;
+    if ((rc = tap())) return rc;
+  }
+  gp.out = logits;
+  gp.top2_part = reinterpret_cast<Top2*>(ws + L.top2);
+  gp.done_counter = b.head_counter;
+  gp.argmax = argmax;
+  gp.gap = top2_gap;
+  const GemmPlan ph = plan_gemm(d.vocab, H, true);
+  return launch_gemm(GEMM_HEAD, model->lm_head, d.vocab, H, b.h, rows, ph, gp, sms, s);
+}
+
+int tv_commit_stack(const tv_stack* model, const tv_kv* kv, float* const* dn_states, const tv_tree* trees, int n_req,
+                    const int32_t* path, const int32_t* accept_len, int32_t* committed_src, int32_t* new_ctx,
+                    const void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int rc = stack_check(model);
+  if (rc) return rc;
+  if (!trees || !path || !accept_len || !committed_src || !new_ctx || !dev_status) return TV_E_ARG;
+  const StackLayout L = stack_layout(*model);
+  if ((L.n_attn > 0 && !kv) || (L.n_dn > 0 && !dn_states)) return TV_E_ARG;
+  if (!workspace || workspace_bytes < L.total || !aligned16(workspace)) return TV_E_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const tv_dn_dims& dn = model->dn;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  ReqTable t;
+  for (int j = 0; j < L.n_attn; ++j) {
+    if ((rc = stack_table(t, trees, kv, n_req, j))) return rc;
+    if ((rc = launch_commit(t, model->dims, path, accept_len, committed_src, new_ctx, dev_status, s))) return rc;
+  }
+  if (L.n_dn > 0) {
+    if ((rc = build_table(t, trees, nullptr, n_req, true))) return rc;
+    DnStates st;
+    if ((rc = ::dn_states(st, dn_states, n_req))) return rc;
+    if ((rc = launch_dn_commit(t, st, dn.n_k_heads, dn.n_v_heads, dn.d_k, dn.d_v, L.n_dn,
+                               reinterpret_cast<const float*>(ws + L.dk_all), reinterpret_cast<const float*>(ws + L.du_all),
+                               reinterpret_cast<const float*>(ws + L.dgc_all), path, accept_len, dev_status, s)))
+      return rc;
+  }
+  return TV_OK;
 }
 
 }  // extern "C"

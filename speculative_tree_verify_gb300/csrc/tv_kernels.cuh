@@ -139,15 +139,30 @@ struct LayerBufs {
 };
 
 // the verify's first kernel: per request the tree prologue (validation, depth,
-// position, ancestors), per row the embedding and first RMSNorm
-int launch_prologue_embed(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status,
-                          cudaStream_t st);
+// position, ancestors), per row the embedding and first RMSNorm (h = bf16(
+// RMSNorm(E[token]) gain)); x_out, when not null, receives E[token] itself
+int launch_prologue_embed(const ReqTable& t, const tv_dims& d, const void* embed, const void* gain,
+                          const LayerBufs& b, __nv_bfloat16* x_out, int32_t* status, cudaStream_t st);
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,
                         cudaStream_t st);
 int launch_attention(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int sms, int32_t* status,
                      cudaStream_t st);
 int launch_o_finalize(const ReqTable& t, const tv_model& m, const LayerBufs& b, int splits, int32_t* status,
                       cudaStream_t st);
+
+// ---- the decoder-layer stack (tv_stack.cu) -------------------------------------
+// x = bf16(x + sum of the split-K partials [splits][32][H]); h_out = bf16(
+// RMSNorm(x) g).  A cluster of four CTAs per row.
+int launch_resid(const float* part, int splits, int H, int rows, __nv_bfloat16* x, const void* g, float eps,
+                 __nv_bfloat16* h_out, int32_t* status, cudaStream_t st);
+// a = bf16(silu(gate) * up) from the partials of the [2 I] gate/up projection
+int launch_act(const float* part, int splits, int I, int rows, __nv_bfloat16* a, int32_t* status, cudaStream_t st);
+// Gated DeltaNet input stage: normalised q, k; v, z; beta = sigmoid(b), g = -softplus(a)
+int launch_dn_in(const float* part, int splits, int rows, int Hk, int Hv, int dk, int dv, float* q, float* k,
+                 float* v, float* z, float* beta, float* g, int32_t* status, cudaStream_t st);
+// Gated DeltaNet output stage: y = bf16(RMSNorm(o) w silu(z)) per value head
+int launch_dn_out(const float* o, const float* z, const void* w, int rows, int Hv, int dv, float eps,
+                  __nv_bfloat16* y, int32_t* status, cudaStream_t st);
 
 int launch_accept_greedy(const ReqTable& t, const int32_t* argmax, int32_t* path, int32_t* accept_len,
                          int32_t* out_tokens, int32_t* status, cudaStream_t st);

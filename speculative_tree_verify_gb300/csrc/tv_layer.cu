@@ -90,12 +90,14 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 
 // The verify's first kernel.  Row blocks: h = bf16( x / sqrt(mean(x^2) + eps)
 // * g ), x = E[token], each thread holding up to kRowVecs 8-element vectors of
-// the row.  The last n_req blocks: the prologue of each request (warp 0).
+// the row; x itself also goes to x_out when given (the residual stream of a
+// layer stack).  The last n_req blocks: the prologue of each request (warp 0).
 __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t, int vocab, RowMeta* meta,
                                                                      unsigned int* head_counter,
                                                                      const __nv_bfloat16* embed,
                                                                      const __nv_bfloat16* g, int H, float eps,
-                                                                     __nv_bfloat16* h, int32_t* status) {
+                                                                     __nv_bfloat16* h, __nv_bfloat16* x_out,
+                                                                     int32_t* status) {
   __shared__ float red[33];
   pdl_trigger();   // the QKV GEMM may start streaming its weights now
   // the norm's gain (a weight: no kernel writes it) before the wait
@@ -149,6 +151,7 @@ __global__ void __launch_bounds__(kRowThreads) prologue_embed_kernel(ReqTable t,
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] = xf[k][e] * inv * gf[e];
       hv[vi] = pack8(y);
+      if (x_out) reinterpret_cast<uint4*>(x_out + (size_t)row * H)[vi] = x[vi];
     }
   }
 }
@@ -339,12 +342,12 @@ RopeParams rope_params(int head_dim, float theta) {
 
 }  // namespace
 
-int launch_prologue_embed(const ReqTable& t, const tv_model& m, const LayerBufs& b, int32_t* status,
-                          cudaStream_t st) {
-  if (m.dims.hidden > kRowVecs * kRowThreads * 8) return TV_E_UNSUPPORTED;
-  return launch_pdl(prologue_embed_kernel, dim3(t.total_rows + t.n_req), dim3(kRowThreads), 0, st, t, m.dims.vocab,
-                    b.meta, b.head_counter, reinterpret_cast<const __nv_bfloat16*>(m.embed),
-                    reinterpret_cast<const __nv_bfloat16*>(m.ln1), m.dims.hidden, m.dims.rms_eps, b.h, status);
+int launch_prologue_embed(const ReqTable& t, const tv_dims& d, const void* embed, const void* gain,
+                          const LayerBufs& b, __nv_bfloat16* x_out, int32_t* status, cudaStream_t st) {
+  if (d.hidden > kRowVecs * kRowThreads * 8) return TV_E_UNSUPPORTED;
+  return launch_pdl(prologue_embed_kernel, dim3(t.total_rows + t.n_req), dim3(kRowThreads), 0, st, t, d.vocab,
+                    b.meta, b.head_counter, reinterpret_cast<const __nv_bfloat16*>(embed),
+                    reinterpret_cast<const __nv_bfloat16*>(gain), d.hidden, d.rms_eps, b.h, x_out, status);
 }
 
 int launch_qkv_finalize(const ReqTable& t, const tv_dims& d, const LayerBufs& b, int splits, int32_t* status,

@@ -339,10 +339,15 @@ class StackModel:
 
 
 def gen_stack(dims: StackDims, seed: int, std: float = 0.02, random_gains: bool = False) -> StackModel:
-    """Random-init stack (bf16 bits), gains 1.0 unless ``random_gains``."""
+    """Random-init stack (bf16 bits), gains 1.0 unless ``random_gains``.  The
+    matrices that write into the residual stream (the mixers' output
+    projections and the MLP's down projection) draw with std / sqrt(2 L), L
+    the number of layers (the GPT-2 initialisation of residual layers), so
+    that the residual stream stays O(1) through the stack."""
     rng = np.random.Generator(np.random.PCG64(seed))
     b = dims.base
     H, V = b.hidden, b.vocab
+    out_std = std / float(np.sqrt(2 * dims.n_layers))
 
     def gain(n):
         x = 1.0 + 0.25 * rng.standard_normal(n, dtype=np.float32) if random_gains else np.ones(n, np.float32)
@@ -354,14 +359,14 @@ def gen_stack(dims: StackDims, seed: int, std: float = 0.02, random_gains: bool 
         if dims.is_attn(l):
             lay = StackLayer(True, gain(H), gain(H), None, None,
                              wqkv=_normal_bf16(rng, (b.qkv_out, H), std),
-                             wo=_normal_bf16(rng, (H, b.n_q_heads * b.head_dim), std))
+                             wo=_normal_bf16(rng, (H, b.n_q_heads * b.head_dim), out_std))
         else:
             lay = StackLayer(False, gain(H), gain(H), None, None,
                              w_in=_normal_bf16(rng, (dims.dn_in_out, H), std),
-                             w_out=_normal_bf16(rng, (H, dims.n_v_heads * dims.d_v), std),
+                             w_out=_normal_bf16(rng, (H, dims.n_v_heads * dims.d_v), out_std),
                              dn_norm=gain(dims.d_v))
         lay.w_gu = _normal_bf16(rng, (2 * dims.intermediate, H), std)
-        lay.w_down = _normal_bf16(rng, (H, dims.intermediate), std)
+        lay.w_down = _normal_bf16(rng, (H, dims.intermediate), out_std)
         layers.append(lay)
     ln_f = gain(H)
     lm_head = _normal_bf16(rng, (V, H), std)
