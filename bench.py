@@ -64,6 +64,8 @@ def _args():
     ap.add_argument("--rows", type=int, default=ROWS, help="tree rows of the timed round (profiling runs)")
     ap.add_argument("--ctx", type=int, default=CTX, help="cached context of the timed round (profiling runs)")
     ap.add_argument("--no-stack", action="store_true", help="skip the 64-layer stack section")
+    ap.add_argument("--only-stack", action="store_true", help="only the stack section (profiling runs)")
+    ap.add_argument("--stack-layers", type=int, default=64, help="layers of the stack section (profiling runs)")
     return ap.parse_args()
 
 
@@ -395,10 +397,11 @@ def stack_bytes(sd, n, ctx):
     return L_a * attn + L_d * dn + sd.n_layers * mlp + V * H * 2 + kv + state + n * V * 4
 
 
-def stack_bench(dv, synth, dev, peak, flush):
+def stack_bench(dv, synth, dev, peak, flush, n_layers=64, reps=10):
     """Round time of the 64-layer stack from a CUDA graph, L2 flushed before
     every replay; GB/s against the stack verify's algorithmic bytes."""
-    sd = synth.STACK_FULL
+    import dataclasses
+    sd = dataclasses.replace(synth.STACK_FULL, n_layers=n_layers)
     t0 = time.perf_counter()
     model = dv.DeviceStack.random(sd, 4321, device=dev)
     torch.cuda.synchronize()
@@ -429,7 +432,7 @@ def stack_bench(dv, synth, dev, peak, flush):
         if int(b.status.item()) != 0:
             raise RuntimeError(f"stack round: device status {int(b.status.item())}")
         gs = _graph(round_)
-        ms = _time_graph_flushed(gs, 10, flush)
+        ms = _time_graph_flushed(gs, reps, flush)
         del gs
         by = stack_bytes(sd, n, ctx)
         res["rows"][str(n)] = {"round_ms": round(ms, 4), "GB_per_s": round(by / ms / 1e6, 1),
@@ -449,6 +452,10 @@ def run_ours(args, world, rank, local):
     build.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.only_stack:
+        peak, _ = _peaks()
+        flush, _ = _l2_flush_buffer(dev)
+        return {"stack": stack_bench(dv, synth, dev, peak, flush, args.stack_layers, args.steps)}
     D = synth.FULL
     dm = dv.DeviceModel.random(D, 1234 + rank, device=dev)
     rows, ctx = args.rows, args.ctx

@@ -705,7 +705,7 @@ int tv_verify_stack(const tv_stack* model, const tv_kv* kv, float* const* dn_sta
                              f32(L.dv), f32(L.dz), f32(L.dbeta), f32(L.dg), dev_status, s)))
         return rc;
       if ((rc = launch_dn_verify(t, sl, dn.n_k_heads, dn.n_v_heads, dn.d_k, dn.d_v, f32(L.dq), kl, f32(L.dv),
-                                 f32(L.dbeta), f32(L.dg), f32(L.dout), ul, gcl, dev_status, s)))
+                                 f32(L.dbeta), f32(L.dg), f32(L.dout), ul, gcl, dev_status, s, true)))
         return rc;
       if ((rc = launch_dn_out(f32(L.dout), f32(L.dz), y.dn_norm, rows, dn.n_v_heads, dn.d_v, d.rms_eps, act,
                               dev_status, s)))

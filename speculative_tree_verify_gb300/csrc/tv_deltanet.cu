@@ -64,17 +64,33 @@ __host__ __device__ inline DnVerifyLayout dn_verify_layout(int dk) {
 __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
                                                                const float* q, const float* k, const float* v,
                                                                const float* beta, const float* g, float* o, float* u,
-                                                               float* gc_out, int32_t* status) {
+                                                               float* gc_out, int32_t* status, int state_early) {
   extern __shared__ __align__(16) float dsm[];
   __shared__ float s_gc[kMaxRows], s_beta[kMaxRows];
   __shared__ unsigned s_anc[kMaxRows];   // bit s: s is on t's root path (t included)
   __shared__ int s_err, s_stat;
+  const int h = blockIdx.x, cb = blockIdx.y, r = blockIdx.z;
+  // the state before the round: with state_early, loaded before the wait (the
+  // caller guarantees that every writer of it has completed by then)
+  const int c0 = cb * kDnCols;
+  constexpr int kSB = kDnMaxDim * kDnCols / 4 / kDnThreads;    // float4 of S0 a thread
+  float4 sreg[kSB];
+  const float* S0g = st.S[r] + (size_t)h * dk * dv;
+  auto load_state = [&]() {
+#pragma unroll
+    for (int m = 0; m < kSB; ++m) {
+      const int idx = threadIdx.x + m * kDnThreads;
+      const int i = idx / (kDnCols / 4), c = idx - i * (kDnCols / 4);
+      sreg[m] = idx < dk * kDnCols / 4 ? *reinterpret_cast<const float4*>(S0g + (size_t)i * dv + c0 + 4 * c)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  if (state_early) load_state();
   pdl_wait();
   pdl_trigger();
   // every load below is in bounds whatever an earlier kernel left; the status
   // (an earlier error) is read with them and checked before anything is written
   if (threadIdx.x == 0) s_stat = status_get(status);
-  const int h = blockIdx.x, cb = blockIdx.y, r = blockIdx.z;
   const int n = t.n[r], row0 = t.row_off[r];
   const int kh = h / (Hv / Hk);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -92,11 +108,8 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
     gl = g[(size_t)(row0 + lane) * Hv + h];
     bl = beta[(size_t)(row0 + lane) * Hv + h];
   }
-  const int c0 = cb * kDnCols;
   constexpr int kKQ = kMaxRows * kDnMaxDim / 4 / kDnThreads;   // float4 of K and of Q a thread
-  constexpr int kSB = kDnMaxDim * kDnCols / 4 / kDnThreads;    // float4 of S0 a thread
-  float4 kreg[kKQ], qreg[kKQ], sreg[kSB], vreg = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* S0g = st.S[r] + (size_t)h * dk * dv;
+  float4 kreg[kKQ], qreg[kKQ], vreg = make_float4(0.f, 0.f, 0.f, 0.f);
   const int k4 = dk / 4;
 #pragma unroll
   for (int m = 0; m < kKQ; ++m) {
@@ -111,13 +124,7 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
       qreg[m] = *reinterpret_cast<const float4*>(q + off);
     }
   }
-#pragma unroll
-  for (int m = 0; m < kSB; ++m) {
-    const int idx = threadIdx.x + m * kDnThreads;
-    const int i = idx / (kDnCols / 4), c = idx - i * (kDnCols / 4);
-    sreg[m] = idx < dk * kDnCols / 4 ? *reinterpret_cast<const float4*>(S0g + (size_t)i * dv + c0 + 4 * c)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  if (!state_early) load_state();
   if (threadIdx.x < kMaxRows * kDnCols / 4) {   // 256 = 32 nodes x 8 float4
     const int s = threadIdx.x / (kDnCols / 4), c = threadIdx.x - s * (kDnCols / 4);
     if (s < n) vreg = *reinterpret_cast<const float4*>(v + ((size_t)(row0 + s) * Hv + h) * dv + c0 + 4 * c);
@@ -505,11 +512,11 @@ size_t dn_commit_smem(int dk, int dv) { return (size_t)dn_commit_layout(dk, dv).
 
 int launch_dn_verify(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, const float* q,
                      const float* k, const float* v, const float* beta, const float* g, float* o, float* u, float* gc,
-                     int32_t* status, cudaStream_t s) {
+                     int32_t* status, cudaStream_t s, bool state_early) {
   int rc = ensure_smem_limit(dn_verify_kernel, dn_verify_smem(kDnMaxDim), g_dn_verify_smem);
   if (rc) return rc;
   return launch_pdl(dn_verify_kernel, dim3(Hv, dv / kDnCols, t.n_req), dim3(kDnThreads), dn_verify_smem(dk), s, t,
-                    st, Hk, Hv, dk, dv, q, k, v, beta, g, o, u, gc, status);
+                    st, Hk, Hv, dk, dv, q, k, v, beta, g, o, u, gc, status, state_early ? 1 : 0);
 }
 
 int launch_dn_commit(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, int n_layers,

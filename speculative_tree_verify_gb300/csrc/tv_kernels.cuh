@@ -182,9 +182,13 @@ int launch_gumbel_rows(const ReqTable& t, const float* logits, int vocab, float 
                        GumbelPart* part, int32_t* row_tokens, int32_t* status, cudaStream_t st);
 int launch_draw_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const float* uniforms,
                      RowStat* stats, int32_t* row_tokens, int32_t* status, cudaStream_t st);
+// state_early: load each value head's state before the programmatic-launch
+// wait; only for a caller whose preceding kernel triggers after its own wait
+// and whose earlier kernels include every writer of the state (the layer
+// stack: the DeltaNet input stage precedes it)
 int launch_dn_verify(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, const float* q,
                      const float* k, const float* v, const float* beta, const float* g, float* o, float* u, float* gc,
-                     int32_t* status, cudaStream_t s);
+                     int32_t* status, cudaStream_t s, bool state_early = false);
 int launch_dn_commit(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, int n_layers,
                      const float* k, const float* u, const float* gc, const int32_t* path, const int32_t* accept_len,
                      int32_t* status, cudaStream_t s);
