@@ -85,21 +85,6 @@ struct AtSmem {
   static_assert(OFF_K % 1024 == 0, "swizzled slabs start on 1024-byte boundaries");
 };
 
-// 128B-swizzle smem descriptor with explicit leading / stride byte offsets.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-// byte offset of 16-byte chunk c of row r inside a slab of 128-byte rows
-// stored with the 128-byte swizzle (chunk index XOR row mod 8)
-__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
 // 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz;
 // about 2^-22 relative error, 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
@@ -107,8 +92,6 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // the four warps of one query-column slice (named barriers 1..4)
 __device__ __forceinline__ void slice_sync(int cs) {

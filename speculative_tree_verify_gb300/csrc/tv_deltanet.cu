@@ -19,8 +19,13 @@
 // weights.  A chain cut back to its first n nodes is the path of length n.
 //
 //  - dn_verify_kernel: one CTA per (value head, block of 32 value columns,
-//    request); every product in fp32 from shared memory, the triangular solve
-//    by forward substitution in node order (parents come first).
+//    request).  The dot products of the tree's keys and queries with S0's
+//    columns and with each other (K S0, Q S0, K K^T, Q K^T) run as one
+//    tcgen05 MMA chain over bf16 hi/lo splits of the fp32 operands, the four
+//    hi/lo cross terms summed in fp32 (each product term within 2^-17 of the
+//    fp32 product); the coefficients, the right-hand sides, the triangular
+//    solve by forward substitution in node order (parents come first) and the
+//    outputs follow in fp32 on the CUDA cores.
 //  - dn_commit_kernel: persistent, one CTA per SM over the (request, layer,
 //    value head) tiles, two in flight: each d_k x d_v state tile comes in by
 //    one TMA bulk copy, is updated and written back in place (HBM-bound: the
@@ -37,285 +42,6 @@ constexpr int kDnCols = 32;        // value columns per verify CTA
 constexpr int kDnThreads = 512;    // verify CTA
 constexpr int kDnWarps = kDnThreads / 32;
 constexpr int kDnCommitThreads = 512;
-constexpr int kNodeStride = kMaxRows + 4;   // K^T / Q^T row stride: 16-byte aligned rows
-
-// dynamic shared memory of the verify CTA, in floats
-struct DnVerifyLayout {
-  int kt, qt, s0, vb, ks, qs, u, kk, c, a, part, total;
-};
-__host__ __device__ inline DnVerifyLayout dn_verify_layout(int dk) {
-  DnVerifyLayout L;
-  int o = 0;
-  L.kt = o; o += dk * kNodeStride;       // K^T of the key head: [d_k][32 nodes + 4]
-  L.qt = o; o += dk * kNodeStride;       // Q^T
-  L.s0 = o; o += dk * kDnCols;           // S0[:, column block]
-  L.vb = o; o += kMaxRows * kDnCols;     // v[:, column block]
-  L.ks = o; o += kMaxRows * kDnCols;     // K S0, then the right-hand side
-  L.qs = o; o += kMaxRows * kDnCols;     // Q S0
-  L.u = o; o += kMaxRows * kDnCols;      // pseudo-values (first: partial products)
-  L.kk = o; o += kMaxRows * kMaxRows;    // k_t . k_s
-  L.c = o; o += kMaxRows * kMaxRows;     // q_t . k_s, then exp(gc_t - gc_s) (q_t . k_s) on t's path
-  L.a = o; o += kMaxRows * kMaxRows;     // beta_t exp(gc_t - gc_s) (k_t . k_s), s a strict ancestor
-  L.part = o; o += 7 * 4 * 8 * 32;       // partial products of the d_k parts past the first
-  L.total = o;
-  return L;
-}
-
-__global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
-                                                               const float* q, const float* k, const float* v,
-                                                               const float* beta, const float* g, float* o, float* u,
-                                                               float* gc_out, int32_t* status, int state_early) {
-  extern __shared__ __align__(16) float dsm[];
-  __shared__ float s_gc[kMaxRows], s_beta[kMaxRows];
-  __shared__ unsigned s_anc[kMaxRows];   // bit s: s is on t's root path (t included)
-  __shared__ int s_err, s_stat;
-  const int h = blockIdx.x, cb = blockIdx.y, r = blockIdx.z;
-  // the state before the round: with state_early, loaded before the wait (the
-  // caller guarantees that every writer of it has completed by then)
-  const int c0 = cb * kDnCols;
-  constexpr int kSB = kDnMaxDim * kDnCols / 4 / kDnThreads;    // float4 of S0 a thread
-  float4 sreg[kSB];
-  const float* S0g = st.S[r] + (size_t)h * dk * dv;
-  auto load_state = [&]() {
-#pragma unroll
-    for (int m = 0; m < kSB; ++m) {
-      const int idx = threadIdx.x + m * kDnThreads;
-      const int i = idx / (kDnCols / 4), c = idx - i * (kDnCols / 4);
-      sreg[m] = idx < dk * kDnCols / 4 ? *reinterpret_cast<const float4*>(S0g + (size_t)i * dv + c0 + 4 * c)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  if (state_early) load_state();
-  pdl_wait();
-  pdl_trigger();
-  // every load below is in bounds whatever an earlier kernel left; the status
-  // (an earlier error) is read with them and checked before anything is written
-  if (threadIdx.x == 0) s_stat = status_get(status);
-  const int n = t.n[r], row0 = t.row_off[r];
-  const int kh = h / (Hv / Hk);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const DnVerifyLayout L = dn_verify_layout(dk);
-  float *KT = dsm + L.kt, *QT = dsm + L.qt, *S0 = dsm + L.s0, *VB = dsm + L.vb, *KS = dsm + L.ks, *QS = dsm + L.qs,
-        *U = dsm + L.u, *KK = dsm + L.kk, *C = dsm + L.c, *A = dsm + L.a;
-
-  // the loads on the critical path first (warp 0: the tree and the node gates),
-  // then every other load of the CTA, into registers
-  int par = 0, tok = 0;
-  float gl = 0.f, bl = 0.f;
-  if (warp == 0 && lane < n) {
-    par = t.parent[r][lane];
-    tok = t.token[r][lane];
-    gl = g[(size_t)(row0 + lane) * Hv + h];
-    bl = beta[(size_t)(row0 + lane) * Hv + h];
-  }
-  constexpr int kKQ = kMaxRows * kDnMaxDim / 4 / kDnThreads;   // float4 of K and of Q a thread
-  float4 kreg[kKQ], qreg[kKQ], vreg = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int k4 = dk / 4;
-#pragma unroll
-  for (int m = 0; m < kKQ; ++m) {
-    const int idx = threadIdx.x + m * kDnThreads;
-    // node s = the lane: the transposing stores below then hit 32 banks
-    const int s = idx % kMaxRows, c = idx / kMaxRows;   // coordinates 4c .. 4c + 3
-    kreg[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-    qreg[m] = kreg[m];
-    if (idx < kMaxRows * k4 && s < n) {
-      const size_t off = ((size_t)(row0 + s) * Hk + kh) * dk + 4 * c;
-      kreg[m] = *reinterpret_cast<const float4*>(k + off);
-      qreg[m] = *reinterpret_cast<const float4*>(q + off);
-    }
-  }
-  if (!state_early) load_state();
-  if (threadIdx.x < kMaxRows * kDnCols / 4) {   // 256 = 32 nodes x 8 float4
-    const int s = threadIdx.x / (kDnCols / 4), c = threadIdx.x - s * (kDnCols / 4);
-    if (s < n) vreg = *reinterpret_cast<const float4*>(v + ((size_t)(row0 + s) * Hv + h) * dv + c0 + 4 * c);
-  }
-
-  if (warp == 0) {   // the tree: parent order; then cumulative gates and root paths
-    const int err = check_tree_warp(par, tok, n, 0);
-    if (lane == 0) s_err = err;
-    if (err == TV_OK) {
-      if (lane < n) s_beta[lane] = bl;
-      // pointer doubling over the parent links: gc = sum of g over the root path
-      float acc = gl;
-      unsigned anc = lane < n ? (1u << lane) : 0u;
-      int up = lane < n ? par : -1;
-#pragma unroll
-      for (int step = 0; step < 5; ++step) {
-        const int src = up < 0 ? lane : up;
-        const float a2 = __shfl_sync(FULL, acc, src);
-        const unsigned m2 = __shfl_sync(FULL, anc, src);
-        const int u2 = __shfl_sync(FULL, up, src);
-        if (up >= 0) {
-          acc += a2;
-          anc |= m2;
-          up = u2;
-        }
-      }
-      if (lane < n) {
-        s_gc[lane] = acc;
-        s_anc[lane] = anc;
-      }
-    }
-  }
-  // stage K^T, Q^T, S0 and v in shared memory
-#pragma unroll
-  for (int m = 0; m < kKQ; ++m) {
-    const int idx = threadIdx.x + m * kDnThreads;
-    if (idx < kMaxRows * k4) {
-      const int s = idx % kMaxRows, c = idx / kMaxRows;
-      const float kv[4] = {kreg[m].x, kreg[m].y, kreg[m].z, kreg[m].w};
-      const float qv[4] = {qreg[m].x, qreg[m].y, qreg[m].z, qreg[m].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        KT[(4 * c + e) * kNodeStride + s] = kv[e];
-        QT[(4 * c + e) * kNodeStride + s] = qv[e];
-      }
-    }
-  }
-#pragma unroll
-  for (int m = 0; m < kSB; ++m) {
-    const int idx = threadIdx.x + m * kDnThreads;
-    if (idx < dk * kDnCols / 4) reinterpret_cast<float4*>(S0)[idx] = sreg[m];
-  }
-  if (threadIdx.x < kMaxRows * kDnCols / 4) reinterpret_cast<float4*>(VB)[threadIdx.x] = vreg;
-  __syncthreads();
-  if (s_stat != 0) return;
-  if (s_err != TV_OK) {
-    if (threadIdx.x == 0 && h == 0 && cb == 0) status_set(status, s_err);
-    return;
-  }
-
-  // K S0, Q S0, K K^T, Q K^T.  A warp takes 4 contiguous rows (one float4 of
-  // K^T and of Q^T per coordinate) and the column lane; the row groups share
-  // the 16 warps by cutting d_k into `split` parts, whose sums the first
-  // part's warps add in part order.
-  {
-    float* PART = dsm + L.part;
-    const int ng = (n + 3) / 4;                                // row groups of 4
-    const int split = ng <= 2 ? 8 : (ng <= 4 ? 4 : 2);         // ng * split <= 16
-    const int rg = warp % ng, part = warp / ng;
-    const bool live = part < split;
-    const int span = dk / split, i_lo = part * span, i_hi = i_lo + span;
-    float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
-    float kk[4] = {0.f, 0.f, 0.f, 0.f}, qk[4] = {0.f, 0.f, 0.f, 0.f};
-    if (live) {
-      // rows in pairs through the paired fp32 FMA (each half a correctly
-      // rounded fmaf, so the sums are those of scalar fmaf)
-      float2 ks2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}, qs2[2] = {ks2[0], ks2[1]};
-      float2 kk2[2] = {ks2[0], ks2[1]}, qk2[2] = {ks2[0], ks2[1]};
-#pragma unroll 4
-      for (int i = i_lo; i < i_hi; ++i) {
-        const float sij = S0[i * kDnCols + lane];
-        const float kis = KT[i * kNodeStride + lane];
-        const float4 kt4 = *reinterpret_cast<const float4*>(KT + i * kNodeStride + 4 * rg);
-        const float4 qt4 = *reinterpret_cast<const float4*>(QT + i * kNodeStride + 4 * rg);
-        const float2 kt2[2] = {make_float2(kt4.x, kt4.y), make_float2(kt4.z, kt4.w)};
-        const float2 qt2[2] = {make_float2(qt4.x, qt4.y), make_float2(qt4.z, qt4.w)};
-        const float2 s2 = make_float2(sij, sij), k2 = make_float2(kis, kis);
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          ks2[m] = __ffma2_rn(kt2[m], s2, ks2[m]);
-          qs2[m] = __ffma2_rn(qt2[m], s2, qs2[m]);
-          kk2[m] = __ffma2_rn(kt2[m], k2, kk2[m]);
-          qk2[m] = __ffma2_rn(qt2[m], k2, qk2[m]);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        ks[2 * m] = ks2[m].x; ks[2 * m + 1] = ks2[m].y;
-        qs[2 * m] = qs2[m].x; qs[2 * m + 1] = qs2[m].y;
-        kk[2 * m] = kk2[m].x; kk[2 * m + 1] = kk2[m].y;
-        qk[2 * m] = qk2[m].x; qk[2 * m + 1] = qk2[m].y;
-      }
-    }
-    // PART[((part - 1) 4 + product) (4 ng 32) + row 32 + lane]
-    const int pstride = 4 * ng * 32;
-    if (live && part > 0) {
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int tt = 4 * rg + m;
-        float* base = PART + (size_t)(part - 1) * 4 * pstride + tt * 32 + lane;
-        base[0 * pstride] = ks[m];
-        base[1 * pstride] = qs[m];
-        base[2 * pstride] = kk[m];
-        base[3 * pstride] = qk[m];
-      }
-    }
-    __syncthreads();
-    if (live && part == 0) {
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int tt = 4 * rg + m;
-        for (int pp = 1; pp < split; ++pp) {
-          const float* base = PART + (size_t)(pp - 1) * 4 * pstride + tt * 32 + lane;
-          ks[m] += base[0 * pstride];
-          qs[m] += base[1 * pstride];
-          kk[m] += base[2 * pstride];
-          qk[m] += base[3 * pstride];
-        }
-        KS[tt * kDnCols + lane] = ks[m];
-        QS[tt * kDnCols + lane] = qs[m];
-        KK[tt * kMaxRows + lane] = kk[m];
-        C[tt * kMaxRows + lane] = qk[m];
-      }
-    }
-  }
-  __syncthreads();
-  // right-hand side beta_t (v_t - exp(gc_t) S0^T k_t) in place of K S0; the
-  // coefficients A (strict ancestors) and C (the path, t included)
-  for (int idx = threadIdx.x; idx < n * kMaxRows; idx += kDnThreads) {
-    const int tt = idx / kMaxRows, s = idx - tt * kMaxRows;
-    KS[tt * kDnCols + s] = s_beta[tt] * (VB[tt * kDnCols + s] - expf(s_gc[tt]) * KS[tt * kDnCols + s]);
-    const bool on_path = s < n && ((s_anc[tt] >> s) & 1u);
-    const float decay = on_path ? expf(s_gc[tt] - s_gc[s]) : 0.f;
-    A[tt * kMaxRows + s] = (on_path && s < tt) ? s_beta[tt] * decay * KK[tt * kMaxRows + s] : 0.f;
-    C[tt * kMaxRows + s] = decay * C[tt * kMaxRows + s];
-  }
-  // rows past n of U meet zero coefficients in the outputs: clear them
-  for (int idx = n * kDnCols + threadIdx.x; idx < kMaxRows * kDnCols; idx += kDnThreads) U[idx] = 0.f;
-  __syncthreads();
-  // forward substitution u_t = rhs_t - sum_{s < t} A[t][s] u_s, one column per
-  // lane with the column in registers (A is zero off the path)
-  if (warp == 0) {
-    float ur[kMaxRows];
-#pragma unroll
-    for (int tt = 0; tt < kMaxRows; ++tt) {
-      if (tt < n) {
-        float a0 = KS[tt * kDnCols + lane], a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int s4 = 0; s4 < tt; s4 += 4) {
-          const float4 c4 = *reinterpret_cast<const float4*>(A + tt * kMaxRows + s4);
-          a0 = fmaf(-c4.x, ur[s4], a0);
-          if (s4 + 1 < tt) a1 = fmaf(-c4.y, ur[s4 + 1], a1);
-          if (s4 + 2 < tt) a2 = fmaf(-c4.z, ur[s4 + 2], a2);
-          if (s4 + 3 < tt) a3 = fmaf(-c4.w, ur[s4 + 3], a3);
-        }
-        ur[tt] = (a0 + a1) + (a2 + a3);
-        U[tt * kDnCols + lane] = ur[tt];
-      }
-    }
-  }
-  __syncthreads();
-  // outputs o_t = exp(gc_t) S0^T q_t + sum_s C[t][s] u_s
-#pragma unroll
-  for (int m = 0; m < kMaxRows / kDnWarps; ++m) {
-    const int tt = warp + kDnWarps * m;
-    if (tt < n) {
-      float a0 = expf(s_gc[tt]) * QS[tt * kDnCols + lane], a1 = 0.f;
-      for (int s4 = 0; s4 <= tt; s4 += 4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(C + tt * kMaxRows + s4);
-        a0 = fmaf(c4.x, U[s4 * kDnCols + lane], a0);
-        a1 = fmaf(c4.y, U[(s4 + 1) * kDnCols + lane], a1);
-        a0 = fmaf(c4.z, U[(s4 + 2) * kDnCols + lane], a0);
-        a1 = fmaf(c4.w, U[(s4 + 3) * kDnCols + lane], a1);
-      }
-      const size_t off = ((size_t)(row0 + tt) * Hv + h) * dv + c0 + lane;
-      o[off] = a0 + a1;
-      u[off] = U[tt * kDnCols + lane];
-    }
-  }
-  if (cb == 0 && threadIdx.x < n) gc_out[(size_t)(row0 + threadIdx.x) * Hv + h] = s_gc[threadIdx.x];
-}
 
 // Untiled TMA copy global -> shared, completing on an mbarrier (addresses
 // 16-byte aligned, size a multiple of 16).
@@ -334,6 +60,394 @@ __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_prev() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Dynamic shared memory of the verify CTA (bytes from a 1024-byte aligned
+// base).  The tensor-core operands are bf16, K-major, 128-byte swizzled slabs
+// of 64 coordinates each (d_k padded to a multiple of 64 with zeros):
+//   A: 128 rows = k_t hi (rows 0..31), q_t hi (32..63), k_t lo (64..95),
+//      q_t lo (96..127), nodes past n zero;
+//   B: 2 NB rows = S0's 32 block columns (S0^T) hi, the same lo, then the
+//      tree's k rows (NK = 16 when n <= 16, else 32) hi, the same lo;
+// hi = bf16(x), lo = bf16(x - hi).  D = A B^T (fp32, in TMEM): for a k or q
+// row t the four (row, column) combinations t / t + 64 by the hi / lo column
+// sum to (hi + lo)(hi + lo) over d_k, every product term within 2^-17 of the
+// fp32 product.  Then fp32 matrices: the four sums of D ([128 rows][68]) and
+// the solve's operands.
+struct DnVerifyLayout {
+  static constexpr int A_SLAB = 128 * 128;        // bytes per 64-coordinate slab of A
+  static constexpr int B_SLAB = 128 * 128;        // of B (2 NB <= 128 rows)
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + 2 * A_SLAB;
+  static constexpr int OFF_Y = OFF_B + 2 * B_SLAB;                   // [128][68]: D, hi + lo columns added
+  static constexpr int Y_F = 68;
+  static constexpr int OFF_RHS = OFF_Y + 128 * Y_F * 4;              // [32][36] beta_t (v_t - exp(gc_t) S0^T k_t)
+  static constexpr int OFF_EQS = OFF_RHS + kMaxRows * 36 * 4;        // [32][36] exp(gc_t) S0^T q_t
+  static constexpr int OFF_CA = OFF_EQS + kMaxRows * 36 * 4;         // [32][36] A: strict ancestors
+  static constexpr int OFF_CC = OFF_CA + kMaxRows * 36 * 4;          // [32][36] C: the path, t included
+  static constexpr int OFF_V = OFF_CC + kMaxRows * 36 * 4;           // [32][32] v[:, column block]
+  static constexpr int OFF_U = OFF_V + kMaxRows * kDnCols * 4;       // [32][32] pseudo-values
+  static constexpr int BYTES = OFF_U + kMaxRows * kDnCols * 4;
+  static constexpr size_t ALLOC = 1024 + BYTES;
+};
+constexpr int kDnRowF = 36;
+constexpr uint32_t kDnTmemCols = 128;
+constexpr int kDnStageWarps = kDnWarps - 2;                 // warps 14, 15: the tree
+constexpr int kDnStageThreads = 32 * kDnStageWarps;
+constexpr int kDnTasks = 5;   // staging tasks a thread: 16-byte chunks of 8 coordinates (2048 at most)
+
+__device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// hi and lo bf16 planes of 8 consecutive coordinates
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    const float2 hf = __bfloat1622float2(hv);
+    h[e] = bf16x2_bits(hv);
+    l[e] = bf16x2_bits(__floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// u_t = rhs_t - sum_{s < t} A[t][s] u_s by forward substitution in node order
+// (parents come first), column c on lane c in registers.  All NMAX rows are
+// computed (rows past n from whatever their shared-memory rows hold, and
+// never used: row t depends on rows before it only), so the loop is straight
+// code whose coefficient loads need not wait; rows below n are stored at the end.
+template <int NMAX>
+__device__ __forceinline__ void dn_substitute_warp(const float* RHS, const float* CA, float* U, float* u_out,
+                                                   size_t row_stride, int n, int lane) {
+  float ur[NMAX];
+#pragma unroll
+  for (int tt = 0; tt < NMAX; ++tt) {
+    float a0 = RHS[tt * kDnRowF + lane], a1 = 0.f;
+#pragma unroll
+    for (int s4 = 0; s4 < tt; s4 += 4) {
+      const float4 c4 = *reinterpret_cast<const float4*>(CA + tt * kDnRowF + s4);
+      a0 = fmaf(-c4.x, ur[s4], a0);
+      if (s4 + 1 < tt) a1 = fmaf(-c4.y, ur[s4 + 1], a1);
+      if (s4 + 2 < tt) a0 = fmaf(-c4.z, ur[s4 + 2], a0);
+      if (s4 + 3 < tt) a1 = fmaf(-c4.w, ur[s4 + 3], a1);
+    }
+    ur[tt] = a0 + a1;
+  }
+#pragma unroll
+  for (int tt = 0; tt < NMAX; ++tt) {
+    if (tt < n) {
+      U[tt * kDnCols + lane] = ur[tt];
+      u_out[tt * row_stride + lane] = ur[tt];
+    }
+  }
+}
+
+// One CTA per (value head, block of 32 value columns, request), 512 threads.
+// The dot products of the tree's keys and queries with S0's columns and with
+// the tree's keys run on the tensor core (one M=128 MMA chain); the
+// coefficients, the right-hand sides and the triangular solve follow in fp32
+// on the CUDA cores.  Warps 0..13 stage the operands, warp 14 computes the
+// cumulative gates and root paths, warp 15 checks the tree.
+__global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
+                                                               const float* q, const float* k, const float* v,
+                                                               const float* beta, const float* g, float* o, float* u,
+                                                               float* gc_out, int32_t* status, int state_early) {
+  using L = DnVerifyLayout;
+  extern __shared__ __align__(16) uint8_t dn_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dn_smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t s_mma;
+  __shared__ uint32_t s_tmem;
+  __shared__ float s_gc[kMaxRows], s_beta[kMaxRows], s_eg[kMaxRows];
+  __shared__ unsigned s_anc[kMaxRows];   // bit s: s is on t's root path (t included)
+  __shared__ int s_err, s_stat, s_done;
+  const int h = blockIdx.x, cb = blockIdx.y, r = blockIdx.z;
+  const int c0 = cb * kDnCols;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = t.n[r], row0 = t.row_off[r];
+  const int kh = h / (Hv / Hk);
+  const int kcs = dk > 64 ? 4 : 3;              // log2 of the 16-byte chunks of a padded row
+  const int KC = 1 << kcs;
+  const int NK = n <= 16 ? 16 : 32;             // tree-node rows of B (each plane)
+  const int NB = kDnCols + NK;                  // B rows a plane
+  float* Y = reinterpret_cast<float*>(smem + L::OFF_Y);
+  float* RHS = reinterpret_cast<float*>(smem + L::OFF_RHS);
+  float* EQS = reinterpret_cast<float*>(smem + L::OFF_EQS);
+  float* CA = reinterpret_cast<float*>(smem + L::OFF_CA);
+  float* CC = reinterpret_cast<float*>(smem + L::OFF_CC);
+  float* VB = reinterpret_cast<float*>(smem + L::OFF_V);
+  float* U = reinterpret_cast<float*>(smem + L::OFF_U);
+  if (warp == 0) {
+    tmem_alloc(&s_tmem, kDnTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    mbar_init(&s_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  // staging tasks of warps 0..13, task = threadIdx.x + 448 m: [0, 2 NK KC)
+  // rows of A (NK k rows, then NK q rows), then 32 KC of S0's columns (lane =
+  // column: coalesced), then NK KC tree-node k rows of B.  Rows of nodes past
+  // NK are left as they are: they only meet D rows and columns never read.
+  const int nks = n <= 16 ? 4 : 5;              // log2 NK
+  const int nA = 2 * NK * KC, nS = kDnCols * KC, nT = nA + nS + NK * KC;
+  const bool stager = warp < kDnStageWarps;
+  const float* S0g = st.S[r] + (size_t)h * dk * dv + c0;
+  float x[kDnTasks][8];
+  auto load_task = [&](int m, bool state) {
+    const int task = threadIdx.x + kDnStageThreads * m;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[m][e] = 0.f;
+    if (!stager || task >= nT) return;
+    if (task >= nA && task < nA + nS) {
+      if (!state) return;
+      const int id = task - nA, c = id % kDnCols, j = id / kDnCols;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (8 * j + e < dk) x[m][e] = S0g[(size_t)(8 * j + e) * dv + c];
+      return;
+    }
+    if (state) return;
+    const bool a = task < nA;
+    const int id = a ? task : task - nA - nS;
+    const int row = id >> kcs, j = id & (KC - 1);
+    const int node = row & (NK - 1);
+    if (node >= n || 8 * j >= dk) return;
+    const float* src = (a && row >= NK) ? q : k;
+    const float4* p4 = reinterpret_cast<const float4*>(src + ((size_t)(row0 + node) * Hk + kh) * dk + 8 * j);
+    const float4 lo4 = p4[0], hi4 = p4[1];
+    x[m][0] = lo4.x; x[m][1] = lo4.y; x[m][2] = lo4.z; x[m][3] = lo4.w;
+    x[m][4] = hi4.x; x[m][5] = hi4.y; x[m][6] = hi4.z; x[m][7] = hi4.w;
+  };
+  // the state before the round: with state_early loaded before the wait (the
+  // caller guarantees that every writer of it has completed by then)
+  if (state_early) {
+#pragma unroll
+    for (int m = 0; m < kDnTasks; ++m) load_task(m, true);
+  }
+  pdl_wait();
+  pdl_trigger();
+  // every load below is in bounds whatever an earlier kernel left; the status
+  // (an earlier error) is read with them and checked before anything is written
+  if (warp == kDnWarps - 2) {
+    // cumulative gates and root paths by pointer doubling over the parent
+    // links (gc = sum of g over the root path); the tree is checked by warp 15
+    int up = -1;
+    float acc = 0.f, bl = 0.f;
+    if (lane < n) {
+      up = t.parent[r][lane];
+      acc = g[(size_t)(row0 + lane) * Hv + h];
+      bl = beta[(size_t)(row0 + lane) * Hv + h];
+    }
+    up = (lane > 0 && up >= 0 && up < lane) ? up : -1;   // an out-of-order parent stops the walk (warp 15 reports it)
+    unsigned anc = lane < n ? (1u << lane) : 0u;
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+      const int src = up < 0 ? lane : up;
+      const float a2 = __shfl_sync(FULL, acc, src);
+      const unsigned m2 = __shfl_sync(FULL, anc, src);
+      const int u2 = __shfl_sync(FULL, up, src);
+      if (up >= 0) {
+        acc += a2;
+        anc |= m2;
+        up = u2;
+      }
+    }
+    if (lane < n) {
+      s_gc[lane] = acc;
+      s_eg[lane] = expf(acc);
+      s_anc[lane] = anc;
+      s_beta[lane] = bl;
+    }
+  } else if (warp == kDnWarps - 1) {
+    int par = 0, tok = 0;
+    if (lane < n) {
+      par = t.parent[r][lane];
+      tok = t.token[r][lane];
+    }
+    const int err = check_tree_warp(par, tok, n, 0);
+    if (lane == 0) {
+      s_err = err;
+      s_stat = status_get(status);
+    }
+  } else {
+#pragma unroll
+    for (int m = 0; m < kDnTasks; ++m) {
+      const int task = threadIdx.x + kDnStageThreads * m;
+      const bool is_state = task >= nA && task < nA + nS;
+      if (is_state) {
+        if (!state_early) load_task(m, true);
+      } else {
+        load_task(m, false);
+      }
+    }
+    float4 vreg = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int vs = threadIdx.x >> 3, vc = threadIdx.x & 7;   // v[:, column block]: 32 nodes x 8 float4
+    if (threadIdx.x < kMaxRows * kDnCols / 4 && vs < n)
+      vreg = *reinterpret_cast<const float4*>(v + ((size_t)(row0 + vs) * Hv + h) * dv + c0 + 4 * vc);
+    // the operand planes (zeros for nodes past n and coordinates past d_k)
+#pragma unroll
+    for (int m = 0; m < kDnTasks; ++m) {
+      const int task = threadIdx.x + kDnStageThreads * m;
+      if (task >= nT) continue;
+      uint4 hi, lo;
+      split8(x[m], hi, lo);
+      if (task < nA) {
+        const int id = task >> kcs, j = task & (KC - 1);
+        const int row = ((id >> nks) << 5) | (id & (NK - 1));   // k node rows 0.., q node rows 32..
+        uint8_t* base = smem + L::OFF_A + (j >> 3) * L::A_SLAB;
+        *reinterpret_cast<uint4*>(base + swz(row, j & 7)) = hi;
+        *reinterpret_cast<uint4*>(base + swz(row + 64, j & 7)) = lo;
+      } else {
+        int row, row_lo, j;
+        if (task < nA + nS) {   // S0^T: hi rows 0..31, lo rows 32..63
+          const int id = task - nA;
+          row = id % kDnCols;
+          row_lo = kDnCols + row;
+          j = id / kDnCols;
+        } else {                // tree nodes: hi rows 64.., lo rows 64 + NK..
+          const int id = task - nA - nS;
+          row = 2 * kDnCols + (id >> kcs);
+          row_lo = row + NK;
+          j = id & (KC - 1);
+        }
+        uint8_t* base = smem + L::OFF_B + (j >> 3) * L::B_SLAB;
+        *reinterpret_cast<uint4*>(base + swz(row, j & 7)) = hi;
+        *reinterpret_cast<uint4*>(base + swz(row_lo, j & 7)) = lo;
+      }
+    }
+    if (threadIdx.x < kMaxRows * kDnCols / 4) reinterpret_cast<float4*>(VB)[threadIdx.x] = vreg;
+    fence_async_smem();
+  }
+  __syncthreads();
+  const bool go = s_stat == 0 && s_err == TV_OK;
+  if (!go && s_stat == 0 && threadIdx.x == 0 && h == 0 && cb == 0) status_set(status, s_err);
+  if (go) {
+    // (1) D = A B^T: one thread issues and waits
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16_f32(128, 2 * NB);
+      const uint32_t a0 = smem_u32(smem + L::OFF_A), b0 = smem_u32(smem + L::OFF_B);
+      const int ksteps = KC / 2;   // 16 coordinates a step
+#pragma unroll 1
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const uint32_t aa = a0 + (uint32_t)((ks >> 2) * L::A_SLAB + (ks & 3) * 32);
+        const uint32_t bb = b0 + (uint32_t)((ks >> 2) * L::B_SLAB + (ks & 3) * 32);
+        umma_bf16(tmem, sdesc_sw128(aa, 16, 1024), sdesc_sw128(bb, 16, 1024), idesc, ks ? 1u : 0u);
+      }
+      umma_commit(&s_mma);
+      int done = 1;
+      if (!mbar_wait(&s_mma, 0)) {   // report, then wait (bounded) once more before TMEM is freed
+        status_set(status, TV_E_TIMEOUT);
+        mbar_wait(&s_mma, 0);
+        done = 0;
+      }
+      s_done = done;
+    }
+    __syncthreads();
+    if (s_done) {
+      // (2) D to shared memory, hi and lo columns added: warp w reads TMEM
+      //     lanes 32 (w & 3) .. (its subpartition); w < 4 the S0 columns, 4 <= w
+      //     < 8 the tree-node columns
+      if (warp < 8) {
+        tc_fence_after();
+        const int sp = warp & 3;
+        const uint32_t ta = tmem + ((uint32_t)(32 * sp) << 16);
+        float* yr = Y + (32 * sp + lane) * L::Y_F;
+        uint32_t d0[32], d1[32];
+        if (warp < 4) {
+          tmem_ld_32x32b_x32(ta, d0);             // S0 columns x hi
+          tmem_ld_32x32b_x32(ta + kDnCols, d1);   // x lo
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(yr)[j] = make_float4(
+                __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]),
+                __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]),
+                __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]),
+                __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]));
+        } else {
+          const uint32_t tn = ta + 2 * kDnCols;
+          tmem_ld_32x32b_x32(tn, d0);   // NK = 16: hi 0..15, lo 16..31; NK = 32: hi
+          if (NK == 32) tmem_ld_32x32b_x32(tn + 32, d1);   // lo
+          tmem_ld_wait();
+          if (NK == 16) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              reinterpret_cast<float4*>(yr + kDnCols)[j] = make_float4(
+                  __uint_as_float(d0[4 * j]) + __uint_as_float(d0[16 + 4 * j]),
+                  __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d0[16 + 4 * j + 1]),
+                  __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d0[16 + 4 * j + 2]),
+                  __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d0[16 + 4 * j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              reinterpret_cast<float4*>(yr + kDnCols)[j] = make_float4(
+                  __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]),
+                  __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]),
+                  __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]),
+                  __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]));
+          }
+        }
+      }
+      __syncthreads();
+      // (3) a warp per tree row t, the column on the lane: x = Y[t] + Y[64 + t]
+      //     (k_t) and Y[32 + t] + Y[96 + t] (q_t); the right-hand side and A
+      //     from k_t, exp(gc_t) S0^T q_t and C from q_t, zero off the path
+      for (int tt = warp; tt < n; tt += kDnWarps) {
+        const float* yk = Y + tt * L::Y_F;
+        const float* yq = Y + (32 + tt) * L::Y_F;
+        const float bt = s_beta[tt], et = s_eg[tt];
+        const float pk = yk[lane] + yk[64 * L::Y_F + lane];
+        const float pq = yq[lane] + yq[64 * L::Y_F + lane];
+        RHS[tt * kDnRowF + lane] = bt * (VB[tt * kDnCols + lane] - et * pk);
+        EQS[tt * kDnRowF + lane] = et * pq;
+        if (lane < NK) {
+          const int s = lane;
+          const float kk = yk[kDnCols + s] + yk[64 * L::Y_F + kDnCols + s];
+          const float qk = yq[kDnCols + s] + yq[64 * L::Y_F + kDnCols + s];
+          const bool on = s < n && ((s_anc[tt] >> s) & 1u);
+          const float decay = on ? expf(s_gc[tt] - s_gc[s]) : 0.f;
+          CA[tt * kDnRowF + s] = (on && s != tt) ? bt * decay * kk : 0.f;
+          CC[tt * kDnRowF + s] = on ? decay * qk : 0.f;
+        }
+      }
+      __syncthreads();
+      // (4) the pseudo-values, one warp
+      if (warp == 0) {
+        float* uo = u + ((size_t)row0 * Hv + h) * dv + c0;
+        if (n <= 16) dn_substitute_warp<16>(RHS, CA, U, uo, (size_t)Hv * dv, n, lane);
+        else dn_substitute_warp<kMaxRows>(RHS, CA, U, uo, (size_t)Hv * dv, n, lane);
+      }
+      __syncthreads();
+      // (5) o_t = exp(gc_t) S0^T q_t + sum_{s <= t} C[t][s] u_s
+      for (int r2 = warp; r2 < n; r2 += kDnWarps) {
+        float a0 = EQS[r2 * kDnRowF + lane], a1 = 0.f;
+        for (int s4 = 0; s4 <= r2; s4 += 4) {
+          const float4 c4 = *reinterpret_cast<const float4*>(CC + r2 * kDnRowF + s4);
+          a0 = fmaf(c4.x, U[s4 * kDnCols + lane], a0);
+          if (s4 + 1 <= r2) a1 = fmaf(c4.y, U[(s4 + 1) * kDnCols + lane], a1);
+          if (s4 + 2 <= r2) a0 = fmaf(c4.z, U[(s4 + 2) * kDnCols + lane], a0);
+          if (s4 + 3 <= r2) a1 = fmaf(c4.w, U[(s4 + 3) * kDnCols + lane], a1);
+        }
+        o[((size_t)(row0 + r2) * Hv + h) * dv + c0 + lane] = a0 + a1;
+      }
+      if (cb == 0 && threadIdx.x < n) gc_out[(size_t)(row0 + threadIdx.x) * Hv + h] = s_gc[threadIdx.x];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kDnTmemCols);
+  }
+}
 
 // dynamic shared memory of the commit CTA, in floats: two slots of (state
 // tile, the path's k rows, u rows, gates, weights)
@@ -499,7 +613,7 @@ __global__ void __launch_bounds__(kDnCommitThreads, 1) dn_commit_kernel(ReqTable
     if (tile + 2 * (int)gridDim.x < n_tiles) stage(tile + 2 * gridDim.x, slot);
     cp_async_commit();
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  cp_async_wait_all();
 }
 
 std::atomic<bool> g_dn_verify_smem[64];
@@ -507,7 +621,7 @@ std::atomic<bool> g_dn_commit_smem[64];
 
 }  // namespace
 
-size_t dn_verify_smem(int dk) { return (size_t)dn_verify_layout(dk).total * sizeof(float); }
+size_t dn_verify_smem(int) { return DnVerifyLayout::ALLOC; }
 size_t dn_commit_smem(int dk, int dv) { return (size_t)dn_commit_layout(dk, dv).total * sizeof(float); }
 
 int launch_dn_verify(const ReqTable& t, const DnStates& st, int Hk, int Hv, int dk, int dv, const float* q,

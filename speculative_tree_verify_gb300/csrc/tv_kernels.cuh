@@ -88,12 +88,14 @@ __device__ __forceinline__ int check_tree_warp(int par, int tok, int n, int voca
   const int lane = threadIdx.x & 31;
   const bool bad_order = lane < n && (lane == 0 ? par != -1 : (par < 0 || par >= lane));
   const bool bad_token = lane < n && vocab > 0 && (tok < 0 || tok >= vocab);
-  bool dup = false;
-  for (int j = 1; j < 32; ++j) {
-    const int pj = __shfl_sync(0xffffffffu, par, j);
-    const int tj = __shfl_sync(0xffffffffu, tok, j);
-    if (j < lane && lane < n && pj == par && tj == tok) dup = true;
-  }
+  // a duplicate sibling: a lower lane with the same (parent, token); lanes
+  // past n get keys no tree lane has (a parent of 0x80000000 + lane would be
+  // out of order, which is reported first)
+  const unsigned long long key =
+      lane < n ? ((unsigned long long)(unsigned)par << 32) | (unsigned)tok
+               : (unsigned long long)(0x80000000u + (unsigned)lane) << 32;
+  const unsigned same = __match_any_sync(0xffffffffu, key);
+  const bool dup = lane < n && (same & ((1u << lane) - 1u)) != 0u;
   if (__any_sync(0xffffffffu, bad_order)) return TV_E_ORDER;
   if (__any_sync(0xffffffffu, bad_token)) return TV_E_TOKEN;
   if (__any_sync(0xffffffffu, dup)) return TV_E_DUP_SIBLING;

@@ -63,6 +63,7 @@ def _close(gpu, orc, what):
     err = np.abs(gpu.astype(np.float64) - orc) / (1.0 + np.abs(orc))
     assert np.all(np.isfinite(gpu)), f"{what}: non-finite"
     assert err.max() <= TOL, f"{what}: worst error {err.max():.3e} x (1 + |x|) > {TOL}"
+    print(f"{what}: worst error {err.max():.3e} x (1 + |x|)")
     return float(err.max())
 
 
