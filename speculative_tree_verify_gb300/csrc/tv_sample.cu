@@ -62,6 +62,11 @@ struct FilterShared {
   int cnt2[2];                          // its level-2 boundary-bin tokens, per selection (read by the cluster)
   int off[kFCluster + 1];               // the cluster's level-2 boundary-bin tokens, prefix by CTA
   uint32_t key_sel;
+  unsigned long long totw[kFBins];      // the fast cut: the cluster's weight histogram
+  unsigned long long wsum[kFWarps];     // and block scans' warp totals
+  unsigned long long csum[kFWarps];
+  float pub_top;                        // the fast top_k cut: this CTA's grid anchor (read by the cluster)
+  float tops[kFCluster];                // every CTA's anchor
 };
 
 // The cluster's histogram tot[] from every CTA's hist[hb] (after a cluster barrier).
@@ -314,6 +319,330 @@ __device__ uint32_t select_key(FilterShared& sh, const float* xs, uint16_t* cand
   return prefix;
 }
 
+// The fast cut.  One level-1 pass over the slice counts the tokens (key >= 1:
+// not NaN) per bin, and weighs them too when top_p is the only cut; the
+// cluster's histogram places the boundary bin B of the first cut (the k-th
+// largest, else the top_p boundary).  When B and the bins above it hold at
+// most kFastCap tokens cluster-wide, every CTA lists its tokens of bins <= B,
+// gathers the cluster's (a thread a candidate) and takes the cuts exactly,
+// with the integer weights of select_key and no further cluster barrier, by
+// counting: a candidate's key is the k-th largest when fewer than k keys are
+// larger and at least k are at least as large, and the top_p key when the
+// weight of the larger keys falls short of need and with its ties reaches it;
+// kfloor = the top_k key, then the top_p key among the tokens at or above it.
+// Returns false, having decided nothing, when the candidates are more (the
+// caller then takes the general path after a cluster barrier).  `region`
+// holds the private histograms, then the gathered keys, logits and weights.
+constexpr int kFastCap = 256;
+
+// Over a histogram h[256] (a thread a bin, threads 0..255): the first bin at
+// which the running sum reaches need, the sum before it and the running
+// count (c) through it; res = {bin or ~0, count through it}.  Block-wide scan.
+__device__ __forceinline__ void boundary_bin(FilterShared& sh, const unsigned long long* h,
+                                             const unsigned long long* c, unsigned long long need) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = 0ull, y = 0ull;
+  if (threadIdx.x < kFBins) {
+    x = h[threadIdx.x];
+    y = c[threadIdx.x];
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(FULL, x, o), v = __shfl_up_sync(FULL, y, o);
+    if (lane >= o) {
+      x += u;
+      y += v;
+    }
+  }
+  if (lane == 31 && warp < kFBins / 32) {
+    sh.wsum[warp] = x;
+    sh.csum[warp] = y;
+  }
+  if (threadIdx.x == 0) sh.res[0] = ~0ull;
+  __syncthreads();
+  if (threadIdx.x < kFBins) {
+    unsigned long long bx = 0ull, by = 0ull;
+    for (int v = 0; v < warp; ++v) {
+      bx += sh.wsum[v];
+      by += sh.csum[v];
+    }
+    const unsigned long long incl = bx + x, excl = incl - h[threadIdx.x];
+    if (incl >= need && excl < need) {   // the one bin where the running sum crosses need
+      sh.res[0] = (unsigned long long)threadIdx.x;
+      sh.res[1] = by + y;
+    }
+  }
+  __syncthreads();
+}
+
+__device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsigned char* region, int n_loc,
+                         float& M, float m_loc, float inv_t, int top_k, float top_p, bool by_k, float log_min_p,
+                         float* orow) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // top_p alone: bins of (M - x) / T * 8 under the cluster maximum M.  top_k:
+  // bins on a fixed grid, g(x) = floor(x / T * 8), counted down from each CTA's
+  // own anchor floor(m_loc / T * 8); the cluster's histogram shifts each CTA's
+  // by its anchor's distance to the highest anchor, exact in bins 0..254 (bin
+  // 255 lumps the rest), so no maximum needs exchanging first
+  const bool anchored = by_k;
+  const float s8 = inv_t * kFBinsPerUnit;
+  const float top_loc = floorf(m_loc * s8);
+  auto bin_of = [&](float x) { return (int)fminf((M - x) * inv_t * kFBinsPerUnit, (float)(kFBins - 1)); };
+  auto lbin = [&](float x) { return anchored ? (int)fminf(top_loc - floorf(x * s8), (float)(kFBins - 1)) : bin_of(x); };
+  auto wt = [&](float x) { return (unsigned long long)__float2ull_rn(expf((x - M) * inv_t) * 4294967296.f); };
+  // level 1 into private histograms: counts; weights as hi * 2^16 + lo
+  uint32_t* pc = reinterpret_cast<uint32_t*>(region);            // [kFPriv][kFBins]
+  uint32_t* pw = pc + kFPriv * kFBins;                            // [kFPriv][2][kFBins]
+  for (int b = threadIdx.x; b < kFPriv * 3 * kFBins; b += kFThreads) pc[b] = 0u;
+  if (threadIdx.x == 0) {
+    sh.cnt1 = 0;
+    sh.pub_top = top_loc;
+  }
+  __syncthreads();
+  {
+    uint32_t* myc = pc + (warp & (kFPriv - 1)) * kFBins;
+    uint32_t* myw = pw + (warp & (kFPriv - 1)) * 2 * kFBins;
+    auto one = [&](float x) {
+      if (fkey(x) >= 1u) {
+        const int b = lbin(x);
+        atomicAdd(&myc[b], 1u);
+        if (!by_k) {
+          const unsigned long long w = wt(x);
+          atomicAdd(&myw[b], (uint32_t)(w & 0xFFFFull));
+          const uint32_t hi = (uint32_t)(w >> 16);
+          if (hi != 0u) atomicAdd(&myw[kFBins + b], hi);
+        }
+      }
+    };
+    const int n4 = n_loc >> 2;
+    for (int j = threadIdx.x; j < n4; j += kFThreads) {
+      const float4 x4 = reinterpret_cast<const float4*>(xs)[j];
+      one(x4.x);
+      one(x4.y);
+      one(x4.z);
+      one(x4.w);
+    }
+    for (int i = 4 * n4 + threadIdx.x; i < n_loc; i += kFThreads) one(xs[i]);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < kFBins; b += kFThreads) {
+    unsigned long long c = 0ull, w = 0ull;
+#pragma unroll
+    for (int g = 0; g < kFPriv; ++g) {
+      c += pc[g * kFBins + b];
+      w += (unsigned long long)pw[g * 2 * kFBins + b] + ((unsigned long long)pw[g * 2 * kFBins + kFBins + b] << 16);
+    }
+    sh.hist[0][b] = c;
+    sh.hist[1][b] = w;
+  }
+  cluster_sync_all();
+  float top = 0.f;   // anchored: the highest anchor
+  if (anchored) {    // every CTA's anchor and maximum
+    if (threadIdx.x < 32) {
+      float t = -INFINITY, m = -INFINITY;
+      if (lane < kFCluster) {
+        t = ld_dsmem_f32(dsmem_addr(&sh.pub_top, lane));
+        m = ld_dsmem_f32(dsmem_addr(&sh.pub_max, lane));
+        sh.tops[lane] = t;
+      }
+      // anchors past 2^23 are not exact integers: no fast cut
+      const bool bad = __any_sync(FULL, t != -INFINITY && fabsf(t) >= 8388608.f);
+      t = warp_max(t);
+      m = warp_max(m);
+      if (lane == 0) {
+        sh.M = m;
+        sh.res[0] = bad ? 1ull : 0ull;
+        sh.key_sel = __float_as_uint(t);
+      }
+    }
+    __syncthreads();
+    M = sh.M;
+    top = __uint_as_float(sh.key_sel);
+    if (M == -INFINITY || sh.res[0] != 0ull) return false;
+  }
+  unsigned long long wall = 0ull;   // this bin's cluster weight
+  if (threadIdx.x < kFBins) {   // every remote load issued before the sums
+    unsigned long long c[kFCluster], wv[kFCluster];
+#pragma unroll
+    for (int r = 0; r < kFCluster; ++r) {
+      int lb = threadIdx.x;
+      if (anchored) {   // this CTA's bin at global bin threadIdx.x, or none
+        const float d = top - sh.tops[r];
+        lb = (threadIdx.x < kFBins - 1 && d <= (float)(kFBins - 2)) ? (int)threadIdx.x - (int)d : -1;
+      }
+      c[r] = lb >= 0 ? ld_dsmem_u64(dsmem_addr(&sh.hist[0][lb], r)) : 0ull;
+      wv[r] = by_k ? 0ull : ld_dsmem_u64(dsmem_addr(&sh.hist[1][threadIdx.x], r));
+    }
+    unsigned long long cs = 0ull;
+#pragma unroll
+    for (int r = 0; r < kFCluster; ++r) {
+      cs += c[r];
+      wall += wv[r];
+    }
+    // anchored: the last bin lumps tokens of every depth; as the boundary it
+    // holds too many candidates for the fast cut
+    if (anchored && threadIdx.x == kFBins - 1) cs = 1ull << 40;
+    sh.tot[threadIdx.x] = cs;
+    sh.totw[threadIdx.x] = wall;
+  }
+  // the need of the first cut: k, else ceil(top_p x the row's weight)
+  unsigned long long need = (unsigned long long)top_k;
+  if (!by_k) {   // one thread evaluates the need (FP64 is slow here)
+    const unsigned long long ws = warp_sum(wall);
+    if (lane == 0 && warp < kFBins / 32) sh.csum[warp] = ws;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long s = 0ull;
+      for (int v = 0; v < kFBins / 32; ++v) s += sh.csum[v];
+      const double want = ceil((double)top_p * (double)s);
+      sh.res[2] = want < 1.0 ? 1ull : (want >= (double)s ? s : (unsigned long long)want);
+    }
+    __syncthreads();
+    need = sh.res[2];
+  }
+  __syncthreads();
+  boundary_bin(sh, by_k ? sh.tot : sh.totw, sh.tot, need);
+  if (sh.res[0] == ~0ull || sh.res[1] > (unsigned long long)kFastCap) return false;
+  const int B = (int)sh.res[0];
+  const int C = (int)sh.res[1];
+  
+  // the candidates (key >= 1, bin <= B), listed by every CTA with their
+  // logits; every output of the slice is written -inf on the way (the kept
+  // candidates are written again at the end, after a CTA barrier)
+  float* cx = reinterpret_cast<float*>(region + kFPriv * 3 * kFBins * sizeof(uint32_t));   // past the histograms
+  {
+    const float gmin = top - (float)B;   // anchored: bins <= B are g(x) >= top - B
+    auto in = [&](float x) { return fkey(x) >= 1u && (anchored ? floorf(x * s8) >= gmin : bin_of(x) <= B); };
+    auto put = [&](bool ok, int i, float x) {
+      const unsigned mk = __ballot_sync(FULL, ok);
+      if (mk == 0u) return;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sh.cnt1, __popc(mk));
+      base = __shfl_sync(FULL, base, 0);
+      if (ok) {   // at most C <= kFastCap a CTA
+        const int slot = base + __popc(mk & ((1u << lane) - 1u));
+        cand[slot] = (uint16_t)i;
+        cx[slot] = x;
+      }
+    };
+    const bool vec_out = (reinterpret_cast<uintptr_t>(orow) & 15u) == 0;
+    const int n4 = n_loc >> 2;
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    for (int j0 = warp * 32; j0 < n4; j0 += kFThreads) {   // warp-uniform trip count
+      const int j = j0 + lane;
+      float4 x4 = make_float4(NAN, NAN, NAN, NAN);
+      if (j < n4) {
+        x4 = reinterpret_cast<const float4*>(xs)[j];
+        if (vec_out) {
+          reinterpret_cast<float4*>(orow)[j] = ninf;
+        } else {
+          orow[4 * j] = -INFINITY;
+          orow[4 * j + 1] = -INFINITY;
+          orow[4 * j + 2] = -INFINITY;
+          orow[4 * j + 3] = -INFINITY;
+        }
+      }
+      const bool a0 = in(x4.x), a1 = in(x4.y), a2 = in(x4.z), a3 = in(x4.w);
+      if (__any_sync(FULL, a0 || a1 || a2 || a3)) {
+        put(a0, 4 * j, x4.x);
+        put(a1, 4 * j + 1, x4.y);
+        put(a2, 4 * j + 2, x4.z);
+        put(a3, 4 * j + 3, x4.w);
+      }
+    }
+    if (warp == 0) {
+      const int i = 4 * n4 + lane;
+      const float x = i < n_loc ? xs[i] : NAN;
+      if (i < n_loc) orow[i] = -INFINITY;
+      put(in(x), i, x);
+    }
+  }
+  cluster_sync_all();
+  if (threadIdx.x < 32) {
+    int c = lane < kFCluster ? ld_dsmem_s32(dsmem_addr(&sh.cnt1, lane)) : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(FULL, c, o);
+      if (lane >= o) c += u;
+    }
+    if (lane < kFCluster) sh.off[lane + 1] = c;
+    if (lane == 0) sh.off[0] = 0;
+  }
+  __syncthreads();
+  // gathered: thread i < C holds candidate i; keys and weights shared
+  uint32_t* gk = reinterpret_cast<uint32_t*>(region);
+  unsigned long long* gw = reinterpret_cast<unsigned long long*>(region + kFastCap * sizeof(uint32_t));
+  uint32_t key = 0u;
+  unsigned long long w = 0ull;
+  if ((int)threadIdx.x < C) {
+    int r = 0;
+    while ((int)threadIdx.x >= sh.off[r + 1]) ++r;
+    const float x = ld_dsmem_f32(dsmem_addr(&cx[threadIdx.x - sh.off[r]], r));
+    key = fkey(x);
+    w = top_p < 1.f ? wt(x) : 0ull;
+    gk[threadIdx.x] = key;
+    gw[threadIdx.x] = w;
+  }
+  cluster_arrive();   // no more reads of other CTAs' shared memory
+  if (threadIdx.x == 0) {
+    sh.key_sel = 1u;   // above every NaN key
+    sh.res[2] = 0ull;
+  }
+  __syncthreads();
+  // one pass over the candidates: the count and the weight of the keys above
+  // and at or above each candidate's own; G adjacent threads share a
+  // candidate (each every G-th key), summed across them by shuffles
+  int G = 1;
+  while (G < 32 && G * 2 * C <= kFThreads) G <<= 1;
+  const int ci = (int)threadIdx.x / G, part = (int)threadIdx.x % G;
+  const uint32_t ki = ci < C ? gk[ci] : 0u;
+  int above = 0, ge = 0;
+  unsigned long long wabove = 0ull, wge = 0ull;
+  if (ci < C) {
+#pragma unroll 4
+    for (int j = part; j < C; j += G) {
+      const uint32_t kj = gk[j];
+      const unsigned long long wj = gw[j];
+      above += kj > ki;
+      ge += kj >= ki;
+      wabove += kj > ki ? wj : 0ull;
+      wge += kj >= ki ? wj : 0ull;
+    }
+  }
+  for (int o = 1; o < G; o <<= 1) {   // G divides 32: the group sits in one warp
+    above += __shfl_xor_sync(FULL, above, o);
+    ge += __shfl_xor_sync(FULL, ge, o);
+    wabove += __shfl_xor_sync(FULL, wabove, o);
+    wge += __shfl_xor_sync(FULL, wge, o);
+  }
+  // top_k: the k-th largest key, and top_p's need over the weight at or above
+  // it, evaluated by the key's threads only (FP64 is slow here; a key's ties
+  // write the same values)
+  if (ci < C && part == 0 && by_k && above < top_k && ge >= top_k) {
+    sh.key_sel = ki;
+    if (top_p < 1.f) {
+      const double want = ceil((double)top_p * (double)wge);
+      sh.res[2] = want < 1.0 ? 1ull : (want >= (double)wge ? wge : (unsigned long long)want);
+    }
+  }
+  __syncthreads();
+  uint32_t kfloor = sh.key_sel;
+  if (top_p < 1.f) {
+    const unsigned long long nd = by_k ? sh.res[2] : need;
+    __syncthreads();   // every thread has read the top_k key
+    if (ci < C && part == 0 && ki >= kfloor && wabove < nd && wge >= nd) sh.key_sel = ki;
+    __syncthreads();
+    kfloor = sh.key_sel;
+  }
+  // the kept candidates' outputs: x = l / T when key >= kfloor and min_p holds
+  for (int s2 = threadIdx.x; s2 < sh.cnt1; s2 += kFThreads) {
+    const float l = cx[s2];
+    if (fkey(l) >= kfloor && (l - M) * inv_t >= log_min_p) orow[cand[s2]] = l * inv_t;
+  }
+  cluster_wait();
+  return true;
+}
+
 __device__ __forceinline__ float block_max(float v, float* red) {
   v = warp_max(v);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
@@ -347,24 +676,47 @@ __global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
   float* orow = out + (size_t)row * V + lo;
 
   float mx = -INFINITY;
-  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
+  // float4 where the row slice is 16-byte aligned (the slice offset is a
+  // multiple of 8 tokens), the tail one by one
+  const bool vec_in = (reinterpret_cast<uintptr_t>(lr) & 15u) == 0;
+  const int n4 = vec_in ? n_loc >> 2 : 0;
+  for (int j = threadIdx.x; j < n4; j += kFThreads) {
+    const float4 v = reinterpret_cast<const float4*>(lr)[j];
+    reinterpret_cast<float4*>(xs)[j] = v;
+    mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+  }
+  for (int i = 4 * n4 + threadIdx.x; i < n_loc; i += kFThreads) {
     const float v = lr[i];
     xs[i] = v;
     mx = fmaxf(mx, v);
   }
   mx = block_max(mx, sh.redf);
   if (threadIdx.x == 0) sh.pub_max = mx;
-  cluster_sync_all();
-  if (threadIdx.x < 32) {
-    float m = threadIdx.x < kFCluster ? ld_dsmem_f32(dsmem_addr(&sh.pub_max, threadIdx.x)) : -INFINITY;
-    m = warp_max(m);
-    if (threadIdx.x == 0) sh.M = m;
-  }
-  __syncthreads();
-  const float M = sh.M;
   int hb = 0;
   uint32_t kfloor = 1u;   // above every NaN key
-  if (M != -INFINITY) {
+  const bool by_k = top_k > 0 && top_k < V;
+  float M = -INFINITY;
+  unsigned char* region = reinterpret_cast<unsigned char*>(cand2);
+  if (by_k) {   // the fast top_k cut reads the cluster maximum with its histograms
+    if (fast_cut(sh, xs, cand1, region, n_loc, M, mx, inv_t, top_k, top_p, true, log_min_p, orow))
+      return;   // outputs written, and the cluster's reads of this CTA done
+    cluster_sync_all();   // every CTA has read the fast cut's shared memory
+  } else {
+    cluster_sync_all();
+    if (threadIdx.x < 32) {
+      float m = threadIdx.x < kFCluster ? ld_dsmem_f32(dsmem_addr(&sh.pub_max, threadIdx.x)) : -INFINITY;
+      m = warp_max(m);
+      if (threadIdx.x == 0) sh.M = m;
+    }
+    __syncthreads();
+    M = sh.M;
+    if (M != -INFINITY && top_p < 1.f) {
+      if (fast_cut(sh, xs, cand1, region, n_loc, M, mx, inv_t, top_k, top_p, false, log_min_p, orow)) return;
+      cluster_sync_all();
+    }
+  }
+  const bool done = M == -INFINITY || (!by_k && !(top_p < 1.f));
+  if (!done) {
     if (top_k > 0 && top_k < V)
       kfloor = select_key(sh, xs, cand1, cand2, scratch, n_loc, M, inv_t, kfloor, (unsigned long long)top_k, 0.0,
                           [](float) { return 1ull; }, 0, hb);
@@ -374,11 +726,16 @@ __global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
           [=](float x) { return (unsigned long long)__float2ull_rn(expf((x - M) * inv_t) * 4294967296.f); }, 1, hb);
   }
   // min_p: x >= x_max + log(min_p), i.e. (l - l_max) / T >= log(min_p)
-  for (int i = threadIdx.x; i < n_loc; i += kFThreads) {
-    const float l = xs[i];
+  auto filt = [&](float l) {
     const bool keep = M != -INFINITY && fkey(l) >= kfloor && (l - M) * inv_t >= log_min_p;
-    orow[i] = keep ? l * inv_t : -INFINITY;
+    return keep ? l * inv_t : -INFINITY;
+  };
+  const int o4 = (reinterpret_cast<uintptr_t>(orow) & 15u) == 0 ? n_loc >> 2 : 0;
+  for (int j = threadIdx.x; j < o4; j += kFThreads) {
+    const float4 l = reinterpret_cast<const float4*>(xs)[j];
+    reinterpret_cast<float4*>(orow)[j] = make_float4(filt(l.x), filt(l.y), filt(l.z), filt(l.w));
   }
+  for (int i = 4 * o4 + threadIdx.x; i < n_loc; i += kFThreads) orow[i] = filt(xs[i]);
   cluster_sync_all();   // no CTA leaves while the cluster may still read its shared memory
 }
 
