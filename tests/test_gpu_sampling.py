@@ -144,6 +144,21 @@ def test_filter_signed_zero_ties(gpu):
     g = _filter_check(logits, 1.0, 4, 1.0, 0.0)
     assert np.isfinite(g[0, 10]) and np.isfinite(g[0, 20]) and np.isfinite(g[0]).sum() == 5
 
+def test_filter_large_logits(gpu):
+    """logits near 1e7: the fast top_k cut's fixed grid (8 bins a unit of
+    l / T) leaves float's exact integers there, so the three-level selection
+    decides; a row with few tokens per slice and one small row take the fast cut"""
+    V = 151936
+    rng = np.random.default_rng(12)
+    logits = np.empty((3, V), np.float32)
+    logits[0] = (1e7 + rng.standard_normal(V) * 1e3).astype(np.float32)
+    logits[1] = (rng.standard_normal(V) * 4.0).astype(np.float32)
+    logits[2] = -np.inf
+    logits[2, rng.choice(V, 40, replace=False)] = rng.standard_normal(40).astype(np.float32)
+    for T, k, p, mp in ((1.0, 20, 1.0, 0.0), (0.8, 50, 0.9, 0.02), (1.0, 30, 0.7, 0.0)):
+        _filter_check(logits, T, k, p, mp)
+
+
 def test_filter_rejects_bad_arguments(gpu):
     x = torch.zeros(2, 16, device="cuda")
     out = torch.empty_like(x)
