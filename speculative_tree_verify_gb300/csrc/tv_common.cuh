@@ -301,6 +301,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
 // every thread of every CTA of the cluster; orders shared-memory writes before
 // it against reads after it, in this CTA and the others
 __device__ __forceinline__ void cluster_sync_all() {
@@ -408,6 +413,27 @@ inline int launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...) == cudaSuccess ? TV_OK : TV_E_CUDA;
+}
+
+// launch_pdl with thread-block clusters of cluster_x CTAs along x
+template <typename... Exp, typename... Act>
+inline int launch_pdl_cluster(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              int cluster_x, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...) == cudaSuccess ? TV_OK : TV_E_CUDA;
 }
 

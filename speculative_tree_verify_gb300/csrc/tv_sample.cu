@@ -30,7 +30,7 @@ namespace {
 constexpr unsigned FULL = 0xffffffffu;
 
 // ---- filter --------------------------------------------------------------------------
-constexpr int kFCluster = 8;            // CTAs per row
+constexpr int kFCluster = 8;            // CTAs per row at most (6 or 8, chosen at launch)
 constexpr int kFThreads = 512;
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kFBins = 256;
@@ -74,7 +74,8 @@ __device__ __forceinline__ void cluster_hist(FilterShared& sh, int hb) {
   if (threadIdx.x < kFBins) {
     unsigned long long s = 0ull;
 #pragma unroll
-    for (int r = 0; r < kFCluster; ++r) s += ld_dsmem_u64(dsmem_addr(&sh.hist[hb][threadIdx.x], r));
+    for (int r = 0; r < kFCluster; ++r)
+      if (r < (int)cluster_nctarank()) s += ld_dsmem_u64(dsmem_addr(&sh.hist[hb][threadIdx.x], r));
     sh.tot[threadIdx.x] = s;
   }
   __syncthreads();
@@ -256,17 +257,18 @@ __device__ uint32_t select_key(FilterShared& sh, const float* xs, uint16_t* cand
   cluster_sync_all();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    int c = lane < kFCluster ? ld_dsmem_s32(dsmem_addr(&sh.cnt2[sel], lane)) : 0;
+    const int ncl = (int)cluster_nctarank();
+    int c = lane < ncl ? ld_dsmem_s32(dsmem_addr(&sh.cnt2[sel], lane)) : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int u = __shfl_up_sync(FULL, c, o);
       if (lane >= o) c += u;
     }
-    if (lane < kFCluster) sh.off[lane + 1] = c;
+    if (lane < ncl) sh.off[lane + 1] = c;
     if (lane == 0) sh.off[0] = 0;
   }
   __syncthreads();
-  const int total = sh.off[kFCluster];
+  const int total = sh.off[cluster_nctarank()];
 
   if (total <= kGatherMax) {   // every CTA ranks the whole bin (each listed all of its tokens)
     unsigned long long* gw = reinterpret_cast<unsigned long long*>(scratch);
@@ -379,6 +381,7 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
                          float& M, float m_loc, float inv_t, int top_k, float top_p, bool by_k, float log_min_p,
                          float* orow) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ncl = (int)cluster_nctarank();
   // top_p alone: bins of (M - x) / T * 8 under the cluster maximum M.  top_k:
   // bins on a fixed grid, g(x) = floor(x / T * 8), counted down from each CTA's
   // own anchor floor(m_loc / T * 8); the cluster's histogram shifts each CTA's
@@ -440,7 +443,7 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
   if (anchored) {    // every CTA's anchor and maximum
     if (threadIdx.x < 32) {
       float t = -INFINITY, m = -INFINITY;
-      if (lane < kFCluster) {
+      if (lane < ncl) {
         t = ld_dsmem_f32(dsmem_addr(&sh.pub_top, lane));
         m = ld_dsmem_f32(dsmem_addr(&sh.pub_max, lane));
         sh.tops[lane] = t;
@@ -465,6 +468,9 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
     unsigned long long c[kFCluster], wv[kFCluster];
 #pragma unroll
     for (int r = 0; r < kFCluster; ++r) {
+      c[r] = 0ull;
+      wv[r] = 0ull;
+      if (r >= ncl) continue;
       int lb = threadIdx.x;
       if (anchored) {   // this CTA's bin at global bin threadIdx.x, or none
         const float d = top - sh.tops[r];
@@ -559,13 +565,13 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
   }
   cluster_sync_all();
   if (threadIdx.x < 32) {
-    int c = lane < kFCluster ? ld_dsmem_s32(dsmem_addr(&sh.cnt1, lane)) : 0;
+    int c = lane < ncl ? ld_dsmem_s32(dsmem_addr(&sh.cnt1, lane)) : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int u = __shfl_up_sync(FULL, c, o);
       if (lane >= o) c += u;
     }
-    if (lane < kFCluster) sh.off[lane + 1] = c;
+    if (lane < ncl) sh.off[lane + 1] = c;
     if (lane == 0) sh.off[0] = 0;
   }
   __syncthreads();
@@ -656,7 +662,7 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 // out = x = logit / T where kept, -inf elsewhere; selection on the raw logits
 // (the scale by 1/T keeps their order).  Dynamic shared memory: the slice, the
 // level-1 and level-2 lists, the scratch area.
-__global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
+__global__ void __launch_bounds__(kFThreads)
     filter_kernel(const float* logits, float* out, int V, int slice, float inv_t, int top_k, float top_p,
                   float log_min_p, const int32_t* status) {
   __shared__ FilterShared sh;
@@ -704,7 +710,8 @@ __global__ void __cluster_dims__(kFCluster, 1, 1) __launch_bounds__(kFThreads)
   } else {
     cluster_sync_all();
     if (threadIdx.x < 32) {
-      float m = threadIdx.x < kFCluster ? ld_dsmem_f32(dsmem_addr(&sh.pub_max, threadIdx.x)) : -INFINITY;
+      float m = (int)threadIdx.x < (int)cluster_nctarank() ? ld_dsmem_f32(dsmem_addr(&sh.pub_max, threadIdx.x))
+                                                             : -INFINITY;
       m = warp_max(m);
       if (threadIdx.x == 0) sh.M = m;
     }
@@ -898,24 +905,66 @@ std::atomic<bool> g_filter_smem_set[64];
 
 // tokens per CTA of a row's cluster (a multiple of 8, so the index array that
 // follows the slice stays 16-byte aligned)
-int filter_slice(int vocab) { return ((vocab + kFCluster - 1) / kFCluster + 7) / 8 * 8; }
-size_t filter_smem(int vocab) {
-  return (size_t)filter_slice(vocab) * sizeof(float) + 2 * kCandCap * sizeof(uint16_t) + kFScratch;
+int filter_slice(int vocab, int ncl) { return ((vocab + ncl - 1) / ncl + 7) / 8 * 8; }
+size_t filter_smem(int vocab, int ncl) {
+  return (size_t)filter_slice(vocab, ncl) * sizeof(float) + 2 * kCandCap * sizeof(uint16_t) + kFScratch;
+}
+// dynamic shared memory that leaves room for one CTA an SM only
+constexpr size_t kFOnePerSm = 110 * 1024;
+std::atomic<int> g_filter_fit[64][2];   // clusters of 8 / of 6 active at once at one CTA an SM (0: unknown)
+
+int filter_fit(int dev, int ncl) {
+  std::atomic<int>& slot = g_filter_fit[dev][ncl == 8 ? 0 : 1];
+  int n = slot.load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)ncl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(ncl, 1, 1);
+  cfg.blockDim = dim3(kFThreads, 1, 1);
+  cfg.dynamicSmemBytes = kFOnePerSm;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)filter_kernel, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = 1;
+  }
+  slot.store(n, std::memory_order_relaxed);
+  return n;
 }
 
 }  // namespace
 
+// One cluster per row.  The rows' clusters run side by side when each CTA has
+// an SM of its own: clusters of 8 when that many fit the GPU's partition into
+// clusters, else of 6 (more clusters fit; a third more tokens a CTA), padding
+// the shared memory to one CTA an SM; beyond that clusters of 8 share SMs.
 int launch_filter(const float* logits, float* out, int rows, int vocab, float temperature, int top_k, float top_p,
                   float min_p, int32_t* status, cudaStream_t st) {
   if (vocab > kFilterMaxVocab) return TV_E_UNSUPPORTED;
   const float inv_t = (float)(1.0 / (double)temperature);
   const float log_min_p = min_p > 0.f ? (float)std::log((double)min_p) : -INFINITY;
-  const int slice = filter_slice(vocab);
   // the limit is raised once per device, to what the largest vocabulary needs
-  const int rc = ensure_smem_limit(filter_kernel, filter_smem(kFilterMaxVocab), g_filter_smem_set);
+  const size_t max_smem = filter_smem(kFilterMaxVocab, 6);
+  int rc = ensure_smem_limit(filter_kernel, max_smem, g_filter_smem_set);
   if (rc) return rc;
-  return launch_pdl(filter_kernel, dim3(kFCluster, rows), dim3(kFThreads), filter_smem(vocab), st, logits, out, vocab, slice,
-                    inv_t, top_k, top_p, log_min_p, (const int32_t*)status);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TV_E_CUDA;
+  int ncl = kFCluster;
+  size_t smem = filter_smem(vocab, kFCluster);
+  if (rows <= filter_fit(dev, 8)) {
+    smem = smem > kFOnePerSm ? smem : kFOnePerSm;
+  } else if (rows <= filter_fit(dev, 6)) {
+    ncl = 6;
+    smem = filter_smem(vocab, 6);
+    smem = smem > kFOnePerSm ? smem : kFOnePerSm;
+  }
+  const int slice = filter_slice(vocab, ncl);
+  return launch_pdl_cluster(filter_kernel, dim3(ncl, rows), dim3(kFThreads), smem, st, ncl, logits, out, vocab, slice,
+                            inv_t, top_k, top_p, log_min_p, (const int32_t*)status);
 }
 
 int launch_gumbel_rows(const ReqTable& t, const float* logits, int vocab, float temperature, const SeedTable& sd,
