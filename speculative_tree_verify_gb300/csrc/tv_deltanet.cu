@@ -121,19 +121,33 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo
 template <int NMAX>
 __device__ __forceinline__ void dn_substitute_warp(const float* RHS, const float* CA, float* U, float* u_out,
                                                    size_t row_stride, int n, int lane) {
+  constexpr int NQ = NMAX / 4;
   float ur[NMAX];
+  float4 cur[NQ], nxt[NQ];
+  float rcur = RHS[lane], rnxt = 0.f;
 #pragma unroll
   for (int tt = 0; tt < NMAX; ++tt) {
-    float a0 = RHS[tt * kDnRowF + lane], a1 = 0.f;
+    // the next row's coefficients and right-hand side, asked for before this
+    // row's FMAs (software pipelining: their latency hides behind them)
+    if (tt + 1 < NMAX) {
+#pragma unroll
+      for (int q4 = 0; q4 < NQ; ++q4)
+        if (4 * q4 < tt + 1) nxt[q4] = *reinterpret_cast<const float4*>(CA + (tt + 1) * kDnRowF + 4 * q4);
+      rnxt = RHS[(tt + 1) * kDnRowF + lane];
+    }
+    float a0 = rcur, a1 = 0.f;
 #pragma unroll
     for (int s4 = 0; s4 < tt; s4 += 4) {
-      const float4 c4 = *reinterpret_cast<const float4*>(CA + tt * kDnRowF + s4);
+      const float4 c4 = cur[s4 / 4];
       a0 = fmaf(-c4.x, ur[s4], a0);
       if (s4 + 1 < tt) a1 = fmaf(-c4.y, ur[s4 + 1], a1);
       if (s4 + 2 < tt) a0 = fmaf(-c4.z, ur[s4 + 2], a0);
       if (s4 + 3 < tt) a1 = fmaf(-c4.w, ur[s4 + 3], a1);
     }
     ur[tt] = a0 + a1;
+#pragma unroll
+    for (int q4 = 0; q4 < NQ; ++q4) cur[q4] = nxt[q4];
+    rcur = rnxt;
   }
 #pragma unroll
   for (int tt = 0; tt < NMAX; ++tt) {
@@ -141,6 +155,27 @@ __device__ __forceinline__ void dn_substitute_warp(const float* RHS, const float
       U[tt * kDnCols + lane] = ur[tt];
       u_out[tt * row_stride + lane] = ur[tt];
     }
+  }
+}
+
+// o_t = exp(gc_t) S0^T q_t + sum_{s <= t} C[t][s] u_s for the rows t = warp,
+// warp + 16, ... below n; the s loop unrolled to NMAX (C is zero off the path)
+template <int NMAX>
+__device__ __forceinline__ void dn_outputs(const float* EQS, const float* CC, const float* U, float* o_out,
+                                           size_t row_stride, int n, int warp, int lane) {
+  for (int r2 = warp; r2 < n; r2 += kDnWarps) {
+    float a0 = EQS[r2 * kDnRowF + lane], a1 = 0.f;
+#pragma unroll
+    for (int s4 = 0; s4 < NMAX; s4 += 4) {
+      if (s4 <= r2) {
+        const float4 c4 = *reinterpret_cast<const float4*>(CC + r2 * kDnRowF + s4);
+        a0 = fmaf(c4.x, U[s4 * kDnCols + lane], a0);
+        if (s4 + 1 <= r2) a1 = fmaf(c4.y, U[(s4 + 1) * kDnCols + lane], a1);
+        if (s4 + 2 <= r2) a0 = fmaf(c4.z, U[(s4 + 2) * kDnCols + lane], a0);
+        if (s4 + 3 <= r2) a1 = fmaf(c4.w, U[(s4 + 3) * kDnCols + lane], a1);
+      }
+    }
+    o_out[(size_t)r2 * row_stride + lane] = a0 + a1;
   }
 }
 
@@ -427,16 +462,10 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
       }
       __syncthreads();
       // (5) o_t = exp(gc_t) S0^T q_t + sum_{s <= t} C[t][s] u_s
-      for (int r2 = warp; r2 < n; r2 += kDnWarps) {
-        float a0 = EQS[r2 * kDnRowF + lane], a1 = 0.f;
-        for (int s4 = 0; s4 <= r2; s4 += 4) {
-          const float4 c4 = *reinterpret_cast<const float4*>(CC + r2 * kDnRowF + s4);
-          a0 = fmaf(c4.x, U[s4 * kDnCols + lane], a0);
-          if (s4 + 1 <= r2) a1 = fmaf(c4.y, U[(s4 + 1) * kDnCols + lane], a1);
-          if (s4 + 2 <= r2) a0 = fmaf(c4.z, U[(s4 + 2) * kDnCols + lane], a0);
-          if (s4 + 3 <= r2) a1 = fmaf(c4.w, U[(s4 + 3) * kDnCols + lane], a1);
-        }
-        o[((size_t)(row0 + r2) * Hv + h) * dv + c0 + lane] = a0 + a1;
+      {
+        float* oo = o + ((size_t)row0 * Hv + h) * dv + c0;
+        if (n <= 16) dn_outputs<16>(EQS, CC, U, oo, (size_t)Hv * dv, n, warp, lane);
+        else dn_outputs<kMaxRows>(EQS, CC, U, oo, (size_t)Hv * dv, n, warp, lane);
       }
       if (cb == 0 && threadIdx.x < n) gc_out[(size_t)(row0 + threadIdx.x) * Hv + h] = s_gc[threadIdx.x];
     }
