@@ -41,6 +41,7 @@ constexpr int kFPriv = 4;               // private level-1 histograms per CTA (w
 constexpr int kCandCap = 4096;          // tokens a CTA lists per level; past that it rescans its slice
 constexpr int kGatherMax = 512;         // last bins this small (cluster-wide) are finished by ranking
 constexpr int kFScratch = kFPriv * 2 * kFBins * 4;   // bytes: private histograms, or the gathered tokens
+constexpr int kFRegF4 = 16;             // float4s of its slice a thread also keeps in registers (the fast cut's passes)
 static_assert(kGatherMax * 12 <= kFScratch, "gathered keys and weights fit the scratch area");
 
 // order-preserving key: larger float -> larger unsigned; -0 and +0 share a
@@ -377,9 +378,9 @@ __device__ __forceinline__ void boundary_bin(FilterShared& sh, const unsigned lo
   __syncthreads();
 }
 
-__device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsigned char* region, int n_loc,
-                         float& M, float m_loc, float inv_t, int top_k, float top_p, bool by_k, float log_min_p,
-                         float* orow) {
+__device__ bool fast_cut(FilterShared& sh, const float* xs, const float4 (&xr)[kFRegF4], bool inreg,
+                         uint16_t* cand, unsigned char* region, int n_loc, float& M, float m_loc, float inv_t,
+                         int top_k, float top_p, bool by_k, float log_min_p, float* orow) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ncl = (int)cluster_nctarank();
   // top_p alone: bins of (M - x) / T * 8 under the cluster maximum M.  top_k:
@@ -390,8 +391,20 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
   const bool anchored = by_k;
   const float s8 = inv_t * kFBinsPerUnit;
   const float top_loc = floorf(m_loc * s8);
+  // the grid index g(x) = floor(x / T * 8) as an integer (saturating; every
+  // anchor is below 2^23 in magnitude when the cut goes on, so a token at or
+  // below the maximum never saturates upward and one saturated downward lands
+  // in bin 255 / is never listed, as it would be in float)
+  auto grid = [&](float x) { return __float2int_rd(x * s8); };
+  const int top_loc_i = (fabsf(top_loc) < 8388608.f) ? (int)top_loc : 0;
   auto bin_of = [&](float x) { return (int)fminf((M - x) * inv_t * kFBinsPerUnit, (float)(kFBins - 1)); };
-  auto lbin = [&](float x) { return anchored ? (int)fminf(top_loc - floorf(x * s8), (float)(kFBins - 1)) : bin_of(x); };
+  auto lbin = [&](float x) {
+    return anchored ? (int)min((uint32_t)top_loc_i - (uint32_t)grid(x), (uint32_t)(kFBins - 1)) : bin_of(x);
+  };
+  // the float4s of the slice: [0, kFThreads kFRegF4) from registers when inreg
+  // (NaN past the slice), the rest from shared memory
+  const int n4 = n_loc >> 2;
+  const int j_smem = inreg ? kFThreads * kFRegF4 : 0;
   auto wt = [&](float x) { return (unsigned long long)__float2ull_rn(expf((x - M) * inv_t) * 4294967296.f); };
   // level 1 into private histograms: counts; weights as hi * 2^16 + lo
   uint32_t* pc = reinterpret_cast<uint32_t*>(region);            // [kFPriv][kFBins]
@@ -406,7 +419,7 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
     uint32_t* myc = pc + (warp & (kFPriv - 1)) * kFBins;
     uint32_t* myw = pw + (warp & (kFPriv - 1)) * 2 * kFBins;
     auto one = [&](float x) {
-      if (fkey(x) >= 1u) {
+      if (x == x) {   // NaN is never counted
         const int b = lbin(x);
         atomicAdd(&myc[b], 1u);
         if (!by_k) {
@@ -417,8 +430,16 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
         }
       }
     };
-    const int n4 = n_loc >> 2;
-    for (int j = threadIdx.x; j < n4; j += kFThreads) {
+    if (inreg) {
+#pragma unroll
+      for (int r = 0; r < kFRegF4; ++r) {
+        one(xr[r].x);
+        one(xr[r].y);
+        one(xr[r].z);
+        one(xr[r].w);
+      }
+    }
+    for (int j = j_smem + threadIdx.x; j < n4; j += kFThreads) {
       const float4 x4 = reinterpret_cast<const float4*>(xs)[j];
       one(x4.x);
       one(x4.y);
@@ -517,8 +538,8 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
   // candidates are written again at the end, after a CTA barrier)
   float* cx = reinterpret_cast<float*>(region + kFPriv * 3 * kFBins * sizeof(uint32_t));   // past the histograms
   {
-    const float gmin = top - (float)B;   // anchored: bins <= B are g(x) >= top - B
-    auto in = [&](float x) { return fkey(x) >= 1u && (anchored ? floorf(x * s8) >= gmin : bin_of(x) <= B); };
+    const int gmin = (int)top - B;   // anchored: bins <= B are g(x) >= top - B (top an integer below 2^23)
+    auto in = [&](float x) { return x == x && (anchored ? grid(x) >= gmin : bin_of(x) <= B); };
     auto put = [&](bool ok, int i, float x) {
       const unsigned mk = __ballot_sync(FULL, ok);
       if (mk == 0u) return;
@@ -532,21 +553,38 @@ __device__ bool fast_cut(FilterShared& sh, const float* xs, uint16_t* cand, unsi
       }
     };
     const bool vec_out = (reinterpret_cast<uintptr_t>(orow) & 15u) == 0;
-    const int n4 = n_loc >> 2;
     const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    for (int j0 = warp * 32; j0 < n4; j0 += kFThreads) {   // warp-uniform trip count
+    auto clear4 = [&](int j) {
+      if (vec_out) {
+        reinterpret_cast<float4*>(orow)[j] = ninf;
+      } else {
+        orow[4 * j] = -INFINITY;
+        orow[4 * j + 1] = -INFINITY;
+        orow[4 * j + 2] = -INFINITY;
+        orow[4 * j + 3] = -INFINITY;
+      }
+    };
+    if (inreg) {
+#pragma unroll
+      for (int r = 0; r < kFRegF4; ++r) {   // every lane of the warp takes every step
+        const int j = (int)threadIdx.x + kFThreads * r;
+        if (j < n4) clear4(j);
+        const float4 x4 = xr[r];
+        const bool a0 = in(x4.x), a1 = in(x4.y), a2 = in(x4.z), a3 = in(x4.w);
+        if (__any_sync(FULL, a0 || a1 || a2 || a3)) {
+          put(a0, 4 * j, x4.x);
+          put(a1, 4 * j + 1, x4.y);
+          put(a2, 4 * j + 2, x4.z);
+          put(a3, 4 * j + 3, x4.w);
+        }
+      }
+    }
+    for (int j0 = j_smem + warp * 32; j0 < n4; j0 += kFThreads) {   // warp-uniform trip count
       const int j = j0 + lane;
       float4 x4 = make_float4(NAN, NAN, NAN, NAN);
       if (j < n4) {
         x4 = reinterpret_cast<const float4*>(xs)[j];
-        if (vec_out) {
-          reinterpret_cast<float4*>(orow)[j] = ninf;
-        } else {
-          orow[4 * j] = -INFINITY;
-          orow[4 * j + 1] = -INFINITY;
-          orow[4 * j + 2] = -INFINITY;
-          orow[4 * j + 3] = -INFINITY;
-        }
+        clear4(j);
       }
       const bool a0 = in(x4.x), a1 = in(x4.y), a2 = in(x4.z), a3 = in(x4.w);
       if (__any_sync(FULL, a0 || a1 || a2 || a3)) {
@@ -686,7 +724,21 @@ __global__ void __launch_bounds__(kFThreads)
   // multiple of 8 tokens), the tail one by one
   const bool vec_in = (reinterpret_cast<uintptr_t>(lr) & 15u) == 0;
   const int n4 = vec_in ? n_loc >> 2 : 0;
-  for (int j = threadIdx.x; j < n4; j += kFThreads) {
+  // the first kFThreads kFRegF4 float4s are kept in registers too (NaN past
+  // the slice), for the fast cut's passes
+  float4 xr[kFRegF4];
+#pragma unroll
+  for (int r = 0; r < kFRegF4; ++r) {
+    const int j = (int)threadIdx.x + kFThreads * r;
+    xr[r] = make_float4(NAN, NAN, NAN, NAN);
+    if (j < n4) {
+      const float4 v = reinterpret_cast<const float4*>(lr)[j];
+      xr[r] = v;
+      reinterpret_cast<float4*>(xs)[j] = v;
+      mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
+    }
+  }
+  for (int j = kFThreads * kFRegF4 + threadIdx.x; j < n4; j += kFThreads) {
     const float4 v = reinterpret_cast<const float4*>(lr)[j];
     reinterpret_cast<float4*>(xs)[j] = v;
     mx = fmaxf(fmaxf(mx, fmaxf(v.x, v.y)), fmaxf(v.z, v.w));
@@ -704,7 +756,7 @@ __global__ void __launch_bounds__(kFThreads)
   float M = -INFINITY;
   unsigned char* region = reinterpret_cast<unsigned char*>(cand2);
   if (by_k) {   // the fast top_k cut reads the cluster maximum with its histograms
-    if (fast_cut(sh, xs, cand1, region, n_loc, M, mx, inv_t, top_k, top_p, true, log_min_p, orow))
+    if (fast_cut(sh, xs, xr, vec_in, cand1, region, n_loc, M, mx, inv_t, top_k, top_p, true, log_min_p, orow))
       return;   // outputs written, and the cluster's reads of this CTA done
     cluster_sync_all();   // every CTA has read the fast cut's shared memory
   } else {
@@ -718,7 +770,8 @@ __global__ void __launch_bounds__(kFThreads)
     __syncthreads();
     M = sh.M;
     if (M != -INFINITY && top_p < 1.f) {
-      if (fast_cut(sh, xs, cand1, region, n_loc, M, mx, inv_t, top_k, top_p, false, log_min_p, orow)) return;
+      if (fast_cut(sh, xs, xr, vec_in, cand1, region, n_loc, M, mx, inv_t, top_k, top_p, false, log_min_p, orow))
+        return;
       cluster_sync_all();
     }
   }
