@@ -80,9 +80,9 @@ struct DnVerifyLayout {
   static constexpr int B_SLAB = 128 * 128;        // of B (2 NB <= 128 rows)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + 2 * A_SLAB;
-  static constexpr int OFF_Y = OFF_B + 2 * B_SLAB;                   // [128][68]: D, hi + lo columns added
-  static constexpr int Y_F = 68;
-  static constexpr int OFF_RHS = OFF_Y + 128 * Y_F * 4;              // [32][36] beta_t (v_t - exp(gc_t) S0^T k_t)
+  static constexpr int OFF_Y = 0;                                    // [128][68]: D, hi + lo columns added
+  static constexpr int Y_F = 68;                                     // (over A and B, free once the MMAs are done)
+  static constexpr int OFF_RHS = OFF_B + 2 * B_SLAB;                 // [32][36] beta_t (v_t - exp(gc_t) S0^T k_t)
   static constexpr int OFF_EQS = OFF_RHS + kMaxRows * 36 * 4;        // [32][36] exp(gc_t) S0^T q_t
   static constexpr int OFF_CA = OFF_EQS + kMaxRows * 36 * 4;         // [32][36] A: strict ancestors
   static constexpr int OFF_CC = OFF_CA + kMaxRows * 36 * 4;          // [32][36] C: the path, t included
@@ -90,6 +90,8 @@ struct DnVerifyLayout {
   static constexpr int OFF_U = OFF_V + kMaxRows * kDnCols * 4;       // [32][32] pseudo-values
   static constexpr int BYTES = OFF_U + kMaxRows * kDnCols * 4;
   static constexpr size_t ALLOC = 1024 + BYTES;
+  static_assert(OFF_Y + 128 * Y_F * 4 <= OFF_RHS, "D's staging fits over the operands");
+  static_assert(2 * (ALLOC + 1024) <= 227 * 1024, "two CTAs an SM");
 };
 constexpr int kDnRowF = 36;
 constexpr uint32_t kDnTmemCols = 128;
@@ -98,6 +100,27 @@ constexpr int kDnStageThreads = 32 * kDnStageWarps;
 constexpr int kDnTasks = 5;   // staging tasks a thread: 16-byte chunks of 8 coordinates (2048 at most)
 
 __device__ __forceinline__ uint32_t bf16x2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// 32 lanes x 16 consecutive 32-bit TMEM columns (this thread's lane)
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// y[0..16) = hi + lo of 16 columns
+__device__ __forceinline__ void add16(float* y, const uint32_t (&a)[16], const uint32_t (&b)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    reinterpret_cast<float4*>(y)[j] =
+        make_float4(__uint_as_float(a[4 * j]) + __uint_as_float(b[4 * j]),
+                    __uint_as_float(a[4 * j + 1]) + __uint_as_float(b[4 * j + 1]),
+                    __uint_as_float(a[4 * j + 2]) + __uint_as_float(b[4 * j + 2]),
+                    __uint_as_float(a[4 * j + 3]) + __uint_as_float(b[4 * j + 3]));
+}
 
 // hi and lo bf16 planes of 8 consecutive coordinates
 __device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
@@ -185,7 +208,7 @@ __device__ __forceinline__ void dn_outputs(const float* EQS, const float* CC, co
 // coefficients, the right-hand sides and the triangular solve follow in fp32
 // on the CUDA cores.  Warps 0..13 stage the operands, warp 14 computes the
 // cumulative gates and root paths, warp 15 checks the tree.
-__global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
+__global__ void __launch_bounds__(kDnThreads, 2) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
                                                                const float* q, const float* k, const float* v,
                                                                const float* beta, const float* g, float* o, float* u,
                                                                float* gc_out, int32_t* status, int state_early) {
@@ -395,39 +418,22 @@ __global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnSta
         const int sp = warp & 3;
         const uint32_t ta = tmem + ((uint32_t)(32 * sp) << 16);
         float* yr = Y + (32 * sp + lane) * L::Y_F;
-        uint32_t d0[32], d1[32];
-        if (warp < 4) {
-          tmem_ld_32x32b_x32(ta, d0);             // S0 columns x hi
-          tmem_ld_32x32b_x32(ta + kDnCols, d1);   // x lo
-          tmem_ld_wait();
+        uint32_t d0[16], d1[16];   // 16 columns a load (two CTAs share the SM's registers)
+        if (warp < 4) {   // S0 columns: hi at 0.., lo at kDnCols..
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            reinterpret_cast<float4*>(yr)[j] = make_float4(
-                __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]),
-                __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]),
-                __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]),
-                __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]));
-        } else {
+          for (int hf = 0; hf < 2; ++hf) {
+            tmem_ld_x16(ta + 16 * hf, d0);
+            tmem_ld_x16(ta + kDnCols + 16 * hf, d1);
+            tmem_ld_wait();
+            add16(yr + 16 * hf, d0, d1);
+          }
+        } else {          // tree-node columns: hi at 0.., lo at NK..
           const uint32_t tn = ta + 2 * kDnCols;
-          tmem_ld_32x32b_x32(tn, d0);   // NK = 16: hi 0..15, lo 16..31; NK = 32: hi
-          if (NK == 32) tmem_ld_32x32b_x32(tn + 32, d1);   // lo
-          tmem_ld_wait();
-          if (NK == 16) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              reinterpret_cast<float4*>(yr + kDnCols)[j] = make_float4(
-                  __uint_as_float(d0[4 * j]) + __uint_as_float(d0[16 + 4 * j]),
-                  __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d0[16 + 4 * j + 1]),
-                  __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d0[16 + 4 * j + 2]),
-                  __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d0[16 + 4 * j + 3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              reinterpret_cast<float4*>(yr + kDnCols)[j] = make_float4(
-                  __uint_as_float(d0[4 * j]) + __uint_as_float(d1[4 * j]),
-                  __uint_as_float(d0[4 * j + 1]) + __uint_as_float(d1[4 * j + 1]),
-                  __uint_as_float(d0[4 * j + 2]) + __uint_as_float(d1[4 * j + 2]),
-                  __uint_as_float(d0[4 * j + 3]) + __uint_as_float(d1[4 * j + 3]));
+          for (int hf = 0; hf < NK / 16; ++hf) {
+            tmem_ld_x16(tn + 16 * hf, d0);
+            tmem_ld_x16(tn + NK + 16 * hf, d1);
+            tmem_ld_wait();
+            add16(yr + kDnCols + 16 * hf, d0, d1);
           }
         }
       }

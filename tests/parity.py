@@ -173,11 +173,15 @@ def check_verify(model, host_reqs, dm=None, reqs_b=None):
              "swapped": check_argmax(logits, to_np(b.argmax), to_np(b.gap)),
              "attn_err": check_close_bf16(np.concatenate([o["attn"] for o in orc]), to_np(b.attn), ATTN_TOL, "attn")}
     Hkv = model.dims.n_kv_heads
+    stats["kv_err"] = 0.0
     for (c, t), o, r in zip(host_reqs, orc, reqs):
         ctx, n = c.ctx_len, t.n
         k, v = to_np(r.k), to_np(r.v)
-        check_close_bf16(o["k"], k[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree K", relative=True)
-        check_close_bf16(o["v"], v[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree V", relative=True)
+        ek = check_close_bf16(o["k"], k[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree K",
+                              relative=True)
+        ev = check_close_bf16(o["v"], v[:, ctx:ctx + n, :].transpose(1, 0, 2).reshape(n, -1), KV_TOL, "tree V",
+                              relative=True)
+        stats["kv_err"] = max(stats["kv_err"], ek, ev)
         np.testing.assert_array_equal(k[:, :ctx], c.k[:, :ctx])           # cached rows are only read
         np.testing.assert_array_equal(v[:, :ctx], c.v[:, :ctx])
         np.testing.assert_array_equal(k[:, ctx + n:], c.k[:, ctx + n:])   # nothing past the tree rows
