@@ -288,6 +288,11 @@ __global__ void __launch_bounds__(kDnThreads, 2) dn_verify_kernel(ReqTable t, Dn
   if (state_early) {
 #pragma unroll
     for (int m = 0; m < kDnTasks; ++m) load_task(m, true);
+  } else if ((int)threadIdx.x < dk) {
+    // otherwise the state's rows (128 bytes of this block's columns each) are
+    // only asked into L2, which every write reaches: whatever writes them
+    // before the wait, the loads after it read the written values
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(S0g + (size_t)threadIdx.x * dv) : "memory");
   }
   pdl_wait();
   pdl_trigger();
