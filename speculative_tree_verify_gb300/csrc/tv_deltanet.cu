@@ -91,7 +91,6 @@ struct DnVerifyLayout {
   static constexpr int BYTES = OFF_U + kMaxRows * kDnCols * 4;
   static constexpr size_t ALLOC = 1024 + BYTES;
   static_assert(OFF_Y + 128 * Y_F * 4 <= OFF_RHS, "D's staging fits over the operands");
-  static_assert(2 * (ALLOC + 1024) <= 227 * 1024, "two CTAs an SM");
 };
 constexpr int kDnRowF = 36;
 constexpr uint32_t kDnTmemCols = 128;
@@ -208,7 +207,7 @@ __device__ __forceinline__ void dn_outputs(const float* EQS, const float* CC, co
 // coefficients, the right-hand sides and the triangular solve follow in fp32
 // on the CUDA cores.  Warps 0..13 stage the operands, warp 14 computes the
 // cumulative gates and root paths, warp 15 checks the tree.
-__global__ void __launch_bounds__(kDnThreads, 2) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
+__global__ void __launch_bounds__(kDnThreads) dn_verify_kernel(ReqTable t, DnStates st, int Hk, int Hv, int dk, int dv,
                                                                const float* q, const float* k, const float* v,
                                                                const float* beta, const float* g, float* o, float* u,
                                                                float* gc_out, int32_t* status, int state_early) {
@@ -340,49 +339,55 @@ __global__ void __launch_bounds__(kDnThreads, 2) dn_verify_kernel(ReqTable t, Dn
       s_stat = status_get(status);
     }
   } else {
-#pragma unroll
-    for (int m = 0; m < kDnTasks; ++m) {
-      const int task = threadIdx.x + kDnStageThreads * m;
-      const bool is_state = task >= nA && task < nA + nS;
-      if (is_state) {
-        if (!state_early) load_task(m, true);
-      } else {
-        load_task(m, false);
-      }
-    }
     float4 vreg = make_float4(0.f, 0.f, 0.f, 0.f);
     const int vs = threadIdx.x >> 3, vc = threadIdx.x & 7;   // v[:, column block]: 32 nodes x 8 float4
     if (threadIdx.x < kMaxRows * kDnCols / 4 && vs < n)
       vreg = *reinterpret_cast<const float4*>(v + ((size_t)(row0 + vs) * Hv + h) * dv + c0 + 4 * vc);
-    // the operand planes (zeros for nodes past n and coordinates past d_k)
+    // two waves of tasks (0..2, then the rest: only trees past 16 nodes have
+    // them), each loaded, then split and stored
 #pragma unroll
-    for (int m = 0; m < kDnTasks; ++m) {
-      const int task = threadIdx.x + kDnStageThreads * m;
-      if (task >= nT) continue;
-      uint4 hi, lo;
-      split8(x[m], hi, lo);
-      if (task < nA) {
-        const int id = task >> kcs, j = task & (KC - 1);
-        const int row = ((id >> nks) << 5) | (id & (NK - 1));   // k node rows 0.., q node rows 32..
-        uint8_t* base = smem + L::OFF_A + (j >> 3) * L::A_SLAB;
-        *reinterpret_cast<uint4*>(base + swz(row, j & 7)) = hi;
-        *reinterpret_cast<uint4*>(base + swz(row + 64, j & 7)) = lo;
-      } else {
-        int row, row_lo, j;
-        if (task < nA + nS) {   // S0^T: hi rows 0..31, lo rows 32..63
-          const int id = task - nA;
-          row = id % kDnCols;
-          row_lo = kDnCols + row;
-          j = id / kDnCols;
-        } else {                // tree nodes: hi rows 64.., lo rows 64 + NK..
-          const int id = task - nA - nS;
-          row = 2 * kDnCols + (id >> kcs);
-          row_lo = row + NK;
-          j = id & (KC - 1);
+    for (int wv = 0; wv < 2; ++wv) {
+      const int m0 = wv == 0 ? 0 : 3, m1 = wv == 0 ? 3 : kDnTasks;
+#pragma unroll
+      for (int m = m0; m < m1; ++m) {
+        const int task = threadIdx.x + kDnStageThreads * m;
+        const bool is_state = task >= nA && task < nA + nS;
+        if (is_state) {
+          if (!state_early) load_task(m, true);
+        } else {
+          load_task(m, false);
         }
-        uint8_t* base = smem + L::OFF_B + (j >> 3) * L::B_SLAB;
-        *reinterpret_cast<uint4*>(base + swz(row, j & 7)) = hi;
-        *reinterpret_cast<uint4*>(base + swz(row_lo, j & 7)) = lo;
+      }
+      // the operand planes (zeros for nodes past n and coordinates past d_k)
+#pragma unroll
+      for (int m = m0; m < m1; ++m) {
+        const int task = threadIdx.x + kDnStageThreads * m;
+        if (task >= nT) continue;
+        uint4 hi, lo;
+        split8(x[m], hi, lo);
+        if (task < nA) {
+          const int id = task >> kcs, j = task & (KC - 1);
+          const int row = ((id >> nks) << 5) | (id & (NK - 1));   // k node rows 0.., q node rows 32..
+          uint8_t* base = smem + L::OFF_A + (j >> 3) * L::A_SLAB;
+          *reinterpret_cast<uint4*>(base + swz(row, j & 7)) = hi;
+          *reinterpret_cast<uint4*>(base + swz(row + 64, j & 7)) = lo;
+        } else {
+          int row, row_lo, j;
+          if (task < nA + nS) {   // S0^T: hi rows 0..31, lo rows 32..63
+            const int id = task - nA;
+            row = id % kDnCols;
+            row_lo = kDnCols + row;
+            j = id / kDnCols;
+          } else {                // tree nodes: hi rows 64.., lo rows 64 + NK..
+            const int id = task - nA - nS;
+            row = 2 * kDnCols + (id >> kcs);
+            row_lo = row + NK;
+            j = id & (KC - 1);
+          }
+          uint8_t* base = smem + L::OFF_B + (j >> 3) * L::B_SLAB;
+          *reinterpret_cast<uint4*>(base + swz(row, j & 7)) = hi;
+          *reinterpret_cast<uint4*>(base + swz(row_lo, j & 7)) = lo;
+        }
       }
     }
     if (threadIdx.x < kMaxRows * kDnCols / 4) reinterpret_cast<float4*>(VB)[threadIdx.x] = vreg;
