@@ -117,6 +117,15 @@ def test_filter_vocab_sizes(gpu, V):
     _filter_check(logits, 0.9, min(7, V - 1), 0.85, 0.01)
 
 
+@pytest.mark.parametrize("V", [151936, 262144])
+@pytest.mark.parametrize("T,k,p,mp", [(0.8, 50, 0.9, 0.02), (0.8, 0, 0.9, 0.0)])
+def test_filter_sixteen_rows(gpu, V, T, k, p, mp):
+    # 16 rows: the launch takes smaller clusters, so a CTA holds a longer slice
+    # (at 262144 past the part its threads keep in registers)
+    logits = synth.logits_rows(16, V, 90 + V % 13, scale=1.5)
+    _filter_check(logits, T, k, p, mp)
+
+
 def test_filter_ties_and_masked_rows(gpu):
     V = 20000
     rng = np.random.default_rng(3)
