@@ -223,6 +223,17 @@ def test_stack_tiny_joint_and_ragged_context(tiny):
     print("stack joint:", stats)
 
 
+def test_stack_32_rows_dk128(gpu):
+    # DeltaNet heads of 128 and a 32-row tree: the state loaded before the
+    # programmatic-launch wait lands in both staging waves of the verify core
+    sd = synth.StackDims(base=synth.MID, n_layers=4, attn_every=4, n_k_heads=2, n_v_heads=4, d_k=128, d_v=128,
+                         intermediate=1024)
+    m = synth.gen_stack(sd, 33, random_gains=True)
+    dm = dv.DeviceStack.from_host(m)
+    stats = run_and_check(m, dm, _host(sd, m, [96], [synth.tree_lattice(32, 15, sd.base.vocab, 13)], 800))
+    print("stack hidden 512, DeltaNet heads of 128, 32 rows:", stats)
+
+
 def test_stack_packed_equals_row_major(tiny):
     sd, m, dm = tiny
     assert dm.packed
