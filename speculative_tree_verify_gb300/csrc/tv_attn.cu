@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
 // and sum of chunks i and i + 32.  The row's chunk count follows from the
 // kernel parameters, so the partials are requested right after the wait, up
 // to kMergeBatch chunks at a time.
-constexpr int kMergeWarps = 8;
+constexpr int kMergeWarps = 2;
 constexpr int kMergeBatch = 20;
 static_assert(kChunkSlots <= 64, "a lane holds at most two chunks' offsets");
 
