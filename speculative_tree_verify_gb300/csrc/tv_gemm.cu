@@ -49,7 +49,8 @@ constexpr int EPI_STRIDE = 33;
 constexpr int kPartialStages = 8;
 constexpr size_t SMEM_BAR = 1024;
 constexpr size_t SMEM_EPI = 4 * 32 * EPI_STRIDE * sizeof(float);
-constexpr size_t SMEM_T2 = 4 * 32 * sizeof(Top2);
+constexpr int kMergeWarpsHead = THREADS / 32;   // the last head CTA merges with all its warps
+constexpr size_t SMEM_T2 = kMergeWarpsHead * 32 * sizeof(Top2);
 // Ring depth and shared memory by mode.  The head streams 1.5 GB with eight
 // 16 KB weight stages (six and ten were slower); the split-K GEMMs measured
 // the same with eight and eleven; they need no top-2 tables.
@@ -312,8 +313,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (MODE == GEMM_HEAD) {
     // this CTA's best per activation row goes out; the CTA that finishes last
-    // merges every CTA's with its four epilogue warps (CTAs ew, ew + 4, ...,
-    // sixteen 16-byte loads in flight a lane), then warp 2 merges the four.
+    // merges every CTA's with all six of its warps (warp w: CTAs w, w + 6, ...,
+    // every load in flight at once for a grid of up to 156), then warp 2
+    // merges the six.
     // The merge keeps the largest value and the lowest index among equal
     // ones, so its order does not change the result.
     __shared__ int s_last;
@@ -328,26 +330,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) s_last = prev == gridDim.x - 1;
     }
     __syncthreads();
-    if (s_last && warp >= 2) {
+    if (s_last) {
       __threadfence();
-      const unsigned ew = (unsigned)(warp - 2);
+      const unsigned ew = (unsigned)warp;
       Top2 g;
       g.m1 = -INFINITY;
       g.i1 = INT_MAX;
       g.m2 = -INFINITY;
       g.pad = 0;
-      constexpr int kBatch = 16;
-      for (unsigned c0 = ew; c0 < gridDim.x; c0 += 4 * kBatch) {
+      constexpr int kBatch = 26;
+      for (unsigned c0 = ew; c0 < gridDim.x; c0 += kMergeWarpsHead * kBatch) {
         int4 raw[kBatch];
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-          const unsigned c = c0 + 4u * (unsigned)i;
+          const unsigned c = c0 + (unsigned)(kMergeWarpsHead * i);
           raw[i] = c < gridDim.x ? __ldcg(reinterpret_cast<const int4*>(p.top2_part + (size_t)c * 32 + lane))
                                  : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
-          if (c0 + 4u * (unsigned)i < gridDim.x) {
+          if (c0 + (unsigned)(kMergeWarpsHead * i) < gridDim.x) {
             Top2 t;
             t.m1 = __int_as_float(raw[i].x);
             t.i1 = raw[i].y;
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     if (s_last && warp == 2) {
       Top2 g = t2s[lane];
-      for (int e = 1; e < 4; ++e) top2_merge(g, t2s[e * 32 + lane]);
+      for (int e = 1; e < kMergeWarpsHead; ++e) top2_merge(g, t2s[e * 32 + lane]);
       if (lane < p.n_rows) {
         p.argmax[lane] = g.i1;
         p.gap[lane] = g.m1 - g.m2;
